@@ -1,0 +1,529 @@
+"""Pins for the fp64 oracle (CPU only).
+
+Each check ties an oracle function to something other than itself: a library
+routine (torch's float8/bfloat16 casts, torch.nn.functional.rms_norm, numpy
+complex multiplication, torch integer matmul, torch.round), a closed form
+(one-hot / permutation projections, power-of-two scales), an invariant of the
+method (RoPE inverse and norm preservation), values fixed by hand in
+``tests/golden/hand_values.txt``, or brute force over a tiny scatter.
+
+The ``check_*`` helpers raise AssertionError on a mismatch; ``test_mutants``
+plants plausible mistakes in the oracle (sign flips, transposed operands,
+wrong widths, dropped terms) and confirms that some check catches each one.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import codes, kv_cache as okv, qkv_cte as oq
+from rope_attention_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F64 = torch.float64
+
+
+def torch_e4m3(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.uint8)).view(torch.float8_e4m3fn).to(F64).numpy()
+
+
+def torch_bf16(b):
+    return torch.from_numpy(np.ascontiguousarray(b, np.uint16).view(np.int16)).view(torch.bfloat16).to(F64).numpy()
+
+
+def finite_e4m3_codes(rng, shape):
+    c = rng.integers(0, 256, shape).astype(np.uint8)
+    return np.where((c & 0x7F) == 0x7F, np.uint8(0x38), c)
+
+
+def assert_close(got, exp, rtol=1e-12, atol=1e-12):
+    np.testing.assert_allclose(np.asarray(got, np.float64), np.asarray(exp, np.float64), rtol=rtol, atol=atol)
+
+
+# ---------------------------------------------------------------------------
+# code decoders
+# ---------------------------------------------------------------------------
+def check_decoders():
+    allc = np.arange(256, dtype=np.uint8)
+    got, exp = codes.decode_e4m3(allc), torch_e4m3(allc)
+    assert np.array_equal(np.isnan(got), np.isnan(exp))
+    assert np.array_equal(got[~np.isnan(got)], exp[~np.isnan(exp)])
+    got = codes.decode_ue8m0(allc)
+    exp = torch.from_numpy(allc).view(torch.float8_e8m0fnu).to(F64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(exp))
+    assert np.array_equal(got[~np.isnan(got)], exp[~np.isnan(exp)])
+    bits = np.random.default_rng(7).integers(0, 65536, 4096).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]  # finite patterns
+    assert np.array_equal(codes.decode_bf16(bits), torch_bf16(bits))
+
+
+def test_decoders_match_torch_casts():
+    check_decoders()
+
+
+def test_e4m3_spec_points():
+    # OCP FP8 E4M3: 0x38 = 1.0, 0x7E = 448 (max), 0x08 = 2^-6 (min normal), 0x01 = 2^-9, 0xB8 = -1
+    v = codes.decode_e4m3(np.array([0x38, 0x7E, 0x08, 0x01, 0xB8, 0x00, 0x80], np.uint8))
+    assert list(v) == [1.0, 448.0, 2.0 ** -6, 2.0 ** -9, -1.0, 0.0, 0.0]
+    assert np.isnan(codes.decode_e4m3(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+# ---------------------------------------------------------------------------
+# projection
+# ---------------------------------------------------------------------------
+def check_projection_permutation():
+    """W is a non-symmetric permutation: O[t, pi(h)] = A_hat[t, h]."""
+    rng = np.random.default_rng(1)
+    T, H = 6, 64
+    a = finite_e4m3_codes(rng, (T, H))
+    a_scale = np.exp2(rng.integers(-3, 4, T)).astype(np.float32)
+    pi = (np.arange(H) * 5 + 3) % H
+    w = np.zeros((H, H), np.uint8)
+    w[np.arange(H), pi] = 0x38
+    w_exp = np.full((H // 32, H), 127, np.uint8)
+    got = oq.project(a, a_scale, w, w_exp)
+    exp = np.zeros((T, H))
+    exp[:, pi] = torch_e4m3(a) * a_scale[:, None]
+    assert_close(got, exp, 0, 0)
+
+
+def check_projection_block_scales():
+    """One-hot rows pick W_hat's row h; the block scale of row h is e[h // 32, i]."""
+    rng = np.random.default_rng(2)
+    H, I = 96, 40
+    hs = np.array([0, 31, 32, 63, 64, 95, 17, 70])
+    a = np.zeros((len(hs), H), np.uint8)
+    a[np.arange(len(hs)), hs] = 0x38
+    w = np.full((H, I), 0x38, np.uint8)
+    w_exp = rng.integers(120, 135, (H // 32, I)).astype(np.uint8)
+    ws = rng.uniform(0.5, 2.0, I).astype(np.float32)
+    got = oq.project(a, np.ones(len(hs), np.float32), w, w_exp, weight_scales=ws)
+    exp = np.exp2(w_exp[hs // 32, :].astype(np.float64) - 127) * ws.astype(np.float64)[None, :]
+    assert_close(got, exp, 0, 0)
+
+
+def check_projection_integer_exact():
+    """Small integer codes, unit scales: the product is an exact integer matmul."""
+    rng = np.random.default_rng(3)
+    T, H, I = 9, 64, 48
+    table = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48}
+    ai = rng.integers(-4, 5, (T, H))
+    wi = rng.integers(-4, 5, (H, I))
+    enc = lambda m: np.vectorize(lambda v: table[abs(v)] | (0x80 if v < 0 else 0))(m).astype(np.uint8)
+    bias_bits = synth.encode_bf16(rng.integers(-8, 9, I).astype(np.float32))
+    got = oq.project(enc(ai), np.ones(T, np.float32), enc(wi), np.full((H // 32, I), 127, np.uint8),
+                     bias=bias_bits)
+    exp = (torch.from_numpy(ai) @ torch.from_numpy(wi)).numpy() + torch_bf16(bias_bits)[None, :]
+    assert_close(got, exp, 0, 0)
+
+
+def check_projection_scaling():
+    """Row scales and channel scales factor out; zero activations give the bias."""
+    rng = np.random.default_rng(4)
+    T, H, I = 5, 64, 32
+    a = finite_e4m3_codes(rng, (T, H))
+    w = finite_e4m3_codes(rng, (H, I))
+    e = rng.integers(118, 136, (H // 32, I)).astype(np.uint8)
+    base = oq.project(a, np.ones(T, np.float32), w, e)
+    k = rng.integers(-4, 5, T)
+    c = np.exp2(rng.integers(-3, 4, I)).astype(np.float32)
+    got = oq.project(a, np.exp2(k).astype(np.float32), w, e, weight_scales=c)
+    assert_close(got, base * np.exp2(k)[:, None] * c[None, :], 0, 0)
+    bias = synth.encode_bf16(rng.normal(0, 1, I).astype(np.float32))
+    z = oq.project(np.zeros((T, H), np.uint8), np.ones(T, np.float32), w, e, bias=bias)
+    assert_close(z, np.broadcast_to(torch_bf16(bias), (T, I)), 0, 0)
+
+
+@pytest.mark.parametrize("check", [check_projection_permutation, check_projection_block_scales,
+                                   check_projection_integer_exact, check_projection_scaling])
+def test_projection(check):
+    check()
+
+
+# ---------------------------------------------------------------------------
+# across-heads RMSNorm + rotate-half RoPE
+# ---------------------------------------------------------------------------
+def read_hand_values():
+    rows = []
+    with open(os.path.join(GOLDEN, "hand_values.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            lhs, rhs = line.split("|")
+            kind, *args = lhs.split()
+            rows.append((kind, [float(x) for x in args], [float(x) for x in rhs.split()]))
+    return rows
+
+
+def check_rmsnorm_hand():
+    for kind, args, out in read_hand_values():
+        if kind == "rmsnorm":
+            x = np.array([args])
+            assert_close(oq.rms_norm_across_heads(x, np.ones(2), 0.0), [out], 1e-15, 0)
+            assert_close(okv.rms_norm(x, np.ones(2), 0.0), [out], 1e-15, 0)
+
+
+def test_rmsnorm_hand_value():
+    check_rmsnorm_hand()
+
+
+def complex_rope_rotate_half(y, theta, d):
+    """Rotate-half pairs (j, j+d/2) as complex numbers y_j + i*y_{j+d/2} times the unit
+    number ``theta`` (an angle array, or complex cos + i*sin values)."""
+    T = y.shape[0]
+    yh = y.reshape(T, -1, d)
+    rot = theta if np.iscomplexobj(theta) else np.exp(1j * theta)
+    z = (yh[..., : d // 2] + 1j * yh[..., d // 2:]) * rot[:, None, :]
+    return np.concatenate([z.real, z.imag], axis=-1).reshape(T, -1)
+
+
+def complex_rope_interleaved(x, theta):
+    """Interleaved pairs (2j, 2j+1) as complex numbers, output de-interleaved (reals first)."""
+    z = (x[..., 0::2] + 1j * x[..., 1::2]) * np.exp(1j * theta)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def identity_qkv(nq, nkv, d, T, seed, rope):
+    """A case whose projection is known without the oracle: H = I, W = identity, unit scales."""
+    rng = np.random.default_rng(seed)
+    I = (nq + 2 * nkv) * d
+    a = finite_e4m3_codes(rng, (T, I))
+    a_scale = np.exp2(rng.integers(-2, 3, T)).astype(np.float32)
+    w = np.zeros((I, I), np.uint8)
+    w[np.arange(I), np.arange(I)] = 0x38
+    e = np.full((I // 32, I), 127, np.uint8)
+    bias = synth.encode_bf16(rng.normal(0, 0.5, I).astype(np.float32))
+    qg = rng.uniform(0.5, 1.5, nq * d).astype(np.float32)
+    kg = rng.uniform(0.5, 1.5, nkv * d).astype(np.float32) if nkv else None
+    theta = rng.uniform(-np.pi, np.pi, (T, d // 2))
+    cos = np.concatenate([np.cos(theta)] * 2, axis=1).astype(np.float32)
+    sin = np.concatenate([np.sin(theta)] * 2, axis=1).astype(np.float32)
+    # the fp32 tables are not exactly unit-modulus: rotate by the complex number cos + i*sin
+    theta = cos[:, : d // 2].astype(np.float64) + 1j * sin[:, : d // 2].astype(np.float64)
+    o = torch_e4m3(a) * a_scale[:, None] + torch_bf16(bias)[None, :]
+    kw = dict(num_heads=nq, num_kv_heads=nkv, head_dim=d, bias=bias, q_gamma=qg, k_gamma=kg,
+              eps=1e-6, fused_rope=rope, cos=cos if rope else None, sin=sin if rope else None)
+    return a, a_scale, w, e, kw, o, theta, (cos, sin)
+
+
+def torch_rms(x, g, eps):
+    return F.rms_norm(torch.from_numpy(x), (x.shape[1],), torch.from_numpy(np.asarray(g, np.float64)), eps).numpy()
+
+
+def check_qkv_norm_segments():
+    """No RoPE: Q and K are F.rms_norm over their own widths (n_q != n_kv), V is O."""
+    nq, nkv, d = 3, 2, 32
+    a, s, w, e, kw, o, _, _ = identity_qkv(nq, nkv, d, 7, 5, rope=False)
+    got = oq.qkv_cte_mx(a, s, w, e, **kw)
+    qw, kwid = nq * d, nkv * d
+    assert_close(got[:, :qw], torch_rms(o[:, :qw], kw["q_gamma"], 1e-6), 1e-12, 1e-13)
+    assert_close(got[:, qw:qw + kwid], torch_rms(o[:, qw:qw + kwid], kw["k_gamma"], 1e-6), 1e-12, 1e-13)
+    assert_close(got[:, qw + kwid:], o[:, qw + kwid:], 0, 0)
+
+
+def check_qkv_single_segment():
+    """num_kv_heads = 0: the whole width is normed as Q."""
+    a, s, w, e, kw, o, _, _ = identity_qkv(4, 0, 32, 5, 6, rope=False)
+    got = oq.qkv_cte_mx(a, s, w, e, **kw)
+    assert_close(got, torch_rms(o, kw["q_gamma"], 1e-6), 1e-12, 1e-13)
+
+
+def check_qkv_norm_then_rope():
+    """With RoPE: complex rotation of F.rms_norm(segment) (gamma before rotation); V untouched."""
+    nq, nkv, d = 2, 3, 64
+    a, s, w, e, kw, o, theta, _ = identity_qkv(nq, nkv, d, 6, 7, rope=True)
+    got = oq.qkv_cte_mx(a, s, w, e, **kw)
+    qw, kwid = nq * d, nkv * d
+    exp_q = complex_rope_rotate_half(torch_rms(o[:, :qw], kw["q_gamma"], 1e-6), theta, d)
+    exp_k = complex_rope_rotate_half(torch_rms(o[:, qw:qw + kwid], kw["k_gamma"], 1e-6), theta, d)
+    assert_close(got[:, :qw], exp_q, 1e-9, 1e-12)
+    assert_close(got[:, qw:qw + kwid], exp_k, 1e-9, 1e-12)
+    assert_close(got[:, qw + kwid:], o[:, qw + kwid:], 0, 0)
+
+
+def check_rotate_half_invariants():
+    rng = np.random.default_rng(8)
+    T, n, d = 5, 3, 16
+    y = rng.normal(0, 1, (T, n * d))
+    theta = rng.uniform(-3, 3, (T, d // 2))
+    cos = np.concatenate([np.cos(theta)] * 2, axis=1)
+    sin = np.concatenate([np.sin(theta)] * 2, axis=1)
+    r = oq.rope_rotate_half(y, cos, sin, d)
+    assert_close(r, complex_rope_rotate_half(y, theta, d), 1e-12, 1e-14)
+    assert_close(oq.rope_rotate_half(r, cos, -sin, d), y, 1e-12, 1e-14)          # inverse
+    assert_close(oq.rope_rotate_half(y, np.ones_like(cos), np.zeros_like(sin), d), y, 0, 0)
+    yh, rh = y.reshape(T, n, d), r.reshape(T, n, d)                              # pair norms
+    assert_close(np.hypot(rh[..., : d // 2], rh[..., d // 2:]), np.hypot(yh[..., : d // 2], yh[..., d // 2:]), 1e-12, 1e-14)
+
+
+@pytest.mark.parametrize("check", [check_qkv_norm_segments, check_qkv_single_segment,
+                                   check_qkv_norm_then_rope, check_rotate_half_invariants])
+def test_qkv(check):
+    check()
+
+
+# ---------------------------------------------------------------------------
+# KvRmsNormRopeCache
+# ---------------------------------------------------------------------------
+def check_interleave_rope():
+    rng = np.random.default_rng(9)
+    R = 16
+    x = rng.normal(0, 1, (4, 3, R))
+    theta = rng.uniform(-3, 3, (4, 3, R // 2))
+    cos = np.concatenate([np.cos(theta)] * 2, axis=-1)
+    sin = np.concatenate([np.sin(theta)] * 2, axis=-1)
+    r = okv.interleave_rope(x, cos, sin)
+    assert_close(r, complex_rope_interleaved(x, theta), 1e-12, 1e-14)
+    # the interleaved form equals rotate-half applied to the de-interleaved vector
+    deint = np.concatenate([x[..., 0::2], x[..., 1::2]], axis=-1)
+    assert_close(r.reshape(12, R), oq.rope_rotate_half(deint.reshape(12, R), cos.reshape(12, R), sin.reshape(12, R), R), 1e-12, 1e-14)
+    # inverse: rotate-half with -sin on the output, then re-interleave
+    back = oq.rope_rotate_half(r.reshape(12, R), cos.reshape(12, R), -sin.reshape(12, R), R).reshape(4, 3, R)
+    re = np.empty_like(x)
+    re[..., 0::2], re[..., 1::2] = back[..., : R // 2], back[..., R // 2:]
+    assert_close(re, x, 1e-12, 1e-14)
+    # position 0 (cos 1, sin 0) is the de-interleave permutation
+    assert_close(okv.interleave_rope(x, np.ones_like(cos), np.zeros_like(sin)), deint, 0, 0)
+
+
+def check_quant_hand():
+    for kind, args, out in read_hand_values():
+        if kind == "quant":
+            x, sc, of = args
+            q, pre = okv.quantize(np.array([x]), np.array([sc]), np.array([of]), False)
+            assert int(q[0]) == int(out[0]), (x, sc, of, q)
+            t = torch.round(torch.tensor([x * sc + of], dtype=F64)).clamp(-128, 127)
+            assert int(t[0]) == int(out[0])
+
+
+def tiny_kv(variant, cache_mode="PA_BNSD", quant=False, seed=11):
+    if variant == 1:
+        kw = dict(B=2, N=1, S=5, Dkv=24, Dv=16, rope_size=8)
+    else:
+        kw = dict(B=2, N=2, S=5, Dkv=24, Dv=16, rope_size=8)
+    case = synth.make_kv("tiny", seed, variant=variant, block_size=4, block_num=4,
+                         cache_mode=cache_mode, quant_k=quant, quant_v=quant, skip_frac=0.3, **kw)
+    case.index[1] = -1
+    return case
+
+
+def run_kv(case):
+    return okv.kv_rms_norm_rope_cache(
+        case.kv, case.gamma, case.cos, case.sin, case.index, case.k_cache, case.ckv_cache,
+        variant=case.variant, rope_size=case.rope_size, block_size=case.block_size,
+        cache_mode=case.cache_mode, epsilon=case.eps, k_scale=case.k_scale, k_offset=case.k_offset,
+        v_scale=case.v_scale, v_offset=case.v_offset, v=case.v, is_output_kv=True)
+
+
+def expected_kv_rows(case):
+    """Per (b, n, s) rows built from library routines: F.rms_norm, complex rotation, torch.round."""
+    x = torch_bf16(case.kv)
+    B, N, S, Dkv = x.shape
+    R = case.rope_size
+    rms = case.rms_size
+    g = torch.from_numpy(torch_bf16(case.gamma))
+    y = F.rms_norm(torch.from_numpy(x[..., :rms].copy()), (rms,), g, case.eps).numpy()
+    cos, sin = torch_bf16(case.cos), torch_bf16(case.sin)
+    theta = np.arctan2(sin[..., : R // 2], cos[..., : R // 2])
+    radius = np.hypot(sin[..., : R // 2], cos[..., : R // 2])  # bf16 tables are not exactly unit
+    def rot(v):
+        z = (v[..., 0::2] + 1j * v[..., 1::2]) * radius * np.exp(1j * theta)
+        return np.concatenate([z.real, z.imag], axis=-1)
+    if case.variant == 1:
+        k_rows, c_rows = rot(x[..., rms:]), y
+    else:
+        k_rows, c_rows = np.concatenate([rot(y[..., :R]), y[..., R:]], axis=-1), torch_bf16(case.v)
+
+    def q(v, sc, of):
+        if sc is None:
+            return v, None
+        sc = sc if case.variant == 1 else sc[None, :, None, :]
+        pre = torch.from_numpy(v) * torch.from_numpy(np.asarray(sc, np.float64))
+        if of is not None:
+            of = of if case.variant == 1 else of[None, :, None, :]
+            pre = pre + torch.from_numpy(np.asarray(of, np.float64))
+        return torch.round(pre).clamp(-128, 127).numpy(), pre.numpy()
+
+    kq, kpre = q(k_rows, case.k_scale, case.k_offset)
+    cq, cpre = q(c_rows, case.v_scale, case.v_offset)
+    return k_rows, c_rows, kq, kpre, cq, cpre
+
+
+def check_kv_op(variant, cache_mode, quant):
+    case = tiny_kv(variant, cache_mode, quant)
+    res = run_kv(case)
+    k_rows, c_rows, kq, kpre, cq, cpre = expected_kv_rows(case)
+    B, N, S = case.B, case.N, case.S
+    assert_close(res["k_rope"], k_rows, 1e-12, 1e-12)
+    assert_close(res["c_kv"], c_rows, 1e-12, 1e-12)
+    k_exp = torch_bf16(case.k_cache) if not quant else case.k_cache.astype(np.float64)
+    c_exp = torch_bf16(case.ckv_cache) if not quant else case.ckv_cache.astype(np.float64)
+    k_exp, c_exp = k_exp.copy(), c_exp.copy()
+    kp_exp = np.full(k_exp.shape, np.nan)
+    cp_exp = np.full(c_exp.shape, np.nan)
+    seen = set()
+    for b in range(B):                       # brute-force scatter
+        for s in range(S):
+            p = int(case.index[b * S + s])
+            if p == -1:
+                continue
+            assert p not in seen
+            seen.add(p)
+            blk, off = divmod(p, case.block_size)
+            for n in range(N):
+                kr = kq[b, n, s] if quant else k_rows[b, n, s]
+                cr = cq[b, n, s] if quant else c_rows[b, n, s]
+                at = (blk, n, off) if cache_mode == "PA_BNSD" else (blk, off, n)
+                k_exp[at], c_exp[at] = kr, cr
+                if quant:
+                    kp_exp[at], cp_exp[at] = kpre[b, n, s], cpre[b, n, s]
+    assert_close(res["k_cache"], k_exp, 1e-12, 1e-12)
+    assert_close(res["ckv_cache"], c_exp, 1e-12, 1e-12)
+    assert res["k_written"].sum() == len(seen) * N * case.k_width
+    if quant:
+        assert_close(res["k_pre"], kp_exp, 1e-12, 1e-12)
+        assert_close(res["ckv_pre"], cp_exp, 1e-12, 1e-12)
+
+
+def check_kv_v1_bf16():
+    check_kv_op(1, "PA_BNSD", False)
+
+
+def check_kv_v1_int8():
+    check_kv_op(1, "PA_BNSD", True)
+
+
+def check_kv_v2_int8():
+    check_kv_op(2, "PA_BNSD", True)
+
+
+def check_kv_v2_pa_bf16():
+    check_kv_op(2, "PA", False)
+
+
+def check_kv_bad_index():
+    case = tiny_kv(2, "PA_BNSD", False)
+    case.index[0] = case.block_num * case.block_size  # out of range: counted, not written
+    case.index[2] = -5
+    res = run_kv(case)
+    assert res["bad_index"] == 2
+    valid = np.count_nonzero(case.index >= 0) - 1
+    assert res["k_written"].sum() == valid * case.N * case.k_width
+
+
+@pytest.mark.parametrize("check", [check_interleave_rope, check_quant_hand, check_kv_v1_bf16,
+                                   check_kv_v1_int8, check_kv_v2_int8, check_kv_v2_pa_bf16,
+                                   check_kv_bad_index])
+def test_kv(check):
+    check()
+
+
+# ---------------------------------------------------------------------------
+# generator fixtures fixed by the pages
+# ---------------------------------------------------------------------------
+def test_wan_seq_len_golden():
+    with open(os.path.join(GOLDEN, "wan_seq_len.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            fr, h, w, lf, ph, pw, st = map(int, line.split())
+            assert synth.wan_latent_grid(fr, h, w) == (lf, ph, pw)
+            assert lf * ph * pw == st
+
+
+def test_generator_encodings():
+    """Row scale bounds every code to |x| <= 448; MX exponents keep blocks in range."""
+    c = synth.qkv_tiny()
+    a_hat = torch_e4m3(c.a)
+    assert np.nanmax(np.abs(a_hat)) <= 448 and not np.isnan(a_hat).any()
+    assert np.allclose(np.max(np.abs(a_hat), axis=1), 448, rtol=0.07)
+    w_hat = torch_e4m3(c.w)
+    assert not np.isnan(w_hat).any() and np.max(np.abs(w_hat)) <= 448
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: every mutant must be caught by at least one check
+# ---------------------------------------------------------------------------
+ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_block_scales,
+              check_projection_integer_exact, check_projection_scaling, check_rmsnorm_hand,
+              check_qkv_norm_segments, check_qkv_single_segment, check_qkv_norm_then_rope,
+              check_rotate_half_invariants, check_interleave_rope, check_quant_hand,
+              check_kv_v1_bf16, check_kv_v1_int8, check_kv_v2_int8, check_kv_v2_pa_bf16,
+              check_kv_bad_index]
+
+
+def mutants():
+    orig_rh = oq.rope_rotate_half
+    orig_norm = oq.rms_norm_across_heads
+    orig_dw = oq.dequant_weight
+    orig_il = okv.interleave_rope
+    orig_q = okv.quantize
+    orig_e4 = codes.decode_e4m3
+    orig_kvn = okv.rms_norm
+
+    def rh_sign(y, cos, sin, d):            # sin sign flipped
+        return orig_rh(y, cos, -sin, d)
+
+    def norm_no_eps(x, g, eps):             # eps dropped
+        return orig_norm(x, g, 0.0)
+
+    def norm_pre_gamma_width(x, g, eps):    # divide by the wrong width
+        return orig_norm(x, g, eps) * np.sqrt(x.shape[1] / (x.shape[1] + 32))
+
+    def dw_transposed_blocks(w, e, ws=None):  # block index taken along I instead of H
+        H, I = w.shape
+        ee = np.repeat(e, 32, axis=0)[:H]
+        ee = np.roll(ee, 1, axis=1)
+        return orig_e4(w) * np.exp2(ee.astype(np.float64) - 127) * (1 if ws is None else ws[None, :])
+
+    def il_no_deinterleave(x, cos, sin):    # output left interleaved
+        r = orig_il(x, cos, sin)
+        out = np.empty_like(r)
+        h = r.shape[-1] // 2
+        out[..., 0::2], out[..., 1::2] = r[..., :h], r[..., h:]
+        return out
+
+    def q_half_away(x, sc, of, nax):        # rounding half away from zero
+        v, pre = orig_q(x, sc, of, nax)
+        if pre is None:
+            return v, pre
+        return np.clip(np.sign(pre) * np.floor(np.abs(pre) + 0.5), -128, 127).astype(np.int64), pre
+
+    def q_offset_after_round(x, sc, of, nax):
+        v, pre = orig_q(x, sc, None, nax)
+        if pre is None or of is None:
+            return v, pre
+        o = np.asarray(of, np.float64)
+        o = o[None, :, None, :] if nax else o
+        return np.clip(v + np.rint(o), -128, 127).astype(np.int64), pre
+
+    def e4m3_bias8(c):                      # exponent bias 8 instead of 7
+        return orig_e4(c) * 0.5
+
+    def kvn_mean_over_all(x, g, eps):       # RMS over the whole last dim + 1
+        n = x.shape[-1] + 1
+        rms = np.sqrt(np.sum(x * x, axis=-1, keepdims=True) / n + eps)
+        return x / rms * g
+
+    return [(oq, "rope_rotate_half", rh_sign), (oq, "rms_norm_across_heads", norm_no_eps),
+            (oq, "rms_norm_across_heads", norm_pre_gamma_width), (oq, "dequant_weight", dw_transposed_blocks),
+            (okv, "interleave_rope", il_no_deinterleave), (okv, "quantize", q_half_away),
+            (okv, "quantize", q_offset_after_round), (codes, "decode_e4m3", e4m3_bias8),
+            (okv, "rms_norm", kvn_mean_over_all)]
+
+
+@pytest.mark.parametrize("i", range(len(mutants())))
+def test_mutants(i, monkeypatch):
+    mod, name, fn = mutants()[i]
+    monkeypatch.setattr(mod, name, fn)
+    if mod is codes:  # decode_e4m3 is also bound by name in qkv_cte
+        monkeypatch.setattr(oq, name, fn)
+    caught = []
+    for check in ALL_CHECKS:
+        try:
+            check()
+        except (AssertionError, ValueError):
+            caught.append(check.__name__)
+    assert caught, f"mutant {name}/{fn.__name__} survived every check"
