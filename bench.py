@@ -1,0 +1,366 @@
+"""Benchmark of the attention-prologue hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  K1 qkv_cte_mx_project   (block-scaled FP8 GEMM + dequant + bias + sums of squares)
+  K2 qkv_cte_mx_norm_rope (across-heads RMSNorm + rotate-half RoPE, in place)
+  K3 kv_rms_norm_rope_cache (RMSNorm + interleaved RoPE + int8 quant + paged scatter)
+on the Wan2.2-A14B 720p self-attention projection (S=75600 = 21x45x80, H=5120,
+40+40+40 heads of 128, I=15360, MXFP8 weights, 3-D RoPE) together with the
+separate-k/v KvRmsNormRopeCache call (kv [8,8,4096,192], v [8,8,4096,128],
+int8 per-head quantisation, PA_BNSD block_size=128).
+
+Prints one JSON line (rank 0).  ``value`` is the QKV GEMM work of a step
+divided by the device time of the whole step (TFLOP/s); per-kernel times,
+throughputs and roofline fractions are in ``passes``.  ``--impl reference``
+times the fp64 CPU oracle on a bounded sample of the same workload instead.
+Multi-GPU (torchrun): every rank runs its own copy of the workload (tokens are
+independent at tp=1, so the work shards with no data-path collective); value
+is the sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "QKV GEMM TFLOP/s (% FP8 peak); norm/RoPE/scatter GB/s (% HBM) at 1 GB300"
+FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor ratio (4.5 : 2.25 PFLOP/s)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def workload(name: str):
+    from rope_attention_gb300 import synth
+    if name == "wan720":
+        return synth.qkv_wan720(), synth.kv_sep_v2(is_output_kv=False)
+    if name == "wan480":
+        return synth.qkv_wan480(), synth.kv_mla_v1(quant=True)
+    if name == "small":
+        return (synth.make_qkv("small", 9, S=4096, H=1024, num_heads=8, num_kv_heads=8, head_dim=128),
+                synth.make_kv("small", 9, variant=2, B=2, N=8, S=1024, Dkv=192, Dv=128,
+                              block_size=128, quant_k=True, quant_v=True, is_output_kv=False))
+    raise SystemExit(f"unknown workload {name}")
+
+
+def qkv_bytes_k2(c) -> int:
+    """Algorithmic bytes of the norm/RoPE pass: Q|K read + write, cos/sin, gammas, sums."""
+    qk = c.T * (c.num_heads + c.num_kv_heads) * c.head_dim * 2
+    b = 2 * qk
+    if c.fused_rope:
+        b += 2 * c.T * c.head_dim * 4
+    b += 4 * (c.num_heads + c.num_kv_heads) * c.head_dim
+    b += c.T * 2 * 4
+    return b
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = [s for s in sm if mx and s >= 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch
+    from rope_attention_gb300 import build, native, runner
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    native.load()
+    peaks = load_peaks()
+    qcase, kcase = workload(args.workload)
+    q = runner.QkvRun(qcase)
+    k = runner.KvRun(kcase)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def step():
+        q.project()
+        q.norm_rope()
+        k.run()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert q.status() == 0, "projection pipeline reported a wait timeout"
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            q.project()
+            ev[i][1].record(stream)
+            q.norm_rope()
+            ev[i][2].record(stream)
+            k.run()
+            ev[i][3].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(end)
+    k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    k3 = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    if ws > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / K
+    flops = qcase.flops
+    k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    k1_tf = flops / (k1_ms * 1e-3) / 1e12
+    k2_bytes = qkv_bytes_k2(qcase)
+    k3_bytes = kcase.algorithmic_bytes()
+    k2_gbs = k2_bytes / (k2_ms * 1e-3) / 1e9
+    k3_gbs = k3_bytes / (k3_ms * 1e-3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    value = ws * flops / (ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(q, k, qcase, kcase, args, ws)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3-mx/bf16/int8", "data": "synthetic",
+        "config": {"workload": f"{qcase.name} (S={qcase.S}, H={qcase.H}, I={qcase.I}) + {kcase.name} "
+                               f"(kv [{kcase.B},{kcase.N},{kcase.S},{kcase.Dkv}])",
+                   "global_batch": ws * qcase.T, "seq_len": qcase.S, "parallelism": f"replica x{ws}",
+                   "l2": "inputs larger than L2 (each step streams > 3 GB)"},
+        "roofline": {"bound": "tensor", "achieved": round(k1_tf, 1), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(k1_tf / fp8_peak, 4), "traffic": None,
+                     "peak_note": "FP8 = 2 x measured sustained bf16 cuBLAS (MEASURED_PEAKS.json)"
+                     if peaks["source"] == "measured" else "FP8 = 2 x fallback bf16"},
+        "passes": {
+            "qkv_project": {"ms": round(k1_ms, 4), "tflops": round(k1_tf, 1), "frac_fp8": round(k1_tf / fp8_peak, 4)},
+            "qk_norm_rope": {"ms": round(k2_ms, 4), "bytes": k2_bytes, "gbs": round(k2_gbs, 1),
+                             "frac_hbm": round(k2_gbs / hbm, 4)},
+            "kv_rms_norm_rope_cache": {"ms": round(k3_ms, 4), "bytes": k3_bytes, "gbs": round(k3_gbs, 1),
+                                       "frac_hbm": round(k3_gbs / hbm, 4)},
+        },
+        "clocks": clk.summary(),
+        "gpu_launches": 3 * K,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(qcase, kcase, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(q, k, qcase, kcase, args, ws):
+    """Same step through the C-ABI with inputs copied from pinned host memory and the
+    results (projection output and both caches) copied back, inside the timed region."""
+    import torch
+    stream = torch.cuda.current_stream()
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    h_in = [(pin(t.cpu()), t) for t in (q.a, q.a_scale, q.cos, q.sin, k.kv, k.v, k.cos, k.sin, k.index)
+            if t is not None]
+    h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in (q.out, k.k_cache, k.ckv_cache)]
+    bi = sum(h.numel() * h.element_size() for h, _ in h_in)
+    bo = sum(h.numel() * h.element_size() for h, _ in h_out)
+
+    def step():
+        for h, d in h_in:
+            d.copy_(h, non_blocking=True)
+        q.project()
+        q.norm_rope()
+        k.run()
+        for h, d in h_out:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 5))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(K):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / K
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(ws * qcase.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def oracle_sample_time(qcase, kcase, q_rows: int, kv_batches: int):
+    """Wall time of the fp64 oracle on q_rows projection rows and kv_batches KV batches."""
+    import oracle
+    from rope_attention_gb300 import synth
+    rows = synth.sample_rows(qcase.T, seed=5, n_head=q_rows // 4, n_tail=q_rows // 4, n_rand=q_rows // 2)
+    c = qcase
+    t0 = time.perf_counter()
+    oracle.qkv_cte_mx(c.a[rows], c.a_scale[rows], c.w, c.w_block_exp, num_heads=c.num_heads,
+                      num_kv_heads=c.num_kv_heads, head_dim=c.head_dim, weight_scales=c.weight_scales,
+                      bias=c.bias, q_norm=c.q_norm, k_norm=c.k_norm, q_gamma=c.q_gamma,
+                      k_gamma=c.k_gamma, eps=c.eps, fused_rope=c.fused_rope,
+                      cos=None if c.cos is None else c.cos[rows], sin=None if c.sin is None else c.sin[rows])
+    t1 = time.perf_counter()
+    kc = kcase
+    nb = min(kv_batches, kc.B)
+    sl = slice(0, nb)
+    oracle.kv_rms_norm_rope_cache(
+        kc.kv[sl], kc.gamma, kc.cos[sl], kc.sin[sl], kc.index[: nb * kc.S], kc.k_cache, kc.ckv_cache,
+        variant=kc.variant, rope_size=kc.rope_size, block_size=kc.block_size, cache_mode=kc.cache_mode,
+        epsilon=kc.eps, k_scale=kc.k_scale, k_offset=kc.k_offset, v_scale=kc.v_scale,
+        v_offset=kc.v_offset, v=None if kc.v is None else kc.v[sl], is_output_kv=kc.is_output_kv)
+    t2 = time.perf_counter()
+    f_q = len(rows) / c.T
+    f_k = nb / kc.B
+    full_s = (t1 - t0) / f_q + (t2 - t1) / f_k
+    return full_s, len(rows), nb, t2 - t0
+
+
+def cpu_baseline(qcase, kcase, args):
+    full_s, nrows, nb, wall = oracle_sample_time(qcase, kcase, args.oracle_rows, 1)
+    return {"value": round(qcase.flops / full_s / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{nrows} of {qcase.T} projection rows (all {qcase.I} columns) + {nb} of {kcase.B} "
+                      f"KV batches, fp64 numpy, {wall:.1f} s wall; step time extrapolated linearly"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    qcase, kcase = workload(args.workload)
+    for _ in range(args.warmup):
+        oracle_sample_time(qcase, kcase, 64, 1)
+    times = []
+    info = None
+    for _ in range(args.steps):
+        full_s, nrows, nb, wall = oracle_sample_time(qcase, kcase, args.oracle_rows, 1)
+        times.append(full_s)
+        info = (nrows, nb, wall)
+    full_s = statistics.mean(times)
+    value = qcase.flops / full_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{qcase.name} (S={qcase.S}, H={qcase.H}, I={qcase.I}) + {kcase.name}",
+                   "global_batch": qcase.T, "seq_len": qcase.S, "parallelism": "cpu"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{info[0]} projection rows + {info[1]} KV batch per step, fp64 numpy; "
+                                   f"step time extrapolated to the full workload"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="wan720", choices=["wan720", "wan480", "small"])
+    ap.add_argument("--oracle-rows", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

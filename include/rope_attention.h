@@ -1,0 +1,207 @@
+/*
+ * rope_attention.h -- C ABI of librope_attention.so, the GB300 (sm_103a)
+ * attention-prologue hot path.
+ *
+ * Two operators:
+ *
+ *  (a) qkv_cte_mx: the fused QKV projection of the AWS Neuron page "Kernel
+ *      reference: qkv_cte -- Wan2.2 additions to the NKI Library QKV CTE MXFP8
+ *      projection" (sections "Applies to"/Pattern, "Upstream behavior",
+ *      Design 1 across-heads RMSNorm, Design 2 rotate-half RoPE, Design 5
+ *      single-segment calls, "Interface"):
+ *        O[T, I] = dequant(A[T, H]) @ dequant(W[H, I]) + bias,
+ *        I = (num_heads + 2*num_kv_heads) * head_dim, T = B*S,
+ *      then, per token, one RMS over the whole Q segment and one over the
+ *      whole K segment, the segment-wide gamma, and rotate-half RoPE on Q and
+ *      K, written back in place; V is left as projected.
+ *
+ *  (b) kv_rms_norm_rope_cache: the CANN ops-transformer operator
+ *      "KvRmsNormRopeCache" (formulas (1) RmsNorm, (2) interleaveRope,
+ *      (3) quantisation, (4) scatter, (5) is_output_kv; parameter table;
+ *      cache/index constraint table), modes V1 (combined kv) and V2
+ *      (separate kv with v_optional).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensor pointers are DEVICE pointers owned by the caller, dense and
+ *    row-major (last dimension contiguous) unless stated otherwise.  The hot
+ *    calls allocate nothing; scratch space is the caller's workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is asynchronous and stream-ordered; no call
+ *    synchronises except the *_status readers.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    rejected call returns a negative ra_status, launches nothing and sets
+ *    the thread-local message returned by ra_last_error().  RA_ERR_CUDA
+ *    means a CUDA runtime call failed (message carries cudaGetErrorString).
+ *  - Device-side conditions (a pipeline wait that ran out of time, an index
+ *    out of range) never trap: they are recorded in device memory that the
+ *    caller reads after synchronising (qkv_cte_mx_status, dev_error_count).
+ *  - bf16 values are passed as their 16-bit patterns (uint16_t).
+ */
+#ifndef ROPE_ATTENTION_H_
+#define ROPE_ATTENTION_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = -1,   /* bad shape, null pointer, illegal combination          */
+  RA_ERR_UNSUPPORTED = -2,   /* legal on the pages but not built here (e.g. NBSd)      */
+  RA_ERR_ALIGNMENT = -3,     /* pointer or stride violates a 16-byte alignment rule    */
+  RA_ERR_WORKSPACE = -4,     /* workspace / packed-weight buffer too small             */
+  RA_ERR_CUDA = -5,          /* a CUDA runtime call failed                             */
+  RA_ERR_TIMEOUT = -6,       /* a device pipeline wait gave up (see qkv_cte_mx_status) */
+  RA_ERR_INDEX = -7          /* reserved: index out of range reported by the host      */
+} ra_status;
+
+typedef enum { RA_BF16 = 0, RA_FP16 = 1, RA_INT8 = 2, RA_FP32 = 3 } ra_dtype;
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* ra_last_error(void);
+
+/* ABI version of this library (bumped on any signature change). */
+int32_t ra_abi_version(void);
+
+/* ========================================================================
+ * (a) qkv_cte_mx
+ * ======================================================================== */
+
+/* Norm selector, after NormType in the page's "Interface" (qk_norm_pre_rope). */
+enum { RA_NORM_NONE = 0, RA_NORM_RMS_ACROSS_HEADS = 1 };
+/* Output layout, after QKVOutputLayout ("Interface", output_layout). */
+enum { RA_LAYOUT_BSD = 0, RA_LAYOUT_NBSD = 1 };
+
+typedef struct {
+  int64_t B, S;           /* tokens T = B*S; rows of A and of the output             */
+  int64_t H;              /* contraction (hidden) size; multiple of 128              */
+  int32_t num_heads;      /* Q heads in this call                                     */
+  int32_t num_kv_heads;   /* K/V heads; 0 = single-segment call (Design 5)            */
+  int32_t head_dim;       /* d_head; multiple of 16                                  */
+  int32_t q_norm;         /* RA_NORM_* for the Q segment                              */
+  int32_t k_norm;         /* RA_NORM_* for the K segment; must be NONE when num_kv_heads == 0 */
+  int32_t fused_rope;     /* 1 = rotate-half RoPE on Q and K; needs cos/sin caches    */
+  float norm_eps;         /* epsilon inside the square root                           */
+  int32_t output_layout;  /* RA_LAYOUT_BSD only; RA_LAYOUT_NBSD -> RA_ERR_UNSUPPORTED  */
+} qkv_cte_mx_params;
+
+/* Size in bytes of the packed weight for an [H, I] MX weight. */
+ra_status qkv_cte_mx_packed_weight_bytes(int64_t H, int64_t I, size_t* bytes);
+
+/* One-time weight preparation (not part of the per-token path).
+ *   w            [H, I] FP8 E4M3 codes, row-major (the math layout of W).
+ *   w_block_exp  [H/32, I] UE8M0 exponents: W_hat[h, i] = e4m3(w[h, i]) * 2^(e[h/32, i]-127)
+ *                (MX block of 32 along H).
+ *   packed       device buffer of qkv_cte_mx_packed_weight_bytes(H, I) bytes,
+ *                16-byte aligned; receives an opaque K-major image of W and its
+ *                block scales for the projection kernel.
+ * Asynchronous on `stream`.  H % 128 == 0, I % 16 == 0, I <= 2^31-1. */
+ra_status qkv_cte_mx_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int64_t H, int64_t I,
+                                 void* packed, size_t packed_bytes, void* stream);
+
+/* Workspace bytes needed by qkv_cte_mx / qkv_cte_mx_project / qkv_cte_mx_norm_rope.
+ * The workspace holds a device status word and the per-token sum-of-squares
+ * partials.  Zero-fill it once after allocation; the calls keep it consistent. */
+ra_status qkv_cte_mx_workspace_bytes(const qkv_cte_mx_params* p, size_t* bytes);
+
+/* The whole prologue: projection (with the per-token sums of squares) followed
+ * by the across-heads norm + RoPE pass.
+ *   a             [T, H] FP8 E4M3 activation codes; 16-byte aligned rows (H % 16 == 0).
+ *   a_scale       [T] fp32 per-row dequant scale (the 4-byte tail of the
+ *                 page's row-packed [B, S, H+4] activation, passed separately).
+ *   w_packed      output of qkv_cte_mx_pack_weight for this H and I.
+ *   weight_scales [I] fp32 per-output-channel scale, or NULL (= 1).
+ *   bias          [I] bf16, or NULL.
+ *   cos_cache, sin_cache  [B, S, head_dim] fp32 rotate-half tables (lanes j and
+ *                 j + head_dim/2 pair up); required iff fused_rope.
+ *   q_gamma       [num_heads*head_dim] fp32 segment-wide gamma; required iff q_norm.
+ *   k_gamma       [num_kv_heads*head_dim] fp32; required iff k_norm.
+ *   out           [T, I] bf16 (BSD), 16-byte aligned.  Q|K|V along the last dim.
+ *   workspace     caller-owned, >= qkv_cte_mx_workspace_bytes, 16-byte aligned.
+ * Errors: validation codes above; RA_ERR_CUDA on launch failure.  A device
+ * wait timeout is reported by qkv_cte_mx_status. */
+ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
+                     const void* w_packed, const float* weight_scales, const uint16_t* bias,
+                     const float* cos_cache, const float* sin_cache, const float* q_gamma,
+                     const float* k_gamma, uint16_t* out, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* First half of qkv_cte_mx on its own: out = dequant(A) @ dequant(W) + bias in bf16,
+ * and the per-token Q / K sums of squares (Design 1a) into the workspace.
+ * With norms off and no RoPE this is the complete operator (e.g. the V-only call). */
+ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
+                             const void* w_packed, const float* weight_scales, const uint16_t* bias,
+                             uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Second half on its own (Design 1b-1c, Design 2): reads the sums of squares
+ * left in `workspace` by qkv_cte_mx_project for the same `out`, and applies
+ * inv_rms * gamma and RoPE to Q and K of `out` in place.  V is not touched.
+ * This is the seam where a tensor-parallel all-reduce of the sums would go. */
+ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cache,
+                               const float* sin_cache, const float* q_gamma, const float* k_gamma,
+                               uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads the workspace status word, clears it, and
+ * stores it in *device_status (0 = fine).  Returns RA_ERR_TIMEOUT if a
+ * projection wait gave up since the last read, else RA_OK. */
+ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_status);
+
+/* Test hook: time limit, in nanoseconds, of each device pipeline wait in the
+ * projection kernel (default 2e9).  Values < 1000 are raised to 1000. */
+void ra_set_wait_timeout_ns(int64_t ns);
+
+/* ========================================================================
+ * (b) kv_rms_norm_rope_cache
+ * ======================================================================== */
+
+/* cache_mode, from the page's constraint table.  PA = [block_num, block_size, N, D];
+ * PA_BNSD = [block_num, N, block_size, D]. */
+enum { RA_CACHE_PA = 1, RA_CACHE_PA_BNSD = 2 };
+
+typedef struct {
+  int64_t B, N, S;        /* kv is [B, N, S, Dkv]                                     */
+  int64_t Dkv;            /* last dim of kv                                           */
+  int64_t Dv;             /* V1: rms_size (= Dkv - rope_size); V2: last dim of v_optional */
+  int32_t rope_size;      /* RoPE width (64 in both of the page's modes); even        */
+  int32_t variant;        /* 1 = V1 combined kv (N == 1), 2 = V2 separate kv (N in 1,2,4,8) */
+  int32_t cache_mode;     /* RA_CACHE_PA or RA_CACHE_PA_BNSD                          */
+  int64_t block_num;      /* paged cache blocks                                       */
+  int64_t block_size;     /* slots per block; %16 (bf16 caches), %32 (int8 caches)    */
+  int32_t kv_dtype;       /* RA_BF16 (kv, gamma, cos, sin, v_optional share it)       */
+  int32_t k_cache_dtype;  /* RA_BF16, or RA_INT8 when k_rope_scale is given           */
+  int32_t ckv_cache_dtype;/* RA_BF16, or RA_INT8 when c_kv_scale is given             */
+  float epsilon;          /* RMSNorm epsilon (page default 1e-5)                      */
+  int32_t is_output_kv;   /* 1 = also write k_rope and c_kv                           */
+} kv_rms_norm_rope_cache_params;
+
+/* One call of KvRmsNormRopeCache.
+ *   kv          [B, N, S, Dkv] bf16.
+ *   gamma       [rms_size] bf16 (rms_size = Dkv - rope_size in V1, Dkv in V2).
+ *   cos, sin    [B, N, S, rope_size] bf16 (interleaved-RoPE tables).
+ *   index       [B*S] int64 slot per token; -1 = skip.  Slots must be unique.
+ *   k_cache     paged cache of width k_w = rope_size (V1) or Dkv (V2), updated in place.
+ *   ckv_cache   paged cache of width c_w = rms_size (V1) or Dv (V2), updated in place.
+ *   k_rope_scale / k_rope_offset  fp32 per channel: [k_w] (V1) or [N, k_w] (V2); NULL = absent.
+ *   c_kv_scale   / c_kv_offset    fp32 per channel: [c_w] (V1) or [N, c_w] (V2); NULL = absent.
+ *               An offset without its scale is rejected.
+ *   v_optional  [B, N, S, Dv] bf16; required in V2, must be NULL in V1.
+ *   k_rope      [B, N, S, k_w] bf16 and c_kv [B, N, S, c_w] bf16: written iff is_output_kv.
+ *   dev_error_count  optional int32 device counter: incremented once per token whose
+ *               index lies outside [-1, block_num*block_size); such tokens are not written.
+ * All row pointers 16-byte aligned; Dkv, Dv and rope_size multiples of 8. */
+ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const uint16_t* kv,
+                                 const uint16_t* gamma, const uint16_t* cos, const uint16_t* sin,
+                                 const int64_t* index, void* k_cache, void* ckv_cache,
+                                 const float* k_rope_scale, const float* c_kv_scale,
+                                 const float* k_rope_offset, const float* c_kv_offset,
+                                 const uint16_t* v_optional, uint16_t* k_rope, uint16_t* c_kv,
+                                 int32_t* dev_error_count, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ROPE_ATTENTION_H_ */

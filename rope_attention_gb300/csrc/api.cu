@@ -1,0 +1,394 @@
+// C-ABI entry points of librope_attention.so (declared in include/rope_attention.h).
+// Host-side validation happens here, before anything is launched.
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <string>
+
+#include "../../include/rope_attention.h"
+#include "internal.h"
+
+namespace ra {
+
+int device_sm_count() {
+  static std::atomic<int> cached{0};
+  int v = cached.load();
+  if (v > 0) return v;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  cached.store(n);
+  return n;
+}
+
+}  // namespace ra
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<int64_t> g_wait_ns{2000000000LL};
+
+ra_status fail(ra_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+ra_status fail(ra_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+ra_status ok() {
+  g_last_error.clear();
+  return RA_OK;
+}
+
+ra_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(RA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct QkvShape {
+  int64_t T, H, I;
+  int32_t q_w, k_w;
+  int32_t q_end, k_end;
+  int32_t n_part_tiles;
+  size_t workspace;
+};
+
+ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
+  if (p == nullptr) return fail(RA_ERR_INVALID_ARG, "params is NULL");
+  if (p->B < 1 || p->S < 1) return fail(RA_ERR_INVALID_ARG, "B and S must be >= 1 (no empty tensors)");
+  if (p->H < 128 || p->H % 128 != 0)
+    return fail(RA_ERR_INVALID_ARG, "H must be a positive multiple of 128 (got %lld)",
+                static_cast<long long>(p->H));
+  if (p->num_heads < 1) return fail(RA_ERR_INVALID_ARG, "num_heads must be >= 1");
+  if (p->num_kv_heads < 0) return fail(RA_ERR_INVALID_ARG, "num_kv_heads must be >= 0");
+  if (p->head_dim < 16 || p->head_dim % 16 != 0)
+    return fail(RA_ERR_INVALID_ARG, "head_dim must be a positive multiple of 16");
+  if (p->q_norm != RA_NORM_NONE && p->q_norm != RA_NORM_RMS_ACROSS_HEADS)
+    return fail(RA_ERR_INVALID_ARG, "q_norm must be RA_NORM_NONE or RA_NORM_RMS_ACROSS_HEADS");
+  if (p->k_norm != RA_NORM_NONE && p->k_norm != RA_NORM_RMS_ACROSS_HEADS)
+    return fail(RA_ERR_INVALID_ARG, "k_norm must be RA_NORM_NONE or RA_NORM_RMS_ACROSS_HEADS");
+  if (p->k_norm != RA_NORM_NONE && p->num_kv_heads == 0)
+    return fail(RA_ERR_INVALID_ARG, "k_norm needs a K segment (num_kv_heads == 0)");
+  if (p->fused_rope != 0 && p->fused_rope != 1) return fail(RA_ERR_INVALID_ARG, "fused_rope must be 0 or 1");
+  if (!(p->norm_eps >= 0.f) || !std::isfinite(p->norm_eps))
+    return fail(RA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  if (p->output_layout == RA_LAYOUT_NBSD)
+    return fail(RA_ERR_UNSUPPORTED, "output_layout NBSd is not built; use BSD");
+  if (p->output_layout != RA_LAYOUT_BSD) return fail(RA_ERR_INVALID_ARG, "unknown output_layout");
+  const int64_t T = p->B * p->S;
+  const int64_t I = static_cast<int64_t>(p->num_heads + 2 * p->num_kv_heads) * p->head_dim;
+  if (T > 0x7fffffffLL || I > 0x7fffffffLL || p->H > 0x7fffffffLL || T * I > (1LL << 40))
+    return fail(RA_ERR_INVALID_ARG, "problem too large for 32-bit tile coordinates");
+  s->T = T;
+  s->H = p->H;
+  s->I = I;
+  s->q_w = p->num_heads * p->head_dim;
+  s->k_w = p->num_kv_heads * p->head_dim;
+  s->q_end = s->q_w;
+  s->k_end = s->q_w + s->k_w;
+  const bool any_norm = p->q_norm != RA_NORM_NONE || p->k_norm != RA_NORM_NONE;
+  const int32_t normed_end = p->k_norm != RA_NORM_NONE ? s->k_end : s->q_end;
+  s->n_part_tiles = any_norm ? (normed_end + ra::kProjBN - 1) / ra::kProjBN : 0;
+  s->workspace = ra::kWorkspaceHeader + static_cast<size_t>(s->n_part_tiles) * T * sizeof(float2);
+  return RA_OK;
+}
+
+ra_status check_project_args(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
+                             const float* a_scale, const void* w_packed, const float* ws,
+                             const uint16_t* bias, const uint16_t* out, const void* workspace,
+                             size_t workspace_bytes) {
+  (void)p;
+  if (!a || !a_scale || !w_packed || !out || !workspace)
+    return fail(RA_ERR_INVALID_ARG, "a, a_scale, w_packed, out and workspace are required");
+  if (!aligned16(a) || !aligned16(out) || !aligned16(w_packed) || !aligned16(workspace))
+    return fail(RA_ERR_ALIGNMENT, "a, out, w_packed and workspace must be 16-byte aligned");
+  if ((ws && !aligned16(ws)) || (bias && !aligned16(bias)))
+    return fail(RA_ERR_ALIGNMENT, "weight_scales and bias must be 16-byte aligned");
+  if (workspace_bytes < s.workspace)
+    return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
+  return RA_OK;
+}
+
+ra_status check_norm_args(const qkv_cte_mx_params* p, const float* cos, const float* sin,
+                          const float* qg, const float* kg, const uint16_t* out,
+                          const void* workspace, size_t workspace_bytes, const QkvShape& s) {
+  if (!out || !workspace) return fail(RA_ERR_INVALID_ARG, "out and workspace are required");
+  if (!aligned16(out) || !aligned16(workspace))
+    return fail(RA_ERR_ALIGNMENT, "out and workspace must be 16-byte aligned");
+  if (p->fused_rope && (!cos || !sin))
+    return fail(RA_ERR_INVALID_ARG, "fused_rope requires cos_cache and sin_cache");
+  if (p->q_norm && !qg) return fail(RA_ERR_INVALID_ARG, "q_norm requires q_gamma");
+  if (p->k_norm && !kg) return fail(RA_ERR_INVALID_ARG, "k_norm requires k_gamma");
+  if ((cos && !aligned16(cos)) || (sin && !aligned16(sin)) || (qg && !aligned16(qg)) ||
+      (kg && !aligned16(kg)))
+    return fail(RA_ERR_ALIGNMENT, "cos/sin caches and gammas must be 16-byte aligned");
+  if (workspace_bytes < s.workspace)
+    return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
+  return RA_OK;
+}
+
+ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
+                      const float* a_scale, const void* w_packed, const float* ws,
+                      const uint16_t* bias, uint16_t* out, void* workspace, cudaStream_t st) {
+  ra::ProjLaunch L{};
+  L.a = a;
+  L.a_scale = a_scale;
+  L.w_t = static_cast<const uint8_t*>(w_packed);
+  L.sf = static_cast<const uint8_t*>(w_packed) + ra::packed_sf_offset(s.H, s.I);
+  L.weight_scales = ws;
+  L.bias = bias;
+  L.out = out;
+  L.status = static_cast<int32_t*>(workspace);
+  L.partials = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ra::kWorkspaceHeader);
+  L.T = s.T;
+  L.H = s.H;
+  L.I = s.I;
+  L.q_end = s.q_end;
+  L.k_end = p->num_kv_heads > 0 ? s.k_end : s.q_end;
+  L.n_part_tiles = s.n_part_tiles;
+  L.wait_ns = g_wait_ns.load();
+  const char* why = "launch failed";
+  cudaError_t e = ra::launch_qkv_project(L, st, &why);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "qkv projection: %s (%s)", why, cudaGetErrorString(e));
+  return RA_OK;
+}
+
+ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const float* cos,
+                        const float* sin, const float* qg, const float* kg, uint16_t* out,
+                        void* workspace, cudaStream_t st) {
+  const bool do_q = p->q_norm || p->fused_rope;
+  const bool do_k = p->num_kv_heads > 0 && (p->k_norm || p->fused_rope);
+  if (!do_q && !do_k) return RA_OK;
+  ra::NormRopeLaunch L{};
+  L.out = out;
+  L.partials =
+      reinterpret_cast<const float2*>(static_cast<const uint8_t*>(workspace) + ra::kWorkspaceHeader);
+  L.cos = cos;
+  L.sin = sin;
+  L.q_gamma = qg;
+  L.k_gamma = kg;
+  L.T = s.T;
+  L.I = s.I;
+  L.head_dim = p->head_dim;
+  L.num_q_heads = p->num_heads;
+  L.num_k_heads = p->num_kv_heads;
+  L.q_norm = p->q_norm != RA_NORM_NONE;
+  L.k_norm = p->k_norm != RA_NORM_NONE;
+  L.rope = p->fused_rope;
+  L.n_part_tiles = s.n_part_tiles;
+  L.eps = p->norm_eps;
+  cudaError_t e = ra::launch_qk_norm_rope(L, st);
+  if (e != cudaSuccess) return cuda_fail(e, "norm/rope launch");
+  return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ra_last_error(void) { return g_last_error.c_str(); }
+
+int32_t ra_abi_version(void) { return 1; }
+
+void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
+
+ra_status qkv_cte_mx_packed_weight_bytes(int64_t H, int64_t I, size_t* bytes) {
+  if (!bytes) return fail(RA_ERR_INVALID_ARG, "bytes is NULL");
+  if (H < 128 || H % 128 != 0) return fail(RA_ERR_INVALID_ARG, "H must be a positive multiple of 128");
+  if (I < 16 || I % 16 != 0) return fail(RA_ERR_INVALID_ARG, "I must be a positive multiple of 16");
+  *bytes = ra::packed_weight_bytes(H, I);
+  return ok();
+}
+
+ra_status qkv_cte_mx_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int64_t H, int64_t I,
+                                 void* packed, size_t packed_bytes, void* stream) {
+  size_t need = 0;
+  ra_status st = qkv_cte_mx_packed_weight_bytes(H, I, &need);
+  if (st != RA_OK) return st;
+  if (!w || !w_block_exp || !packed) return fail(RA_ERR_INVALID_ARG, "w, w_block_exp and packed are required");
+  if (!aligned16(packed)) return fail(RA_ERR_ALIGNMENT, "packed must be 16-byte aligned");
+  if (packed_bytes < need) return fail(RA_ERR_WORKSPACE, "packed buffer too small: %zu < %zu", packed_bytes, need);
+  if (H > 0x7fffffffLL || I > 0x7fffffffLL) return fail(RA_ERR_INVALID_ARG, "H or I too large");
+  cudaError_t e = ra::launch_pack_weight(w, w_block_exp, H, I, static_cast<uint8_t*>(packed),
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pack_weight launch");
+  return ok();
+}
+
+ra_status qkv_cte_mx_workspace_bytes(const qkv_cte_mx_params* p, size_t* bytes) {
+  if (!bytes) return fail(RA_ERR_INVALID_ARG, "bytes is NULL");
+  QkvShape s;
+  ra_status st = check_params(p, &s);
+  if (st != RA_OK) return st;
+  *bytes = s.workspace;
+  return ok();
+}
+
+ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
+                             const void* w_packed, const float* weight_scales, const uint16_t* bias,
+                             uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  QkvShape s;
+  ra_status st = check_params(p, &s);
+  if (st != RA_OK) return st;
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace, workspace_bytes);
+  if (st != RA_OK) return st;
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace,
+                   static_cast<cudaStream_t>(stream));
+  return st == RA_OK ? ok() : st;
+}
+
+ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cache,
+                               const float* sin_cache, const float* q_gamma, const float* k_gamma,
+                               uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  QkvShape s;
+  ra_status st = check_params(p, &s);
+  if (st != RA_OK) return st;
+  st = check_norm_args(p, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace, workspace_bytes, s);
+  if (st != RA_OK) return st;
+  st = run_norm_rope(p, s, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace,
+                     static_cast<cudaStream_t>(stream));
+  return st == RA_OK ? ok() : st;
+}
+
+ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
+                     const void* w_packed, const float* weight_scales, const uint16_t* bias,
+                     const float* cos_cache, const float* sin_cache, const float* q_gamma,
+                     const float* k_gamma, uint16_t* out, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  QkvShape s;
+  ra_status st = check_params(p, &s);
+  if (st != RA_OK) return st;
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace, workspace_bytes);
+  if (st != RA_OK) return st;
+  st = check_norm_args(p, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace, workspace_bytes, s);
+  if (st != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace, cs);
+  if (st != RA_OK) return st;
+  st = run_norm_rope(p, s, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace, cs);
+  return st == RA_OK ? ok() : st;
+}
+
+ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_status) {
+  if (!workspace || !device_status) return fail(RA_ERR_INVALID_ARG, "workspace and device_status are required");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *device_status = v;
+  if (v != 0) return fail(RA_ERR_TIMEOUT, "a projection pipeline wait ran out of time (status %d)", v);
+  return ok();
+}
+
+ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const uint16_t* kv,
+                                 const uint16_t* gamma, const uint16_t* cos, const uint16_t* sin,
+                                 const int64_t* index, void* k_cache, void* ckv_cache,
+                                 const float* k_rope_scale, const float* c_kv_scale,
+                                 const float* k_rope_offset, const float* c_kv_offset,
+                                 const uint16_t* v_optional, uint16_t* k_rope, uint16_t* c_kv,
+                                 int32_t* dev_error_count, void* stream) {
+  if (p == nullptr) return fail(RA_ERR_INVALID_ARG, "params is NULL");
+  if (!kv || !gamma || !cos || !sin || !index || !k_cache || !ckv_cache)
+    return fail(RA_ERR_INVALID_ARG, "kv, gamma, cos, sin, index, k_cache and ckv_cache are required");
+  if (p->B < 1 || p->N < 1 || p->S < 1 || p->Dkv < 1)
+    return fail(RA_ERR_INVALID_ARG, "empty tensors are not supported");
+  if (p->kv_dtype == RA_FP16) return fail(RA_ERR_UNSUPPORTED, "fp16 kv is not built; use bf16");
+  if (p->kv_dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "kv dtype must be bf16 or fp16");
+  const int64_t R = p->rope_size;
+  if (R < 8 || R % 8 != 0 || R > 256)
+    return fail(RA_ERR_INVALID_ARG, "rope_size must be even; this build needs a multiple of 8 in [8, 256]");
+  if (p->Dkv % 8 != 0 || p->Dv % 8 != 0 || p->Dv < 8)
+    return fail(RA_ERR_INVALID_ARG, "Dkv and Dv must be positive multiples of 8");
+  int64_t rms = 0;
+  if (p->variant == 1) {
+    if (p->N != 1) return fail(RA_ERR_INVALID_ARG, "V1 (combined kv) supports N == 1 only");
+    if (v_optional) return fail(RA_ERR_INVALID_ARG, "v_optional must be NULL in V1");
+    if (p->Dv != p->Dkv - R) return fail(RA_ERR_INVALID_ARG, "V1 needs Dv == Dkv - rope_size");
+    rms = p->Dv;
+  } else if (p->variant == 2) {
+    if (!(p->N == 1 || p->N == 2 || p->N == 4 || p->N == 8))
+      return fail(RA_ERR_INVALID_ARG, "V2 (separate kv) supports N in {1, 2, 4, 8}");
+    if (!v_optional) return fail(RA_ERR_INVALID_ARG, "V2 needs v_optional");
+    if (R > p->Dkv) return fail(RA_ERR_INVALID_ARG, "rope_size exceeds Dkv");
+    if (p->Dv > 8 * 32 * 64) return fail(RA_ERR_INVALID_ARG, "Dv too large");
+    rms = p->Dkv;
+  } else {
+    return fail(RA_ERR_INVALID_ARG, "variant must be 1 or 2");
+  }
+  if (rms < 8 || rms > 1024) return fail(RA_ERR_INVALID_ARG, "rms_size must be in [8, 1024]");
+  if ((k_rope_offset && !k_rope_scale) || (c_kv_offset && !c_kv_scale))
+    return fail(RA_ERR_INVALID_ARG, "an offset without its scale is illegal");
+  const bool qk = k_rope_scale != nullptr, qv = c_kv_scale != nullptr;
+  if (qk ? p->k_cache_dtype != RA_INT8 : p->k_cache_dtype != p->kv_dtype)
+    return fail(qk && p->k_cache_dtype != RA_INT8 && p->k_cache_dtype != RA_BF16 ? RA_ERR_UNSUPPORTED
+                                                                                 : RA_ERR_INVALID_ARG,
+                "k_cache dtype must be int8 with a k scale, else equal to the kv dtype");
+  if (qv ? p->ckv_cache_dtype != RA_INT8 : p->ckv_cache_dtype != p->kv_dtype)
+    return fail(qv && p->ckv_cache_dtype != RA_INT8 && p->ckv_cache_dtype != RA_BF16 ? RA_ERR_UNSUPPORTED
+                                                                                     : RA_ERR_INVALID_ARG,
+                "ckv_cache dtype must be int8 with a c_kv scale, else equal to the kv dtype");
+  if (p->cache_mode != RA_CACHE_PA && p->cache_mode != RA_CACHE_PA_BNSD)
+    return fail(RA_ERR_UNSUPPORTED, "cache_mode must be PA or PA_BNSD in this build");
+  if (p->block_num < 1 || p->block_size <= 1)
+    return fail(RA_ERR_INVALID_ARG, "block_num >= 1 and block_size > 1 are required");
+  if ((qk || qv) && p->block_size % 32 != 0)
+    return fail(RA_ERR_INVALID_ARG, "int8 caches need block_size %% 32 == 0");
+  if ((!qk || !qv) && p->block_size % 16 != 0)
+    return fail(RA_ERR_INVALID_ARG, "bf16 caches need block_size %% 16 == 0");
+  if (!(p->epsilon >= 0.f) || !std::isfinite(p->epsilon))
+    return fail(RA_ERR_INVALID_ARG, "epsilon must be finite and >= 0");
+  if (p->is_output_kv && (!k_rope || !c_kv))
+    return fail(RA_ERR_INVALID_ARG, "is_output_kv requires k_rope and c_kv");
+  if (!aligned16(kv) || !aligned16(gamma) || !aligned16(cos) || !aligned16(sin) ||
+      !aligned16(k_cache) || !aligned16(ckv_cache) || (v_optional && !aligned16(v_optional)) ||
+      (k_rope && !aligned16(k_rope)) || (c_kv && !aligned16(c_kv)) ||
+      (k_rope_scale && !aligned16(k_rope_scale)) || (c_kv_scale && !aligned16(c_kv_scale)) ||
+      (k_rope_offset && !aligned16(k_rope_offset)) || (c_kv_offset && !aligned16(c_kv_offset)) ||
+      (reinterpret_cast<uintptr_t>(index) & 7u))
+    return fail(RA_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned (index 8-byte)");
+  if (p->B * p->N * p->S > (1LL << 40)) return fail(RA_ERR_INVALID_ARG, "too many rows");
+
+  ra::KvLaunch L{};
+  L.kv = kv;
+  L.gamma = gamma;
+  L.cos = cos;
+  L.sin = sin;
+  L.index = index;
+  L.k_cache = k_cache;
+  L.ckv_cache = ckv_cache;
+  L.k_scale = k_rope_scale;
+  L.k_offset = k_rope_offset;
+  L.v_scale = c_kv_scale;
+  L.v_offset = c_kv_offset;
+  L.v = v_optional;
+  L.k_rope = k_rope;
+  L.c_kv = c_kv;
+  L.err_count = dev_error_count;
+  L.B = p->B;
+  L.N = p->N;
+  L.S = p->S;
+  L.Dkv = p->Dkv;
+  L.Dv = p->Dv;
+  L.R = p->rope_size;
+  L.variant = p->variant;
+  L.mode = p->cache_mode;
+  L.block_num = p->block_num;
+  L.block_size = p->block_size;
+  L.eps = p->epsilon;
+  L.out_kv = p->is_output_kv;
+  cudaError_t e = ra::launch_kv_rms_norm_rope_cache(L, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_rms_norm_rope_cache launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ra {
+
+// ------------------------------------------------------------ projection (K1)
+// Tile shape of the block-scaled FP8 GEMM; also fixes the packed weight layout.
+constexpr int kProjBM = 128;          // token rows per tile (one TMEM lane per row)
+constexpr int kProjBN = 240;          // output columns per tile
+constexpr int kProjBK = 128;          // contraction elements (= bytes) per pipeline stage
+constexpr int kSfChunkBytes = 512;    // 128 columns x 4 block scales, tcgen05.cp image
+constexpr int kSfStageBytes = ((kProjBN + 127) / 128) * kSfChunkBytes;
+constexpr int kWorkspaceHeader = 256; // status word + padding, ahead of the partial sums
+
+struct ProjLaunch {
+  const uint8_t* a;            // [T, H] e4m3
+  const float* a_scale;        // [T]
+  const uint8_t* w_t;          // [I, H] e4m3 (packed, K-major)
+  const uint8_t* sf;           // packed block-scale images
+  const float* weight_scales;  // [I] or null
+  const uint16_t* bias;        // [I] bf16 or null
+  uint16_t* out;               // [T, I] bf16
+  float2* partials;            // [n_part_tiles, T] (sum sq Q, sum sq K)
+  int32_t* status;
+  int64_t T, H, I;
+  int32_t q_end, k_end;        // Q = [0, q_end), K = [q_end, k_end) output columns
+  int32_t n_part_tiles;
+  int64_t wait_ns;
+};
+cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why);
+
+size_t packed_weight_bytes(int64_t H, int64_t I);
+size_t packed_sf_offset(int64_t H, int64_t I);
+cudaError_t launch_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int64_t H, int64_t I,
+                               uint8_t* packed, cudaStream_t stream);
+
+// ------------------------------------------------------------ norm + RoPE apply (K2)
+struct NormRopeLaunch {
+  uint16_t* out;               // [T, I] bf16, updated in place
+  const float2* partials;      // [n_part_tiles, T]
+  const float* cos;            // [T, d]
+  const float* sin;
+  const float* q_gamma;        // [q_w] or null
+  const float* k_gamma;        // [k_w] or null
+  int64_t T, I;
+  int32_t head_dim, num_q_heads, num_k_heads;
+  int32_t q_norm, k_norm, rope;
+  int32_t n_part_tiles;
+  float eps;
+};
+cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);
+
+// ------------------------------------------------------------ KV cache (K3)
+struct KvLaunch {
+  const uint16_t* kv;
+  const uint16_t* gamma;
+  const uint16_t* cos;
+  const uint16_t* sin;
+  const int64_t* index;
+  void* k_cache;
+  void* ckv_cache;
+  const float* k_scale;
+  const float* k_offset;
+  const float* v_scale;
+  const float* v_offset;
+  const uint16_t* v;
+  uint16_t* k_rope;
+  uint16_t* c_kv;
+  int32_t* err_count;
+  int64_t B, N, S, Dkv, Dv;
+  int32_t R;                   // rope size
+  int32_t variant;             // 1 or 2
+  int32_t mode;                // 1 = PA, 2 = PA_BNSD
+  int64_t block_num, block_size;
+  float eps;
+  int32_t out_kv;
+};
+cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace ra

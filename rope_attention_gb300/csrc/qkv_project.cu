@@ -1,0 +1,500 @@
+// K1: block-scaled FP8 projection with the dequant / bias / sum-of-squares epilogue.
+//
+// Computes, for the fused QKV projection of the AWS Neuron page "Kernel
+// reference: qkv_cte" (section "Upstream behavior": O[S, I] = A[S, H] @ W[H, I]
+// (+ bias); Pattern: the accumulator is dequantised and bias-added while it is
+// read out, then stored to HBM; Design 1a: per-token sum(x^2) over the whole Q
+// and K segments of the un-normalised output):
+//
+//   out[t, i]     = bf16( acc[t, i] * a_scale[t] * wch[i] + bias[i] )
+//   acc[t, i]     = sum_h e4m3(a[t, h]) * e4m3(w[h, i]) * 2^(e[h/32, i] - 127)
+//   partial[j, t] = ( sum over Q columns of tile j of v^2, sum over K columns of v^2 )
+//
+// GB300 design (not the page's NKI schedule):
+//  * persistent CTAs (one per SM), 128 x 240 output tiles, grouped rasterisation
+//    so that concurrently running tiles share A rows and W columns in L2;
+//  * warp 0: TMA producer (A and W tiles with 128-byte swizzle, plus the W block
+//    scales as a plain bulk copy) into a 4-stage shared-memory ring;
+//  * warp 1: allocates 512 TMEM columns and issues tcgen05.mma
+//    kind::mxf8f6f4 (M=128, N=240, K=32 per instruction) from one thread; W's
+//    ue8m0 scales go through tcgen05.cp into TMEM each stage; A's MX scale is
+//    the constant 2^0 (its fp32 row scale is applied in the epilogue, since it is
+//    constant along K);
+//  * warps 2-5: epilogue, one TMEM lane quadrant each; two accumulator buffers
+//    let the epilogue of tile i overlap the mainloop of tile i+1.
+// Every pipeline wait is bounded in time; on expiry the CTA records an error in
+// the status word, drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int BM = kProjBM;
+constexpr int BN = kProjBN;
+constexpr int BK = kProjBK;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int SF_BYTES = kSfStageBytes;
+constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SF_BYTES;
+constexpr int NUM_ACC = 2;
+constexpr int ACC_STRIDE = BN;           // TMEM columns between accumulator buffers
+constexpr int SFA_COL = NUM_ACC * BN;    // 4 columns of A scales
+constexpr int SFB_COL = SFA_COL + 8;     // two 8-column slots of W scales
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+constexpr int GROUP_M = 16;
+
+constexpr int SMEM_A = 0;
+constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
+constexpr int SMEM_SF = SMEM_B + STAGES * B_BYTES;
+constexpr int SMEM_SFA = SMEM_SF + STAGES * SF_BYTES;
+constexpr int SMEM_BAR = SMEM_SFA + 512;
+constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
+constexpr int SMEM_USED = SMEM_MISC + 16;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+
+static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
+static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+static_assert(SFB_COL + 16 <= TMEM_COLS, "TMEM budget");
+static_assert(BN % 16 == 0 && BN <= 256 && BN > 128, "MMA N and scale-image shape");
+
+// Instruction descriptor, block-scaled kinds: A/B format E4M3 (0) in bits
+// [7,10)/[10,13), K-major operands, N>>3 in [17,23), scale type UE8M0 (1) at
+// bit 23, M>>4 in [24,29); the scale-factor ids go in [29,31) (A) and [4,6) (B).
+constexpr uint32_t kIdesc = (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t(BM >> 4) << 24);
+
+struct Params {
+  CUtensorMap tmap_a;   // [T, H] bytes, box 128 x 128, 128-byte swizzle
+  CUtensorMap tmap_b;   // [I, H] bytes, box 128 x BN
+  const uint8_t* sf;
+  const float* a_scale;
+  const float* wch;
+  const uint16_t* bias;
+  uint16_t* out;
+  float2* partials;
+  int32_t* status;
+  int32_t T, I, num_k, num_m, num_n;
+  int32_t q_end, k_end, n_part;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_tile) {
+  const int per_group = GROUP_M * num_n;
+  const int group = tile / per_group;
+  const int first_m = group * GROUP_M;
+  const int gm = min(GROUP_M, num_m - first_m);
+  const int local = tile - group * per_group;
+  m_blk = first_m + local % gm;
+  n_tile = local / gm;
+}
+
+// single-thread bounded wait; false when this or another role gave up
+__device__ bool wait_one(uint32_t bar, uint32_t parity, uint64_t limit, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// warp-collective bounded wait: every lane returns the same answer
+__device__ bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit, volatile int* abort_flag) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((i & 31u) == 31u) {
+      int give_up = 0;
+      if (lane_id() == 0) {
+        const uint64_t t = globaltimer_ns();
+        if (t0 == 0) t0 = t;
+        else if (*abort_flag || t - t0 > limit) give_up = 1;
+      }
+      give_up = __shfl_sync(0xffffffffu, give_up, 0);
+      if (give_up) {
+        if (lane_id() == 0) *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// bounded wait used only while tearing down (ignores the abort flag)
+__device__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit) return;
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sA = s_base + SMEM_A;
+  const uint32_t sB = s_base + SMEM_B;
+  const uint32_t sSF = s_base + SMEM_SF;
+  const uint32_t sSFA = s_base + SMEM_SFA;
+  const uint32_t bar0 = s_base + SMEM_BAR;
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * NUM_ACC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + NUM_ACC + a); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t drain_ns = 200000000ull;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < NUM_ACC; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&p.tmap_a);
+    prefetch_tensormap(&p.tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp >= EPI_WARP0) {
+    // A's MX scale factors: ue8m0 127 (= 1.0) for every row and block
+    uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + SMEM_SFA);
+    sfa[threadIdx.x - EPI_WARP0 * 32] = 0x7F7F7F7Fu;
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int num_tiles = p.num_m * p.num_n;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int mb, nt;
+        tile_coords(tile, p.num_m, p.num_n, mb, nt);
+        const uint8_t* sf_tile = p.sf + static_cast<size_t>(nt) * p.num_k * SF_BYTES;
+        for (int kb = 0; kb < p.num_k; ++kb) {
+          if (!wait_one(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+          tma_load_2d(sA + stage * A_BYTES, &p.tmap_a, full_bar(stage), kb * BK, mb * BM);
+          tma_load_2d(sB + stage * B_BYTES, &p.tmap_b, full_bar(stage), kb * BK, nt * BN);
+          bulk_load(sSF + stage * SF_BYTES, sf_tile + static_cast<size_t>(kb) * SF_BYTES, SF_BYTES,
+                    full_bar(stage));
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // every copy started here must land before this CTA's shared memory is released
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) wait_drain(full_bar(s), (armed_parity >> s) & 1u, drain_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      tc_cp_32x128b_warpx4(tmem + SFA_COL, sdesc_scale_rows(sSFA));
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_parity = (local >> 1) & 1;
+        if (!wait_one(acce_bar(acc), acc_parity ^ 1u, p.wait_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * ACC_STRIDE;
+        for (int kb = 0; kb < p.num_k; ++kb) {
+          if (!wait_one(full_bar(stage), phase, p.wait_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfb = tmem + SFB_COL + (kb & 1) * 8;
+          const uint32_t sf_s = sSF + stage * SF_BYTES;
+          tc_cp_32x128b_warpx4(sfb, sdesc_scale_rows(sf_s));
+          tc_cp_32x128b_warpx4(sfb + 4, sdesc_scale_rows(sf_s + kSfChunkBytes));
+          const uint32_t a_s = sA + stage * A_BYTES;
+          const uint32_t b_s = sB + stage * B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint32_t idesc = kIdesc | (uint32_t(kk) << 29) | (uint32_t(kk) << 4);
+            tc_mma_mxf8(d_tmem, sdesc_kmajor_sw128(a_s + kk * 32), sdesc_kmajor_sw128(b_s + kk * 32),
+                        idesc, tmem + SFA_COL, sfb, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(accf_bar(acc));
+      }
+      // all MMAs issued here must finish before TMEM is released
+      tc_commit(drain_bar);
+      wait_drain(drain_bar, 0, drain_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    const int row_in_tile = quad * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      int mb, nt;
+      tile_coords(tile, p.num_m, p.num_n, mb, nt);
+      const int acc = local & 1;
+      const uint32_t acc_parity = (local >> 1) & 1;
+      if (!wait_warp(accf_bar(acc), acc_parity, p.wait_ns, abort_flag)) break;
+      tc_fence_after();
+      const int row = mb * BM + row_in_tile;
+      const bool row_ok = row < p.T;
+      const float as = row_ok ? __ldg(p.a_scale + row) : 0.f;
+      float ssq = 0.f, ssk = 0.f;
+      const uint32_t t_base = tmem + acc * ACC_STRIDE + (static_cast<uint32_t>(quad * 32) << 16);
+      uint16_t* out_row = p.out + static_cast<size_t>(row_ok ? row : 0) * p.I;
+      for (int c = 0; c < BN / 16; ++c) {
+        const int col0 = nt * BN + c * 16;
+        if (col0 >= p.I) break;  // warp-uniform: ragged last column tile
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(t_base + c * 16, r);
+        tmem_ld_wait();
+        float wch[16], bia[16];
+        if (p.wch != nullptr) {
+          const float4* w4 = reinterpret_cast<const float4*>(p.wch + col0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 t = __ldg(w4 + j);
+            wch[4 * j] = t.x; wch[4 * j + 1] = t.y; wch[4 * j + 2] = t.z; wch[4 * j + 3] = t.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) wch[j] = 1.f;
+        }
+        if (p.bias != nullptr) {
+          const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + col0);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint4 t = __ldg(b4 + j);
+            const uint32_t u[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              bia[8 * j + 2 * k] = bf16_lo(u[k]);
+              bia[8 * j + 2 * k + 1] = bf16_hi(u[k]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) bia[j] = 0.f;
+        }
+        float v[16];
+        float sq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          v[j] = fmaf(__uint_as_float(r[j]) * as, wch[j], bia[j]);
+          sq = fmaf(v[j], v[j], sq);
+        }
+        if (col0 < p.q_end) ssq += sq;
+        else if (col0 < p.k_end) ssk += sq;
+        if (row_ok) {
+          uint4 o0, o1;
+          o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
+          o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
+          o1.x = pack_bf16x2(v[8], v[9]);   o1.y = pack_bf16x2(v[10], v[11]);
+          o1.z = pack_bf16x2(v[12], v[13]); o1.w = pack_bf16x2(v[14], v[15]);
+          uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
+          dst[0] = o0;
+          dst[1] = o1;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (nt < p.n_part && row_ok)
+        p.partials[static_cast<size_t>(nt) * p.T + row] = make_float2(ssq, ssk);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, 1);
+}
+
+// ---------------------------------------------------------------- weight packing
+__global__ void transpose_w_kernel(const uint8_t* __restrict__ w, uint8_t* __restrict__ wt, int H,
+                                   int I) {
+  __shared__ uint8_t tile[64][65];
+  const int i0 = blockIdx.x * 64, h0 = blockIdx.y * 64;
+  for (int r = threadIdx.y; r < 64; r += blockDim.y) {
+    const int h = h0 + r, i = i0 + threadIdx.x;
+    if (h < H && i < I) tile[r][threadIdx.x] = w[static_cast<size_t>(h) * I + i];
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 64; r += blockDim.y) {
+    const int i = i0 + r, h = h0 + threadIdx.x;
+    if (i < I && h < H) wt[static_cast<size_t>(i) * H + h] = tile[threadIdx.x][r];
+  }
+}
+
+// Scale image of one (column tile, K stage): for each 128-column group g, 32
+// rows of 16 bytes; row n0, word c, byte j holds the exponent of column
+// g*128 + c*32 + n0 and 32-block j of the stage -- the layout tcgen05.cp
+// 32x128b.warpx4 turns into "TMEM lane n%32, column n/32, byte = block".
+__global__ void pack_sf_kernel(const uint8_t* __restrict__ e, uint8_t* __restrict__ sf, int H, int I,
+                               int num_n, int num_k) {
+  const size_t total = static_cast<size_t>(num_n) * num_k * SF_BYTES;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int off = static_cast<int>(idx % SF_BYTES);
+    const size_t t = idx / SF_BYTES;
+    const int kb = static_cast<int>(t % num_k);
+    const int nt = static_cast<int>(t / num_k);
+    const int g = off / kSfChunkBytes, w = off % kSfChunkBytes;
+    const int n0 = w / 16, c = (w % 16) / 4, j = w % 4;
+    const int nl = g * 128 + c * 32 + n0;
+    const int n = nt * BN + nl;
+    const int hb = kb * (BK / 32) + j;
+    uint8_t v = 127;
+    if (nl < BN && n < I && hb < H / 32) v = e[static_cast<size_t>(hb) * I + n];
+    sf[idx] = v;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_outer) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};  // bytes per row (1-byte elements)
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t packed_sf_offset(int64_t H, int64_t I) {
+  return ((static_cast<size_t>(H) * I + 1023) / 1024) * 1024;
+}
+
+size_t packed_weight_bytes(int64_t H, int64_t I) {
+  const size_t num_n = (I + BN - 1) / BN, num_k = (H + BK - 1) / BK;
+  return packed_sf_offset(H, I) + num_n * num_k * SF_BYTES;
+}
+
+cudaError_t launch_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int64_t H, int64_t I,
+                               uint8_t* packed, cudaStream_t stream) {
+  dim3 tb(64, 4), tg(static_cast<unsigned>((I + 63) / 64), static_cast<unsigned>((H + 63) / 64));
+  transpose_w_kernel<<<tg, tb, 0, stream>>>(w, packed, static_cast<int>(H), static_cast<int>(I));
+  const int num_n = static_cast<int>((I + BN - 1) / BN), num_k = static_cast<int>((H + BK - 1) / BK);
+  const size_t total = static_cast<size_t>(num_n) * num_k * SF_BYTES;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((total + 255) / 256, 65535));
+  pack_sf_kernel<<<blocks, 256, 0, stream>>>(w_block_exp, packed + packed_sf_offset(H, I),
+                                             static_cast<int>(H), static_cast<int>(I), num_n, num_k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why) {
+  Params p{};
+  if (!make_tmap_2d(&p.tmap_a, L.a, L.H, L.T, BK, BM) ||
+      !make_tmap_2d(&p.tmap_b, L.w_t, L.H, L.I, BK, BN)) {
+    *why = "cuTensorMapEncodeTiled failed or is unavailable";
+    return cudaErrorInvalidValue;
+  }
+  p.sf = L.sf;
+  p.a_scale = L.a_scale;
+  p.wch = L.weight_scales;
+  p.bias = L.bias;
+  p.out = L.out;
+  p.partials = L.partials;
+  p.status = L.status;
+  p.T = static_cast<int32_t>(L.T);
+  p.I = static_cast<int32_t>(L.I);
+  p.num_k = static_cast<int32_t>(L.H / BK);
+  p.num_m = static_cast<int32_t>((L.T + BM - 1) / BM);
+  p.num_n = static_cast<int32_t>((L.I + BN - 1) / BN);
+  p.q_end = L.q_end;
+  p.k_end = L.k_end;
+  p.n_part = L.n_part_tiles;
+  p.wait_ns = static_cast<uint64_t>(L.wait_ns);
+
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(qkv_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_ALLOC);
+  });
+  if (attr_err != cudaSuccess) {
+    *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return attr_err;
+  }
+  const int num_tiles = p.num_m * p.num_n;
+  const int grid = std::min(num_tiles, device_sm_count());
+  qkv_project_kernel<<<grid, NUM_THREADS, SMEM_ALLOC, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,205 @@
+"""ctypes binding of librope_attention.so (include/rope_attention.h).
+
+Argument marshalling only: every function here checks tensor placement,
+dtype and contiguity, turns tensors into raw pointers and calls the C entry
+point of the same name on the current CUDA stream.  All arithmetic happens in
+the library's CUDA kernels; there is no CPU fallback.  ``load()`` raises if
+the library has not been built (``python -m rope_attention_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+RA_OK = 0
+STATUS_NAMES = {0: "RA_OK", -1: "RA_ERR_INVALID_ARG", -2: "RA_ERR_UNSUPPORTED",
+                -3: "RA_ERR_ALIGNMENT", -4: "RA_ERR_WORKSPACE", -5: "RA_ERR_CUDA",
+                -6: "RA_ERR_TIMEOUT", -7: "RA_ERR_INDEX"}
+RA_BF16, RA_FP16, RA_INT8, RA_FP32 = 0, 1, 2, 3
+RA_NORM_NONE, RA_NORM_RMS_ACROSS_HEADS = 0, 1
+RA_LAYOUT_BSD, RA_LAYOUT_NBSD = 0, 1
+RA_CACHE_PA, RA_CACHE_PA_BNSD = 1, 2
+
+EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns",
+           "qkv_cte_mx_packed_weight_bytes", "qkv_cte_mx_pack_weight", "qkv_cte_mx_workspace_bytes",
+           "qkv_cte_mx", "qkv_cte_mx_project", "qkv_cte_mx_norm_rope", "qkv_cte_mx_status",
+           "kv_rms_norm_rope_cache"]
+
+
+class RAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class QkvCteMxParams(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("S", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("num_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("q_norm", ctypes.c_int32), ("k_norm", ctypes.c_int32),
+                ("fused_rope", ctypes.c_int32), ("norm_eps", ctypes.c_float),
+                ("output_layout", ctypes.c_int32)]
+
+
+class KvRmsNormRopeCacheParams(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("N", ctypes.c_int64), ("S", ctypes.c_int64),
+                ("Dkv", ctypes.c_int64), ("Dv", ctypes.c_int64), ("rope_size", ctypes.c_int32),
+                ("variant", ctypes.c_int32), ("cache_mode", ctypes.c_int32),
+                ("block_num", ctypes.c_int64), ("block_size", ctypes.c_int64),
+                ("kv_dtype", ctypes.c_int32), ("k_cache_dtype", ctypes.c_int32),
+                ("ckv_cache_dtype", ctypes.c_int32), ("epsilon", ctypes.c_float),
+                ("is_output_kv", ctypes.c_int32)]
+
+
+_LIB = None
+P = ctypes.c_void_p
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library (once).  Raises FileNotFoundError if it is not built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing: build it with `python -m rope_attention_gb300.build`")
+    lib = ctypes.CDLL(path)
+    i32, i64, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "ra_last_error": (ctypes.c_char_p, []),
+        "ra_abi_version": (i32, []),
+        "ra_set_wait_timeout_ns": (None, [i64]),
+        "qkv_cte_mx_packed_weight_bytes": (i32, [i64, i64, ctypes.POINTER(sz)]),
+        "qkv_cte_mx_pack_weight": (i32, [P, P, i64, i64, P, sz, P]),
+        "qkv_cte_mx_workspace_bytes": (i32, [ctypes.POINTER(QkvCteMxParams), ctypes.POINTER(sz)]),
+        "qkv_cte_mx": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, P, P, sz, P]),
+        "qkv_cte_mx_project": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, sz, P]),
+        "qkv_cte_mx_norm_rope": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, sz, P]),
+        "qkv_cte_mx_status": (i32, [P, P, ctypes.POINTER(i32)]),
+        "kv_rms_norm_rope_cache": (i32, [ctypes.POINTER(KvRmsNormRopeCacheParams), P, P, P, P, P,
+                                         P, P, P, P, P, P, P, P, P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != RA_OK:
+        raise RAError(status, load().ra_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None, dtype: torch.dtype | None = None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bits16(t: torch.Tensor | None) -> torch.Tensor | None:
+    """bf16 tensors are passed as their 16-bit patterns."""
+    if t is None:
+        return None
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+def ra_abi_version() -> int:
+    return int(load().ra_abi_version())
+
+
+def ra_set_wait_timeout_ns(ns: int) -> None:
+    load().ra_set_wait_timeout_ns(int(ns))
+
+
+# ---------------------------------------------------------------- qkv_cte_mx
+def qkv_cte_mx_packed_weight_bytes(H: int, I: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().qkv_cte_mx_packed_weight_bytes(H, I, ctypes.byref(n)))
+    return n.value
+
+
+def qkv_cte_mx_pack_weight(w: torch.Tensor, w_block_exp: torch.Tensor, packed: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """w [H, I] uint8 e4m3 codes, w_block_exp [H/32, I] uint8; returns the packed uint8 buffer."""
+    H, I = w.shape
+    nbytes = qkv_cte_mx_packed_weight_bytes(H, I)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    _check(load().qkv_cte_mx_pack_weight(_ptr(w, torch.uint8, "w"), _ptr(w_block_exp, torch.uint8, "w_block_exp"),
+                                         H, I, _ptr(packed, torch.uint8, "packed"), packed.numel(),
+                                         _stream(stream)))
+    return packed
+
+
+def qkv_cte_mx_workspace_bytes(params: QkvCteMxParams) -> int:
+    n = ctypes.c_size_t()
+    _check(load().qkv_cte_mx_workspace_bytes(ctypes.byref(params), ctypes.byref(n)))
+    return n.value
+
+
+def qkv_cte_mx(params, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache, q_gamma,
+               k_gamma, out, workspace, stream=None) -> None:
+    _check(load().qkv_cte_mx(
+        ctypes.byref(params), _ptr(a, torch.uint8, "a"), _ptr(a_scale, torch.float32, "a_scale"),
+        _ptr(w_packed, torch.uint8, "w_packed"), _ptr(weight_scales, torch.float32, "weight_scales"),
+        _ptr(_bits16(bias), None, "bias"), _ptr(cos_cache, torch.float32, "cos_cache"),
+        _ptr(sin_cache, torch.float32, "sin_cache"), _ptr(q_gamma, torch.float32, "q_gamma"),
+        _ptr(k_gamma, torch.float32, "k_gamma"), _ptr(_bits16(out), None, "out"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def qkv_cte_mx_project(params, a, a_scale, w_packed, weight_scales, bias, out, workspace, stream=None) -> None:
+    _check(load().qkv_cte_mx_project(
+        ctypes.byref(params), _ptr(a, torch.uint8, "a"), _ptr(a_scale, torch.float32, "a_scale"),
+        _ptr(w_packed, torch.uint8, "w_packed"), _ptr(weight_scales, torch.float32, "weight_scales"),
+        _ptr(_bits16(bias), None, "bias"), _ptr(_bits16(out), None, "out"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def qkv_cte_mx_norm_rope(params, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace, stream=None) -> None:
+    _check(load().qkv_cte_mx_norm_rope(
+        ctypes.byref(params), _ptr(cos_cache, torch.float32, "cos_cache"),
+        _ptr(sin_cache, torch.float32, "sin_cache"), _ptr(q_gamma, torch.float32, "q_gamma"),
+        _ptr(k_gamma, torch.float32, "k_gamma"), _ptr(_bits16(out), None, "out"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def qkv_cte_mx_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream; returns the device status word (0 = fine) and clears it."""
+    v = ctypes.c_int32()
+    st = load().qkv_cte_mx_status(_ptr(workspace, torch.uint8, "workspace"), _stream(stream), ctypes.byref(v))
+    if st not in (RA_OK, -6):
+        _check(st)
+    return v.value
+
+
+# ---------------------------------------------------------------- kv_rms_norm_rope_cache
+def kv_rms_norm_rope_cache(params, kv, gamma, cos, sin, index, k_cache, ckv_cache, k_rope_scale=None,
+                           c_kv_scale=None, k_rope_offset=None, c_kv_offset=None, v_optional=None,
+                           k_rope=None, c_kv=None, dev_error_count=None, stream=None) -> None:
+    _check(load().kv_rms_norm_rope_cache(
+        ctypes.byref(params), _ptr(_bits16(kv), None, "kv"), _ptr(_bits16(gamma), None, "gamma"),
+        _ptr(_bits16(cos), None, "cos"), _ptr(_bits16(sin), None, "sin"), _ptr(index, torch.int64, "index"),
+        _ptr(_bits16(k_cache), None, "k_cache"), _ptr(_bits16(ckv_cache), None, "ckv_cache"),
+        _ptr(k_rope_scale, torch.float32, "k_rope_scale"), _ptr(c_kv_scale, torch.float32, "c_kv_scale"),
+        _ptr(k_rope_offset, torch.float32, "k_rope_offset"), _ptr(c_kv_offset, torch.float32, "c_kv_offset"),
+        _ptr(_bits16(v_optional), None, "v_optional"), _ptr(_bits16(k_rope), None, "k_rope"),
+        _ptr(_bits16(c_kv), None, "c_kv"), _ptr(dev_error_count, torch.int32, "dev_error_count"),
+        _stream(stream)))

@@ -1,0 +1,110 @@
+"""Device-side set-up for one operator call: uploads a seeded case (``synth``)
+to HBM, allocates outputs and workspace, and invokes the C-ABI through
+``native``.  Buffer management only; every step of the computation runs in the
+library's kernels.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import native, synth
+
+
+def to_dev(x: np.ndarray | None, device: str = "cuda") -> torch.Tensor | None:
+    """numpy -> device tensor; uint16 arrays (bf16 bit patterns) become torch.bfloat16."""
+    if x is None:
+        return None
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(x).to(device)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class QkvRun:
+    """Device buffers for one qkv_cte_mx call of a synth.QKVCase."""
+
+    def __init__(self, case: synth.QKVCase, device: str = "cuda", stream=None):
+        self.case = case
+        c = case
+        self.params = native.QkvCteMxParams(
+            B=c.B, S=c.S, H=c.H, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
+            head_dim=c.head_dim,
+            q_norm=native.RA_NORM_RMS_ACROSS_HEADS if c.q_norm else native.RA_NORM_NONE,
+            k_norm=native.RA_NORM_RMS_ACROSS_HEADS if c.k_norm else native.RA_NORM_NONE,
+            fused_rope=1 if c.fused_rope else 0, norm_eps=c.eps, output_layout=native.RA_LAYOUT_BSD)
+        self.a = to_dev(c.a, device)
+        self.a_scale = to_dev(c.a_scale, device)
+        w = to_dev(c.w, device)
+        e = to_dev(c.w_block_exp, device)
+        self.w_packed = native.qkv_cte_mx_pack_weight(w, e, stream=stream)
+        torch.cuda.synchronize()
+        del w, e
+        self.weight_scales = to_dev(c.weight_scales, device)
+        self.bias = to_dev(c.bias, device)
+        self.cos = to_dev(c.cos, device) if c.fused_rope else None
+        self.sin = to_dev(c.sin, device) if c.fused_rope else None
+        self.q_gamma = to_dev(c.q_gamma, device) if c.q_norm else None
+        self.k_gamma = to_dev(c.k_gamma, device) if c.k_norm else None
+        self.out = torch.empty((c.T, c.I), dtype=torch.bfloat16, device=device)
+        nws = native.qkv_cte_mx_workspace_bytes(self.params)
+        self.workspace = torch.zeros(nws, dtype=torch.uint8, device=device)
+
+    def run(self, stream=None) -> None:
+        native.qkv_cte_mx(self.params, self.a, self.a_scale, self.w_packed, self.weight_scales,
+                          self.bias, self.cos, self.sin, self.q_gamma, self.k_gamma, self.out,
+                          self.workspace, stream)
+
+    def project(self, stream=None) -> None:
+        native.qkv_cte_mx_project(self.params, self.a, self.a_scale, self.w_packed,
+                                  self.weight_scales, self.bias, self.out, self.workspace, stream)
+
+    def norm_rope(self, stream=None) -> None:
+        native.qkv_cte_mx_norm_rope(self.params, self.cos, self.sin, self.q_gamma, self.k_gamma,
+                                    self.out, self.workspace, stream)
+
+    def status(self, stream=None) -> int:
+        return native.qkv_cte_mx_status(self.workspace, stream)
+
+
+class KvRun:
+    """Device buffers for one kv_rms_norm_rope_cache call of a synth.KVCase."""
+
+    def __init__(self, case: synth.KVCase, device: str = "cuda"):
+        self.case = c = case
+        qk, qv = c.k_scale is not None, c.v_scale is not None
+        self.params = native.KvRmsNormRopeCacheParams(
+            B=c.B, N=c.N, S=c.S, Dkv=c.Dkv, Dv=c.Dv, rope_size=c.rope_size, variant=c.variant,
+            cache_mode=synth.CACHE_MODES[c.cache_mode], block_num=c.block_num,
+            block_size=c.block_size, kv_dtype=native.RA_BF16,
+            k_cache_dtype=native.RA_INT8 if qk else native.RA_BF16,
+            ckv_cache_dtype=native.RA_INT8 if qv else native.RA_BF16,
+            epsilon=c.eps, is_output_kv=1 if c.is_output_kv else 0)
+        self.kv = to_dev(c.kv, device)
+        self.gamma = to_dev(c.gamma, device)
+        self.cos = to_dev(c.cos, device)
+        self.sin = to_dev(c.sin, device)
+        self.index = to_dev(c.index, device)
+        self.k_cache = to_dev(c.k_cache, device)
+        self.ckv_cache = to_dev(c.ckv_cache, device)
+        self.k_scale = to_dev(c.k_scale, device)
+        self.k_offset = to_dev(c.k_offset, device)
+        self.v_scale = to_dev(c.v_scale, device)
+        self.v_offset = to_dev(c.v_offset, device)
+        self.v = to_dev(c.v, device)
+        rows = (c.B, c.N, c.S)
+        self.k_rope = (torch.empty(rows + (c.k_width,), dtype=torch.bfloat16, device=device)
+                       if c.is_output_kv else None)
+        self.c_kv = (torch.empty(rows + (c.ckv_width,), dtype=torch.bfloat16, device=device)
+                     if c.is_output_kv else None)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def run(self, stream=None) -> None:
+        native.kv_rms_norm_rope_cache(
+            self.params, self.kv, self.gamma, self.cos, self.sin, self.index, self.k_cache,
+            self.ckv_cache, self.k_scale, self.v_scale, self.k_offset, self.v_offset, self.v,
+            self.k_rope, self.c_kv, self.err, stream)

@@ -1,0 +1,177 @@
+"""The C-ABI boundary, checked on the CPU (no GPU needed, no kernel launched).
+
+* the library loads and exports every function include/rope_attention.h declares;
+* every rejection rule of the header returns its status code and a message.
+Each rejected call has exactly one violation and fails host-side validation,
+so the placeholder device addresses used here are never dereferenced or
+launched on.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rope_attention_gb300 import native
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "rope_attention.h")
+A16 = 0x10000  # 16-byte aligned placeholder address (never dereferenced)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from rope_attention_gb300 import build
+    build.build()
+    return native.load()
+
+
+def test_exports_every_declared_function(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in the header but not exported"
+    assert sorted(names) == sorted(native.EXPORTS)
+    assert native.ra_abi_version() == 1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = native._LIB
+    native._LIB = None
+    try:
+        with pytest.raises(FileNotFoundError):
+            native.load(str(tmp_path / "librope_attention.so"))
+    finally:
+        native._LIB = saved
+
+
+def qp(**kw):
+    base = dict(B=1, S=256, H=512, num_heads=4, num_kv_heads=4, head_dim=64,
+                q_norm=1, k_norm=1, fused_rope=1, norm_eps=1e-6, output_layout=0)
+    base.update(kw)
+    return native.QkvCteMxParams(**base)
+
+
+def status_and_msg(L, st):
+    return st, L.ra_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=100), -1), (dict(H=0), -1), (dict(B=0), -1), (dict(S=0), -1), (dict(num_heads=0), -1),
+    (dict(num_kv_heads=-1), -1), (dict(head_dim=24), -1), (dict(q_norm=3), -1),
+    (dict(num_kv_heads=0, k_norm=1), -1), (dict(output_layout=1), -2), (dict(output_layout=7), -1),
+    (dict(norm_eps=-1.0), -1), (dict(norm_eps=float("nan")), -1), (dict(fused_rope=2), -1),
+])
+def test_qkv_params_rejected(L, kw, code):
+    n = ctypes.c_size_t()
+    st, msg = status_and_msg(L, L.qkv_cte_mx_workspace_bytes(ctypes.byref(qp(**kw)), ctypes.byref(n)))
+    assert st == code and msg
+
+
+def test_workspace_formula(L):
+    n = ctypes.c_size_t()
+    p = qp(B=1, S=32760, H=5120, num_heads=40, num_kv_heads=40, head_dim=128)
+    assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
+    tiles = -(-(80 * 128) // 240)
+    assert n.value == 256 + tiles * 32760 * 8
+    p = qp(q_norm=0, k_norm=0)
+    assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value == 256
+
+
+def ws_bytes(L, p):
+    n = ctypes.c_size_t()
+    assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
+    return n.value
+
+
+def qkv_call(L, p, **over):
+    args = dict(a=A16, a_scale=A16, w=A16, ws=None, bias=A16, cos=A16, sin=A16, qg=A16, kg=A16,
+                out=A16, work=A16, nwork=ws_bytes(L, p))
+    args.update(over)
+    return L.qkv_cte_mx(ctypes.byref(p), args["a"], args["a_scale"], args["w"], args["ws"], args["bias"],
+                        args["cos"], args["sin"], args["qg"], args["kg"], args["out"], args["work"],
+                        args["nwork"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(cos=None), -1), (dict(sin=None), -1), (dict(qg=None), -1), (dict(kg=None), -1),
+    (dict(a=None), -1), (dict(out=None), -1), (dict(work=None), -1), (dict(w=None), -1),
+    (dict(a=A16 + 1), -3), (dict(out=A16 + 8), -3), (dict(bias=A16 + 2), -3), (dict(cos=A16 + 4), -3),
+    (dict(work=A16 + 4), -3), (dict(nwork=16), -4),
+])
+def test_qkv_call_rejected(L, over, code):
+    st, msg = status_and_msg(L, qkv_call(L, qp(), **over))
+    assert st == code and msg
+
+
+def test_project_and_norm_rejections(L):
+    p = qp()
+    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, A16, A16, 8, None)
+    assert st == -4
+    st = L.qkv_cte_mx_norm_rope(ctypes.byref(p), None, A16, A16, A16, A16, A16, ws_bytes(L, p), None)
+    assert st == -1
+    v = ctypes.c_int32()
+    assert L.qkv_cte_mx_status(None, None, ctypes.byref(v)) == -1
+
+
+def test_pack_weight_rejections(L):
+    n = ctypes.c_size_t()
+    assert L.qkv_cte_mx_packed_weight_bytes(100, 384, ctypes.byref(n)) == -1
+    assert L.qkv_cte_mx_packed_weight_bytes(256, 100, ctypes.byref(n)) == -1
+    assert L.qkv_cte_mx_packed_weight_bytes(256, 384, ctypes.byref(n)) == 0
+    need = n.value
+    assert need >= 256 * 384
+    assert L.qkv_cte_mx_pack_weight(A16, A16, 256, 384, A16, need - 1, None) == -4
+    assert L.qkv_cte_mx_pack_weight(A16, A16, 256, 384, A16 + 4, need, None) == -3
+    assert L.qkv_cte_mx_pack_weight(None, A16, 256, 384, A16, need, None) == -1
+
+
+def kp(**kw):
+    base = dict(B=2, N=1, S=64, Dkv=576, Dv=512, rope_size=64, variant=1, cache_mode=2,
+                block_num=4, block_size=32, kv_dtype=0, k_cache_dtype=0, ckv_cache_dtype=0,
+                epsilon=1e-5, is_output_kv=0)
+    base.update(kw)
+    return native.KvRmsNormRopeCacheParams(**base)
+
+
+def kv_call(L, p, **over):
+    args = dict(kv=A16, gamma=A16, cos=A16, sin=A16, index=A16, kc=A16, cc=A16, ks=None, vs=None,
+                ko=None, vo=None, v=None, kr=None, ckv=None, err=None)
+    args.update(over)
+    return L.kv_rms_norm_rope_cache(ctypes.byref(p), args["kv"], args["gamma"], args["cos"], args["sin"],
+                                    args["index"], args["kc"], args["cc"], args["ks"], args["vs"],
+                                    args["ko"], args["vo"], args["v"], args["kr"], args["ckv"],
+                                    args["err"], None)
+
+
+@pytest.mark.parametrize("pkw,over,code", [
+    (dict(N=2), {}, -1),                                        # V1 needs N == 1
+    (dict(variant=2, N=3, Dkv=192, Dv=128), dict(v=A16), -1),   # V2 needs N in {1,2,4,8}
+    (dict(variant=2, N=2, Dkv=192, Dv=128), {}, -1),            # V2 needs v_optional
+    ({}, dict(v=A16), -1),                                      # V1 takes no v_optional
+    (dict(variant=3), {}, -1),
+    (dict(B=0), {}, -1), (dict(S=0), {}, -1),                   # no empty tensors
+    (dict(rope_size=6, Dv=570), {}, -1),                        # rope width (multiple of 8 here)
+    (dict(Dv=500), {}, -1),                                     # V1: Dv = Dkv - rope
+    ({}, dict(ko=A16), -1),                                     # offset without scale
+    ({}, dict(vs=A16), -1),                                     # quant with a bf16 cache
+    (dict(k_cache_dtype=2), {}, -1),                            # int8 cache without scale
+    (dict(k_cache_dtype=2, ckv_cache_dtype=2, block_size=48), dict(ks=A16, vs=A16), -1),
+    (dict(block_size=24), {}, -1),                              # bf16 caches need %16
+    (dict(block_size=1), {}, -1),
+    (dict(cache_mode=0), {}, -2), (dict(cache_mode=3), {}, -2),  # Norm, PA_NZ not built
+    (dict(kv_dtype=1, k_cache_dtype=1, ckv_cache_dtype=1), {}, -2),  # fp16 not built
+    (dict(is_output_kv=1), {}, -1),                             # needs k_rope / c_kv
+    (dict(epsilon=-1.0), {}, -1),
+    ({}, dict(kv=A16 + 2), -3), ({}, dict(index=A16 + 4), -3), ({}, dict(kc=A16 + 8), -3),
+    ({}, dict(kv=None), -1), ({}, dict(index=None), -1),
+])
+def test_kv_rejected(L, pkw, over, code):
+    st, msg = status_and_msg(L, kv_call(L, kp(**pkw), **over))
+    assert st == code and msg, (st, msg)

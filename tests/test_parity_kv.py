@@ -1,0 +1,91 @@
+"""GPU parity: kv_rms_norm_rope_cache (C-ABI) against the fp64 oracle.
+
+Small cases span several warps, ragged row counts, both variants, both paged
+layouts, bf16 and int8 caches, symmetric and asymmetric quantisation, skipped
+(-1) and out-of-range slots.  The full-size DeepSeek-V3 MLA (V1) and separate
+k/v (V2) workloads are compared element by element over every output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity_util import check_kv
+from rope_attention_gb300 import runner, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(case):
+    r = runner.KvRun(case)
+    r.run()
+    torch.cuda.synchronize()
+    return r
+
+
+SMALL = [
+    # name, kwargs
+    ("v1_bf16_bnsd", dict(variant=1, B=3, N=1, S=37, Dkv=576, Dv=512, block_size=16, block_num=8)),
+    ("v1_int8_bnsd", dict(variant=1, B=2, N=1, S=45, Dkv=576, Dv=512, block_size=32, block_num=4,
+                          quant_k=True, quant_v=True)),
+    ("v1_int8_sym", dict(variant=1, B=2, N=1, S=33, Dkv=576, Dv=512, block_size=32, block_num=4,
+                         quant_k=True, quant_v=True, offsets=False)),
+    ("v1_kq_only", dict(variant=1, B=2, N=1, S=20, Dkv=576, Dv=512, block_size=32, block_num=2,
+                        quant_k=True)),
+    ("v1_pa", dict(variant=1, B=2, N=1, S=19, Dkv=576, Dv=512, block_size=16, block_num=4,
+                   cache_mode="PA")),
+    ("v1_small_dims", dict(variant=1, B=2, N=1, S=11, Dkv=136, Dv=128, rope_size=8, block_size=16,
+                           block_num=2)),
+    ("v2_int8_bnsd", dict(variant=2, B=2, N=8, S=29, Dkv=192, Dv=128, block_size=32, block_num=4,
+                          quant_k=True, quant_v=True)),
+    ("v2_bf16_pa", dict(variant=2, B=3, N=4, S=21, Dkv=192, Dv=128, block_size=16, block_num=8,
+                        cache_mode="PA")),
+    ("v2_vq_only_n2", dict(variant=2, B=2, N=2, S=40, Dkv=192, Dv=128, block_size=32, block_num=4,
+                           quant_v=True)),
+    ("v2_n1_wide", dict(variant=2, B=1, N=1, S=50, Dkv=384, Dv=256, block_size=16, block_num=4)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("skip", [0.0, 0.25])
+def test_small(name, kw, skip):
+    case = synth.make_kv(name, 100 + len(name), skip_frac=skip, **kw)
+    check_kv(case, run_case(case), name)
+
+
+def test_out_of_range_index_counted_not_written():
+    case = synth.make_kv("bad", 7, variant=2, B=2, N=2, S=16, Dkv=192, Dv=128, block_size=16,
+                         block_num=4, skip_frac=0.1)
+    case.index[3] = case.block_num * case.block_size + 5
+    case.index[9] = -4
+    check_kv(case, run_case(case), "bad-index")
+
+
+def test_no_output_kv():
+    case = synth.make_kv("nokv", 8, variant=1, B=2, N=1, S=24, Dkv=576, Dv=512, block_size=16,
+                         block_num=4, is_output_kv=False)
+    check_kv(case, run_case(case), "no-output-kv")
+
+
+@pytest.mark.parametrize("quant", [False, True], ids=["bf16", "int8"])
+def test_full_mla_v1(quant):
+    """kv [32,1,4096,576], PA_BNSD bs=128, 131072 slots, is_output_kv."""
+    case = synth.kv_mla_v1(quant=quant)
+    stats = check_kv(case, run_case(case), "mla_v1")
+    print("tie differences:", stats)
+
+
+def test_full_sep_v2():
+    """kv [8,8,4096,192], v [8,8,4096,128], int8 per-head quantisation, PA_BNSD bs=128."""
+    case = synth.kv_sep_v2(is_output_kv=True)
+    stats = check_kv(case, run_case(case), "sep_v2")
+    print("tie differences:", stats)
+
+
+def test_repeat_call_is_idempotent():
+    case = synth.make_kv("rep", 9, variant=1, B=2, N=1, S=64, Dkv=576, Dv=512, block_size=32,
+                         block_num=4, quant_k=True, quant_v=True)
+    r = run_case(case)
+    first = r.k_cache.clone(), r.ckv_cache.clone()
+    r.run()
+    torch.cuda.synchronize()
+    assert torch.equal(first[0], r.k_cache) and torch.equal(first[1], r.ckv_cache)

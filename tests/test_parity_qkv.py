@@ -1,0 +1,112 @@
+"""GPU parity: qkv_cte_mx (C-ABI) against the fp64 oracle.
+
+Small cases are compared in full: they span several 128-row and 240-column
+tiles, ragged row and column tails, single-segment calls, per-channel weight
+scales, no bias, norm without RoPE and RoPE without norm.  The full-size Wan
+workloads are compared on a deterministic row sample (first 128 rows, last
+256 rows covering the M tail, 640 random rows) with every column, so the
+across-heads norms are checked exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity_util import as_f64, check_bf16, check_qkv, qkv_reference
+from rope_attention_gb300 import runner, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def run_full(case, split=False):
+    r = runner.QkvRun(case)
+    if split:
+        r.project()
+        r.norm_rope()
+    else:
+        r.run()
+    torch.cuda.synchronize()
+    assert r.status() == 0
+    return r
+
+
+def test_tiny_config():
+    """S=128, H=256, n_q=n_kv=2, d=64, 1-D RoPE (the small self-attention workload)."""
+    case = synth.qkv_tiny()
+    r = run_full(case)
+    check_qkv(case, as_f64(r.out), qkv_reference(case), "tiny")
+
+
+SMALL = [
+    ("ragged_rows_cols", dict(S=333, H=384, num_heads=3, num_kv_heads=1, head_dim=64)),
+    ("batch2_ragged", dict(B=2, S=100, H=256, num_heads=2, num_kv_heads=2, head_dim=128)),
+    ("weight_scales_nobias", dict(S=256, H=512, num_heads=4, num_kv_heads=2, head_dim=64,
+                                  weight_scales=True, bias=False)),
+    ("norm_no_rope", dict(S=200, H=256, num_heads=4, num_kv_heads=4, head_dim=64, rope=None)),
+    ("rope_no_norm", dict(S=130, H=256, num_heads=2, num_kv_heads=2, head_dim=64,
+                          q_norm=False, k_norm=False)),
+    ("q_norm_only", dict(S=129, H=256, num_heads=2, num_kv_heads=2, head_dim=64, k_norm=False)),
+    ("single_segment_q", dict(S=300, H=512, num_heads=6, num_kv_heads=0, head_dim=128, rope=None)),
+    ("single_segment_v", dict(S=77, H=256, num_heads=2, num_kv_heads=0, head_dim=128, rope=None,
+                              q_norm=False)),
+    ("one_row", dict(S=1, H=128, num_heads=1, num_kv_heads=1, head_dim=16)),
+    ("wide_heads", dict(S=260, H=640, num_heads=5, num_kv_heads=5, head_dim=128)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
+def test_small(name, kw):
+    case = synth.make_qkv(name, 200 + len(name), **kw)
+    r = run_full(case)
+    check_qkv(case, as_f64(r.out), qkv_reference(case), name)
+
+
+def test_split_entry_points_match_fused():
+    case = synth.make_qkv("split", 5, S=250, H=256, num_heads=3, num_kv_heads=3, head_dim=64)
+    a = run_full(case)
+    b = run_full(case, split=True)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
+def test_deterministic():
+    case = synth.make_qkv("det", 6, S=500, H=512, num_heads=4, num_kv_heads=4, head_dim=128)
+    r = run_full(case)
+    first = r.out.clone()
+    r.run()
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), r.out.view(torch.int16))
+
+
+def test_projection_only_matches_oracle_projection():
+    """With norms and RoPE off, qkv_cte_mx_project is the whole operator."""
+    case = synth.make_qkv("proj", 7, S=389, H=1024, num_heads=4, num_kv_heads=4, head_dim=128,
+                          rope=None, q_norm=False, k_norm=False, weight_scales=True)
+    r = runner.QkvRun(case)
+    r.project()
+    torch.cuda.synchronize()
+    ref = qkv_reference(case)
+    check_bf16(as_f64(r.out), ref, "projection")
+
+
+def _sampled(case, what):
+    r = run_full(case)
+    rows = synth.sample_rows(case.T, seed=123)
+    got = as_f64(r.out[torch.from_numpy(rows).cuda()])
+    del r
+    torch.cuda.empty_cache()
+    return check_qkv(case, got, qkv_reference(case, rows), what)
+
+
+def test_wan480_self_attention_sampled():
+    """S=32760 (21x30x52), H=5120, 40+40+40 heads of 128, 3-D RoPE."""
+    _sampled(synth.qkv_wan480(), "wan480")
+
+
+def test_wan_cross_attention_sampled():
+    """Separate Q (S=32760, normed), K (L=512, normed) and V (L=512) projections, no RoPE."""
+    for case in synth.qkv_wan_cross():
+        _sampled(case, case.name)
+
+
+def test_wan720_self_attention_sampled():
+    """S=75600 (21x45x80), the bench workload."""
+    _sampled(synth.qkv_wan720(), "wan720")
