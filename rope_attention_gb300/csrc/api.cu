@@ -57,6 +57,8 @@ struct QkvShape {
   int32_t q_w, k_w;
   int32_t q_end, k_end;
   int32_t n_part_tiles;
+  int32_t s_begin, s_end;   // Q/K columns carried in fp32 scratch between the passes
+  size_t scratch_offset;
   size_t workspace;
 };
 
@@ -96,7 +98,15 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   const bool any_norm = p->q_norm != RA_NORM_NONE || p->k_norm != RA_NORM_NONE;
   const int32_t normed_end = p->k_norm != RA_NORM_NONE ? s->k_end : s->q_end;
   s->n_part_tiles = any_norm ? (normed_end + ra::kProjBN - 1) / ra::kProjBN : 0;
-  s->workspace = ra::kWorkspaceHeader + static_cast<size_t>(s->n_part_tiles) * T * sizeof(float2);
+  // segments the second pass rewrites stay in fp32 between the passes
+  const bool do_q = p->q_norm != RA_NORM_NONE || p->fused_rope;
+  const bool do_k = p->num_kv_heads > 0 && (p->k_norm != RA_NORM_NONE || p->fused_rope);
+  s->s_begin = do_q ? 0 : s->q_w;
+  s->s_end = do_k ? s->k_end : (do_q ? s->q_w : s->q_w);
+  if (!do_q && !do_k) s->s_begin = s->s_end = 0;
+  const size_t part = static_cast<size_t>(s->n_part_tiles) * T * sizeof(float2);
+  s->scratch_offset = ra::kWorkspaceHeader + ((part + 255) / 256) * 256;
+  s->workspace = s->scratch_offset + static_cast<size_t>(s->s_end - s->s_begin) * T * sizeof(float);
   return RA_OK;
 }
 
@@ -153,6 +163,9 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
   L.q_end = s.q_end;
   L.k_end = p->num_kv_heads > 0 ? s.k_end : s.q_end;
   L.n_part_tiles = s.n_part_tiles;
+  L.scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + s.scratch_offset);
+  L.s_begin = s.s_begin;
+  L.s_end = s.s_end;
   L.wait_ns = g_wait_ns.load();
   const char* why = "launch failed";
   cudaError_t e = ra::launch_qkv_project(L, st, &why);
@@ -183,6 +196,9 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
   L.k_norm = p->k_norm != RA_NORM_NONE;
   L.rope = p->fused_rope;
   L.n_part_tiles = s.n_part_tiles;
+  L.scratch = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + s.scratch_offset);
+  L.s_begin = s.s_begin;
+  L.s_w = s.s_end - s.s_begin;
   L.eps = p->norm_eps;
   cudaError_t e = ra::launch_qk_norm_rope(L, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm/rope launch");

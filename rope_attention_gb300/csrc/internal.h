@@ -23,11 +23,13 @@ struct ProjLaunch {
   const uint8_t* sf;           // packed block-scale images
   const float* weight_scales;  // [I] or null
   const uint16_t* bias;        // [I] bf16 or null
-  uint16_t* out;               // [T, I] bf16
+  uint16_t* out;               // [T, I] bf16 (columns outside [s_begin, s_end))
+  float* scratch;              // [T, s_end - s_begin] fp32: the Q/K columns the second pass rewrites
   float2* partials;            // [n_part_tiles, T] (sum sq Q, sum sq K)
   int32_t* status;
   int64_t T, H, I;
   int32_t q_end, k_end;        // Q = [0, q_end), K = [q_end, k_end) output columns
+  int32_t s_begin, s_end;      // columns kept in fp32 scratch for the norm/RoPE pass
   int32_t n_part_tiles;
   int64_t wait_ns;
 };
@@ -40,7 +42,8 @@ cudaError_t launch_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int
 
 // ------------------------------------------------------------ norm + RoPE apply (K2)
 struct NormRopeLaunch {
-  uint16_t* out;               // [T, I] bf16, updated in place
+  uint16_t* out;               // [T, I] bf16: receives the normed / rotated Q and K columns
+  const float* scratch;        // [T, s_w] fp32 un-normalised Q|K columns from the projection
   const float2* partials;      // [n_part_tiles, T]
   const float* cos;            // [T, d]
   const float* sin;
@@ -50,6 +53,7 @@ struct NormRopeLaunch {
   int32_t head_dim, num_q_heads, num_k_heads;
   int32_t q_norm, k_norm, rope;
   int32_t n_part_tiles;
+  int32_t s_begin, s_w;
   float eps;
 };
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);

@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const 
     // (4) slot of this token
     const int64_t slot = __ldg(p.index + b * p.S + s);
     const bool to_cache = slot >= 0 && slot < slots;
-    if (!to_cache && slot != -1 && lane == 0 && p.err_count != nullptr) atomicAdd(p.err_count, 1);
+    if (!to_cache && slot != -1 && n == 0 && lane == 0 && p.err_count != nullptr)
+      atomicAdd(p.err_count, 1);  // once per token, not per head
     const int64_t blk = to_cache ? slot / p.block_size : 0;
     const int64_t off = to_cache ? slot % p.block_size : 0;
     const int64_t cache_row = p.mode == 2 ? (blk * p.N + n) * p.block_size + off

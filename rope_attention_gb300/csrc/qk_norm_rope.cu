@@ -6,7 +6,9 @@
 //   y          = x * inv_rms * gamma          (segment-wide gamma, per channel);
 //   out_lo     = y_lo * cos_lo - y_hi * sin_lo,  out_hi = y_hi * cos_hi + y_lo * sin_hi,
 //                lanes (j, j + d/2) of every head, cos/sin shared by all heads.
-// V is never read.  The per-token sums arrive as per-column-tile partials
+// The un-normalised Q|K columns arrive in fp32 (the projection keeps them in
+// the workspace rather than as bf16 in ``out``, so the only bf16 rounding is
+// the final one); V is never touched.  The per-token sums arrive as per-column-tile partials
 // written by the projection epilogue; they are reduced here in a fixed order,
 // so the result is deterministic.
 //
@@ -42,6 +44,14 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 __device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
   const float4 a = __ldg(reinterpret_cast<const float4*>(p));
   const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// streaming read of the fp32 scratch (read once, not kept in L1)
+__device__ __forceinline__ void load8s(const float* p, float (&f)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
   f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
@@ -103,11 +113,10 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
       for (int tl = 0; tl < ntok; ++tl) {
         const int64_t t = t0 + tl;
         uint16_t* row = p.out + t * p.I;
-        const uint4 ulo = *reinterpret_cast<const uint4*>(row + col);
-        const uint4 uhi = *reinterpret_cast<const uint4*>(row + col + half);
+        const float* src = p.scratch + t * p.s_w + (col - p.s_begin);
         float xlo[8], xhi[8], clo[8], chi[8], slo[8], shi[8];
-        unpack8(ulo, xlo);
-        unpack8(uhi, xhi);
+        load8s(src, xlo);
+        load8s(src + half, xhi);
         const float* cs = p.cos + t * d + 8 * u;
         const float* sn = p.sin + t * d + 8 * u;
         load8f(cs, clo);
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
         const int64_t t = t0 + tl;
         uint16_t* row = p.out + t * p.I;
         float x[8];
-        unpack8(*reinterpret_cast<const uint4*>(row + col), x);
+        load8s(p.scratch + t * p.s_w + (col - p.s_begin), x);
         const float inv = s_inv[tl][is_k ? 1 : 0];
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = x[j] * inv * g[j];

@@ -6,7 +6,9 @@
 // read out, then stored to HBM; Design 1a: per-token sum(x^2) over the whole Q
 // and K segments of the un-normalised output):
 //
-//   out[t, i]     = bf16( acc[t, i] * a_scale[t] * wch[i] + bias[i] )
+//   v[t, i]       = acc[t, i] * a_scale[t] * wch[i] + bias[i]
+//   out[t, i]     = bf16(v)  for V (and any segment the second pass leaves alone),
+//   scratch[t, i] = v (fp32) for the Q/K columns the norm/RoPE pass rewrites
 //   acc[t, i]     = sum_h e4m3(a[t, h]) * e4m3(w[h, i]) * 2^(e[h/32, i] - 127)
 //   partial[j, t] = ( sum over Q columns of tile j of v^2, sum over K columns of v^2 )
 //
@@ -80,10 +82,12 @@ struct Params {
   const float* wch;
   const uint16_t* bias;
   uint16_t* out;
+  float* scratch;
   float2* partials;
   int32_t* status;
   int32_t T, I, num_k, num_m, num_n;
   int32_t q_end, k_end, n_part;
+  int32_t s_begin, s_end;
   uint64_t wait_ns;
 };
 
@@ -340,7 +344,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __gri
         }
         if (col0 < p.q_end) ssq += sq;
         else if (col0 < p.k_end) ssk += sq;
-        if (row_ok) {
+        if (row_ok && col0 >= p.s_begin && col0 < p.s_end) {
+          // Q/K columns the norm/RoPE pass will rewrite: keep them in fp32
+          float4* dst = reinterpret_cast<float4*>(
+              p.scratch + static_cast<size_t>(row) * (p.s_end - p.s_begin) + (col0 - p.s_begin));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else if (row_ok) {
           uint4 o0, o1;
           o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
           o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
@@ -469,6 +479,7 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.wch = L.weight_scales;
   p.bias = L.bias;
   p.out = L.out;
+  p.scratch = L.scratch;
   p.partials = L.partials;
   p.status = L.status;
   p.T = static_cast<int32_t>(L.T);
@@ -479,6 +490,8 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.q_end = L.q_end;
   p.k_end = L.k_end;
   p.n_part = L.n_part_tiles;
+  p.s_begin = L.s_begin;
+  p.s_end = L.s_end;
   p.wait_ns = static_cast<uint64_t>(L.wait_ns);
 
   static std::once_flag attr_once;
