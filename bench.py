@@ -163,10 +163,14 @@ def run_ours(args):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     with Clocks(local) as clk:
+        # the sampler's start-up leaves the GPU idle for a moment: warm up again so the
+        # timed steps start at full clocks
+        for _ in range(args.warmup):
+            step()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
