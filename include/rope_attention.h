@@ -156,6 +156,29 @@ ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cach
  * projection wait gave up since the last read, else RA_OK. */
 ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_status);
 
+/* qkv_cte_mx for callers that cannot allocate device memory.  The pages have
+ * no counterpart; this entry point exists for host code that must not call
+ * cudaMalloc where it runs the operator (a plugin of an inference runtime
+ * that owns all device memory, or a serving loop that cannot afford
+ * cudaMalloc's implicit device synchronisation).  It takes the same arguments
+ * as qkv_cte_mx minus the workspace and allocates nothing: its scratch is a
+ * static 32 MiB device array inside this library, held on every GPU that
+ * loads the library until the process exits.
+ *   - Problems whose qkv_cte_mx_workspace_bytes exceeds 32 MiB are rejected
+ *     with RA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the array: calls that overlap on the GPU (unordered
+ *     streams or threads) race and give undefined results.  Calls ordered on
+ *     one stream are independent (the status word is cleared by each call).
+ *   - A device wait timeout is recorded only in the shared array and is not
+ *     reported by this entry point. */
+ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
+                             const void* w_packed, const float* weight_scales, const uint16_t* bias,
+                             const float* cos_cache, const float* sin_cache, const float* q_gamma,
+                             const float* k_gamma, uint16_t* out, void* stream);
+
 /* Test hook: time limit, in nanoseconds, of each device pipeline wait in the
  * projection kernel (default 2e9).  Values < 1000 are raised to 1000. */
 void ra_set_wait_timeout_ns(int64_t ns);

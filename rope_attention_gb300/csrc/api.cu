@@ -207,6 +207,12 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
 
 }  // namespace
 
+namespace ra {
+void set_last_error(int code, const char* where, const char* what) {
+  fail(static_cast<ra_status>(code), "%s: %s", where, what);
+}
+}  // namespace ra
+
 extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }

@@ -87,4 +87,7 @@ cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream
 
 int device_sm_count();
 
+// Sets the thread-local message returned by ra_last_error() ("where: what").
+void set_last_error(int code, const char* where, const char* what);
+
 }  // namespace ra

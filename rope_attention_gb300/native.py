@@ -27,7 +27,7 @@ RA_CACHE_PA, RA_CACHE_PA_BNSD = 1, 2
 EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns",
            "qkv_cte_mx_packed_weight_bytes", "qkv_cte_mx_pack_weight", "qkv_cte_mx_workspace_bytes",
            "qkv_cte_mx", "qkv_cte_mx_project", "qkv_cte_mx_norm_rope", "qkv_cte_mx_status",
-           "kv_rms_norm_rope_cache"]
+           "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache"]
 
 
 class RAError(RuntimeError):
@@ -79,6 +79,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qkv_cte_mx_project": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, sz, P]),
         "qkv_cte_mx_norm_rope": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, sz, P]),
         "qkv_cte_mx_status": (i32, [P, P, ctypes.POINTER(i32)]),
+        "qkv_cte_mx_noalloc": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, P, P]),
         "kv_rms_norm_rope_cache": (i32, [ctypes.POINTER(KvRmsNormRopeCacheParams), P, P, P, P, P,
                                          P, P, P, P, P, P, P, P, P, P, P]),
     }
@@ -179,6 +180,17 @@ def qkv_cte_mx_norm_rope(params, cos_cache, sin_cache, q_gamma, k_gamma, out, wo
         _ptr(sin_cache, torch.float32, "sin_cache"), _ptr(q_gamma, torch.float32, "q_gamma"),
         _ptr(k_gamma, torch.float32, "k_gamma"), _ptr(_bits16(out), None, "out"),
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def qkv_cte_mx_noalloc(params, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache,
+                       q_gamma, k_gamma, out, stream=None) -> None:
+    """qkv_cte_mx with the library's static device workspace (no allocation anywhere)."""
+    _check(load().qkv_cte_mx_noalloc(
+        ctypes.byref(params), _ptr(a, torch.uint8, "a"), _ptr(a_scale, torch.float32, "a_scale"),
+        _ptr(w_packed, torch.uint8, "w_packed"), _ptr(weight_scales, torch.float32, "weight_scales"),
+        _ptr(_bits16(bias), None, "bias"), _ptr(cos_cache, torch.float32, "cos_cache"),
+        _ptr(sin_cache, torch.float32, "sin_cache"), _ptr(q_gamma, torch.float32, "q_gamma"),
+        _ptr(k_gamma, torch.float32, "k_gamma"), _ptr(_bits16(out), None, "out"), _stream(stream)))
 
 
 def qkv_cte_mx_status(workspace: torch.Tensor, stream=None) -> int:
