@@ -97,7 +97,7 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   s->k_end = s->q_w + s->k_w;
   const bool any_norm = p->q_norm != RA_NORM_NONE || p->k_norm != RA_NORM_NONE;
   const int32_t normed_end = p->k_norm != RA_NORM_NONE ? s->k_end : s->q_end;
-  s->n_part_tiles = any_norm ? (normed_end + ra::kProjBN - 1) / ra::kProjBN : 0;
+  s->n_part_tiles = any_norm ? (normed_end + ra::kPartCols - 1) / ra::kPartCols : 0;
   // segments the second pass rewrites stay in fp32 between the passes
   const bool do_q = p->q_norm != RA_NORM_NONE || p->fused_rope;
   const bool do_k = p->num_kv_heads > 0 && (p->k_norm != RA_NORM_NONE || p->fused_rope);

@@ -9,9 +9,9 @@ namespace ra {
 
 // ------------------------------------------------------------ projection (K1)
 // Tile shape of the block-scaled FP8 GEMM; also fixes the packed weight layout.
-constexpr int kProjBM = 128;          // token rows per tile (one TMEM lane per row)
-constexpr int kProjBN = 240;          // output columns per tile
+constexpr int kProjBN = 256;          // output columns per CTA-pair tile (256 rows x 256 columns)
 constexpr int kProjBK = 128;          // contraction elements (= bytes) per pipeline stage
+constexpr int kPartCols = 128;        // columns covered by one sum-of-squares partial
 constexpr int kSfChunkBytes = 512;    // 128 columns x 4 block scales, tcgen05.cp image
 constexpr int kSfStageBytes = ((kProjBN + 127) / 128) * kSfChunkBytes;
 constexpr int kWorkspaceHeader = 256; // status word + padding, ahead of the partial sums
@@ -20,12 +20,12 @@ struct ProjLaunch {
   const uint8_t* a;            // [T, H] e4m3
   const float* a_scale;        // [T]
   const uint8_t* w_t;          // [I, H] e4m3 (packed, K-major)
-  const uint8_t* sf;           // packed block-scale images
+  const uint8_t* sf;           // packed block-scale images (1 KB per column tile and K stage)
   const float* weight_scales;  // [I] or null
   const uint16_t* bias;        // [I] bf16 or null
   uint16_t* out;               // [T, I] bf16 (columns outside [s_begin, s_end))
   float* scratch;              // [T, s_end - s_begin] fp32: the Q/K columns the second pass rewrites
-  float2* partials;            // [n_part_tiles, T] (sum sq Q, sum sq K)
+  float2* partials;            // [n_part_tiles, T] (sum sq Q, sum sq K) per 128-column block
   int32_t* status;
   int64_t T, H, I;
   int32_t q_end, k_end;        // Q = [0, q_end), K = [q_end, k_end) output columns

@@ -6,26 +6,35 @@
 // read out, then stored to HBM; Design 1a: per-token sum(x^2) over the whole Q
 // and K segments of the un-normalised output):
 //
+//   acc[t, i]     = sum_h e4m3(a[t, h]) * e4m3(w[h, i]) * 2^(e[h/32, i] - 127)
 //   v[t, i]       = acc[t, i] * a_scale[t] * wch[i] + bias[i]
 //   out[t, i]     = bf16(v)  for V (and any segment the second pass leaves alone),
 //   scratch[t, i] = v (fp32) for the Q/K columns the norm/RoPE pass rewrites
-//   acc[t, i]     = sum_h e4m3(a[t, h]) * e4m3(w[h, i]) * 2^(e[h/32, i] - 127)
-//   partial[j, t] = ( sum over Q columns of tile j of v^2, sum over K columns of v^2 )
+//   partial[j, t] = ( sum of v^2 over the Q columns of 128-column block j,
+//                     sum of v^2 over its K columns )
 //
 // GB300 design (not the page's NKI schedule):
-//  * persistent CTAs (one per SM), 128 x 240 output tiles, grouped rasterisation
-//    so that concurrently running tiles share A rows and W columns in L2;
-//  * warp 0: TMA producer (A and W tiles with 128-byte swizzle, plus the W block
-//    scales as a plain bulk copy) into a 4-stage shared-memory ring;
-//  * warp 1: allocates 512 TMEM columns and issues tcgen05.mma
-//    kind::mxf8f6f4 (M=128, N=240, K=32 per instruction) from one thread; W's
-//    ue8m0 scales go through tcgen05.cp into TMEM each stage; A's MX scale is
-//    the constant 2^0 (its fp32 row scale is applied in the epilogue, since it is
-//    constant along K);
-//  * warps 2-5: epilogue, one TMEM lane quadrant each; two accumulator buffers
-//    let the epilogue of tile i overlap the mainloop of tile i+1.
-// Every pipeline wait is bounded in time; on expiry the CTA records an error in
-// the status word, drains its in-flight copies and MMAs, frees TMEM and exits.
+//  * CTA pairs (clusters of 2) run tcgen05.mma.cta_group::2 kind::mxf8f6f4 on
+//    256 x 256 output tiles (M=256, N=256, K=32 per instruction): each CTA holds
+//    128 rows of A and 128 rows (columns of the output) of W in shared memory, so
+//    each SM stages 33 KB per 128-deep K step instead of the 46 KB a single-SM
+//    128 x 240 tile needs; the pair's accumulator is split by rows across the
+//    two SMs' TMEM;
+//  * persistent pairs (one pair per two SMs), grouped rasterisation;
+//  * warp 0 (both CTAs): TMA producer into a 6-stage ring; the loads of both
+//    CTAs complete on the leader CTA's full barrier;
+//  * warp 1: allocates TMEM (512 columns, pair-wide); in the leader CTA one
+//    thread issues the MMAs and copies W's ue8m0 block scales into TMEM each
+//    stage (tcgen05.cp); A's MX scale is the constant 2^0 (its fp32 row scale is
+//    applied in the epilogue, since it is constant along K); commits multicast
+//    to both CTAs;
+//  * warps 2-9 (both CTAs): epilogue, two warps per TMEM lane quadrant, each
+//    owning 128 of the 256 columns; they pull the whole accumulator into
+//    registers first and release TMEM before the math and stores, so the next
+//    tile's MMAs start after a short drain.
+// Every pipeline wait is bounded in time; on expiry a CTA records an error in
+// the status word, waits (bounded) for the copies and MMAs it started, frees
+// TMEM with its peer and exits.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -37,47 +46,50 @@
 namespace ra {
 namespace {
 
-constexpr int BM = kProjBM;
-constexpr int BN = kProjBN;
+constexpr int BM = 128;               // output rows per CTA (a pair covers 256)
+constexpr int PAIR_M = 2 * BM;
+constexpr int BN = kProjBN;           // output columns per pair tile
+constexpr int BN_HALF = BN / 2;       // W rows staged per CTA
 constexpr int BK = kProjBK;
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
+constexpr int B_BYTES = BN_HALF * BK;
 constexpr int SF_BYTES = kSfStageBytes;
-constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SF_BYTES;
-constexpr int NUM_ACC = 2;
-constexpr int ACC_STRIDE = BN;           // TMEM columns between accumulator buffers
-constexpr int SFA_COL = NUM_ACC * BN;    // 4 columns of A scales
-constexpr int SFB_COL = SFA_COL + 8;     // two 8-column slots of W scales
+constexpr uint32_t STAGE_TX = 2u * (A_BYTES + B_BYTES + SF_BYTES);  // both CTAs, on the leader's barrier
+constexpr int ACC_COL = 0;
+constexpr int SFA_COL = BN;           // 4 columns of A scales
+constexpr int SFB_COL = BN + 8;       // two 8-column slots of W scales
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_WARP0 = 2;
-constexpr int GROUP_M = 16;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int EPI_COLS = BN / 2;      // columns per epilogue warp
+constexpr int GROUP_M = 8;
 
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
 constexpr int SMEM_SF = SMEM_B + STAGES * B_BYTES;
 constexpr int SMEM_SFA = SMEM_SF + STAGES * SF_BYTES;
 constexpr int SMEM_BAR = SMEM_SFA + 512;
-constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+constexpr int NUM_BARS = 2 * STAGES + 3;
 constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
 constexpr int SMEM_USED = SMEM_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 
-static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
+static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 static_assert(SFB_COL + 16 <= TMEM_COLS, "TMEM budget");
-static_assert(BN % 16 == 0 && BN <= 256 && BN > 128, "MMA N and scale-image shape");
+static_assert(BN == 256 && SF_BYTES == 1024, "pair tile shape");
+static_assert(kPartCols == EPI_COLS, "one partial per epilogue warp and row");
 
 // Instruction descriptor, block-scaled kinds: A/B format E4M3 (0) in bits
 // [7,10)/[10,13), K-major operands, N>>3 in [17,23), scale type UE8M0 (1) at
 // bit 23, M>>4 in [24,29); the scale-factor ids go in [29,31) (A) and [4,6) (B).
-constexpr uint32_t kIdesc = (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t(BM >> 4) << 24);
+constexpr uint32_t kIdesc = (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t(PAIR_M >> 4) << 24);
 
 struct Params {
   CUtensorMap tmap_a;   // [T, H] bytes, box 128 x 128, 128-byte swizzle
-  CUtensorMap tmap_b;   // [I, H] bytes, box 128 x BN
-  const uint8_t* sf;
+  CUtensorMap tmap_b;   // [I, H] bytes, box 128 x 128, 128-byte swizzle
+  CUtensorMap tmap_sf;  // scale images viewed as [rows, 256] bytes, box 256 x 2
   const float* a_scale;
   const float* wch;
   const uint16_t* bias;
@@ -147,7 +159,18 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
   }
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __grid_constant__ Params p) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    qkv_project_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -157,16 +180,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __gri
   const uint32_t sSF = s_base + SMEM_SF;
   const uint32_t sSFA = s_base + SMEM_SFA;
   const uint32_t bar0 = s_base + SMEM_BAR;
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * NUM_ACC);
+  const uint32_t accf_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t acce_bar = bar0 + 8u * (2 * STAGES + 1);
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + NUM_ACC + a); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = leader of the pair
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+  // The leader stages W rows [0, 128) of the tile and the peer rows [128, 256); both
+  // stage the full 256-column scale image, since each SM's MMA half applies the
+  // scales of all N columns.
+  const uint32_t b_half = rank;
   const uint64_t drain_ns = 200000000ull;
 
   if (warp == 0 && lane == 0) {
@@ -174,52 +205,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __gri
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int a = 0; a < NUM_ACC; ++a) {
-      mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), 4);
-    }
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, 2 * NUM_EPI_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&p.tmap_a);
     prefetch_tensormap(&p.tmap_b);
+    prefetch_tensormap(&p.tmap_sf);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
   }
-  if (warp >= EPI_WARP0) {
+  if (threadIdx.x >= 64 && threadIdx.x < 64 + 128) {
     // A's MX scale factors: ue8m0 127 (= 1.0) for every row and block
-    uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + SMEM_SFA);
-    sfa[threadIdx.x - EPI_WARP0 * 32] = 0x7F7F7F7Fu;
+    reinterpret_cast<uint32_t*>(smem + SMEM_SFA)[threadIdx.x - 64] = 0x7F7F7F7Fu;
     fence_proxy_async_smem();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = p.num_m * p.num_n;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
+      const uint32_t leader_full0 = map_to_rank(full_bar(0), 0);
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
         int mb, nt;
         tile_coords(tile, p.num_m, p.num_n, mb, nt);
-        const uint8_t* sf_tile = p.sf + static_cast<size_t>(nt) * p.num_k * SF_BYTES;
         for (int kb = 0; kb < p.num_k; ++kb) {
           if (!wait_one(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
-          tma_load_2d(sA + stage * A_BYTES, &p.tmap_a, full_bar(stage), kb * BK, mb * BM);
-          tma_load_2d(sB + stage * B_BYTES, &p.tmap_b, full_bar(stage), kb * BK, nt * BN);
-          bulk_load(sSF + stage * SF_BYTES, sf_tile + static_cast<size_t>(kb) * SF_BYTES, SF_BYTES,
-                    full_bar(stage));
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+          const uint32_t fb = leader_full0 + 8u * stage;
+          tma_load_2d_pair(sA + stage * A_BYTES, &p.tmap_a, fb, kb * BK, mb * PAIR_M + rank * BM);
+          tma_load_2d_pair(sB + stage * B_BYTES, &p.tmap_b, fb, kb * BK, nt * BN + b_half * BN_HALF);
+          const int sf_row = (nt * p.num_k + kb) * (SF_BYTES / 256);
+          const uint32_t sf_dst = sSF + stage * SF_BYTES;
+          tma_load_2d_pair(sf_dst, &p.tmap_sf, fb, 0, sf_row);
+          tma_load_2d_pair(sf_dst + 512u, &p.tmap_sf, fb, 0, sf_row + 2);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -228,30 +260,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __gri
           }
         }
       }
-      if (!ok) {
-        // every copy started here must land before this CTA's shared memory is released
+      if (!ok && leader) {
+        // the leader's full barriers count both CTAs' bytes: let every armed load land
         for (int s = 0; s < STAGES; ++s)
           if (armed & (1u << s)) wait_drain(full_bar(s), (armed_parity >> s) & 1u, drain_ns);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      tc_cp_32x128b_warpx4(tmem + SFA_COL, sdesc_scale_rows(sSFA));
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (leader && lane == 0) {
+      tc_cp_pair_32x128b_warpx4(tmem + SFA_COL, sdesc_scale_rows(sSFA));
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-        const int acc = local & 1;
-        const uint32_t acc_parity = (local >> 1) & 1;
-        if (!wait_one(acce_bar(acc), acc_parity ^ 1u, p.wait_ns, abort_flag)) {
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs, ++local) {
+        if (!wait_one(acce_bar, (static_cast<uint32_t>(local) & 1u) ^ 1u, p.wait_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * ACC_STRIDE;
         for (int kb = 0; kb < p.num_k; ++kb) {
           if (!wait_one(full_bar(stage), phase, p.wait_ns, abort_flag)) {
             ok = false;
@@ -260,53 +289,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __gri
           tc_fence_after();
           const uint32_t sfb = tmem + SFB_COL + (kb & 1) * 8;
           const uint32_t sf_s = sSF + stage * SF_BYTES;
-          tc_cp_32x128b_warpx4(sfb, sdesc_scale_rows(sf_s));
-          tc_cp_32x128b_warpx4(sfb + 4, sdesc_scale_rows(sf_s + kSfChunkBytes));
+          tc_cp_pair_32x128b_warpx4(sfb, sdesc_scale_rows(sf_s));
+          tc_cp_pair_32x128b_warpx4(sfb + 4, sdesc_scale_rows(sf_s + kSfChunkBytes));
           const uint32_t a_s = sA + stage * A_BYTES;
           const uint32_t b_s = sB + stage * B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint32_t idesc = kIdesc | (uint32_t(kk) << 29) | (uint32_t(kk) << 4);
-            tc_mma_mxf8(d_tmem, sdesc_kmajor_sw128(a_s + kk * 32), sdesc_kmajor_sw128(b_s + kk * 32),
-                        idesc, tmem + SFA_COL, sfb, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_pair_mxf8(tmem + ACC_COL, sdesc_kmajor_sw128(a_s + kk * 32),
+                             sdesc_kmajor_sw128(b_s + kk * 32), idesc, tmem + SFA_COL, sfb,
+                             (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(empty_bar(stage));
+          tc_commit_pair_multicast(empty_bar(stage), 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(accf_bar(acc));
+        if (ok) tc_commit_pair_multicast(accf_bar, 0x3);
       }
-      // all MMAs issued here must finish before TMEM is released
-      tc_commit(drain_bar);
+      // every MMA and copy issued here must finish before TMEM is released
+      tc_commit_pair(drain_bar);
       wait_drain(drain_bar, 0, drain_ns);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
-    const int row_in_tile = quad * 32 + lane;
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quad = warp & 3;           // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    const int chalf = ew >> 2;           // which 128 of the tile's 256 columns
+    const int row_in_cta = quad * 32 + lane;
+    const uint32_t acce_leader = map_to_rank(acce_bar, 0);
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++local) {
       int mb, nt;
       tile_coords(tile, p.num_m, p.num_n, mb, nt);
-      const int acc = local & 1;
-      const uint32_t acc_parity = (local >> 1) & 1;
-      if (!wait_warp(accf_bar(acc), acc_parity, p.wait_ns, abort_flag)) break;
+      if (!wait_warp(accf_bar, static_cast<uint32_t>(local) & 1u, p.wait_ns, abort_flag)) break;
       tc_fence_after();
-      const int row = mb * BM + row_in_tile;
+      uint32_t r[EPI_COLS];
+      const uint32_t t_base =
+          tmem + ACC_COL + chalf * EPI_COLS + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < EPI_COLS / 16; ++c) tmem_ld16(t_base + c * 16, r + c * 16);
+      tmem_ld_wait();
+      // the accumulator is in registers: hand TMEM back to the MMA issuer now
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_leader);
+
+      const int row = mb * PAIR_M + static_cast<int>(rank) * BM + row_in_cta;
       const bool row_ok = row < p.T;
       const float as = row_ok ? __ldg(p.a_scale + row) : 0.f;
       float ssq = 0.f, ssk = 0.f;
-      const uint32_t t_base = tmem + acc * ACC_STRIDE + (static_cast<uint32_t>(quad * 32) << 16);
       uint16_t* out_row = p.out + static_cast<size_t>(row_ok ? row : 0) * p.I;
-      for (int c = 0; c < BN / 16; ++c) {
-        const int col0 = nt * BN + c * 16;
-        if (col0 >= p.I) break;  // warp-uniform: ragged last column tile
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(t_base + c * 16, r);
-        tmem_ld_wait();
+      const int col_base = nt * BN + chalf * EPI_COLS;
+#pragma unroll
+      for (int c = 0; c < EPI_COLS / 16; ++c) {
+        const int col0 = col_base + c * 16;
+        if (col0 >= p.I) break;  // ragged last column tile; warp-uniform
         float wch[16], bia[16];
         if (p.wch != nullptr) {
           const float4* w4 = reinterpret_cast<const float4*>(p.wch + col0);
@@ -339,7 +379,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __gri
         float sq = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          v[j] = fmaf(__uint_as_float(r[j]) * as, wch[j], bia[j]);
+          v[j] = fmaf(__uint_as_float(r[c * 16 + j]) * as, wch[j], bia[j]);
           sq = fmaf(v[j], v[j], sq);
         }
         if (col0 < p.q_end) ssq += sq;
@@ -361,18 +401,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) qkv_project_kernel(const __gri
           dst[1] = o1;
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(acc));
-      if (nt < p.n_part && row_ok)
-        p.partials[static_cast<size_t>(nt) * p.T + row] = make_float2(ssq, ssk);
+      const int part = nt * 2 + chalf;
+      if (part < p.n_part && row_ok)
+        p.partials[static_cast<size_t>(part) * p.T + row] = make_float2(ssq, ssk);
     }
   }
 
   __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) {
+    // a wait gave up: give any copy still in flight (possibly signalling the peer) time to land
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
   if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, 1);
 }
@@ -432,7 +478,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                  uint32_t box_inner, uint32_t box_outer) {
+                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -440,8 +486,8 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -469,12 +515,14 @@ cudaError_t launch_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int
 
 cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why) {
   Params p{};
-  if (!make_tmap_2d(&p.tmap_a, L.a, L.H, L.T, BK, BM) ||
-      !make_tmap_2d(&p.tmap_b, L.w_t, L.H, L.I, BK, BN)) {
+  const int num_n = static_cast<int>((L.I + BN - 1) / BN), num_k = static_cast<int>(L.H / BK);
+  const uint64_t sf_rows = static_cast<uint64_t>(num_n) * num_k * (SF_BYTES / 256);
+  if (!make_tmap_2d(&p.tmap_a, L.a, L.H, L.T, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&p.tmap_b, L.w_t, L.H, L.I, BK, BN_HALF, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&p.tmap_sf, L.sf, 256, sf_rows, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE)) {
     *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;
   }
-  p.sf = L.sf;
   p.a_scale = L.a_scale;
   p.wch = L.weight_scales;
   p.bias = L.bias;
@@ -484,9 +532,9 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.status = L.status;
   p.T = static_cast<int32_t>(L.T);
   p.I = static_cast<int32_t>(L.I);
-  p.num_k = static_cast<int32_t>(L.H / BK);
-  p.num_m = static_cast<int32_t>((L.T + BM - 1) / BM);
-  p.num_n = static_cast<int32_t>((L.I + BN - 1) / BN);
+  p.num_k = num_k;
+  p.num_m = static_cast<int32_t>((L.T + PAIR_M - 1) / PAIR_M);
+  p.num_n = num_n;
   p.q_end = L.q_end;
   p.k_end = L.k_end;
   p.n_part = L.n_part_tiles;
@@ -505,8 +553,8 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
     return attr_err;
   }
   const int num_tiles = p.num_m * p.num_n;
-  const int grid = std::min(num_tiles, device_sm_count());
-  qkv_project_kernel<<<grid, NUM_THREADS, SMEM_ALLOC, stream>>>(p);
+  const int pairs = std::max(1, std::min(num_tiles, device_sm_count() / 2));
+  qkv_project_kernel<<<2 * pairs, NUM_THREADS, SMEM_ALLOC, stream>>>(p);
   return cudaGetLastError();
 }
 

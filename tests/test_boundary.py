@@ -78,7 +78,7 @@ def test_workspace_formula(L):
     n = ctypes.c_size_t()
     p = qp(B=1, S=32760, H=5120, num_heads=40, num_kv_heads=40, head_dim=128)
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    tiles = -(-(80 * 128) // 240)
+    tiles = -(-(80 * 128) // 128)
     part = tiles * 32760 * 8
     assert n.value == 256 + -(-part // 256) * 256 + 32760 * 80 * 128 * 4
     p = qp(q_norm=0, k_norm=0, fused_rope=0)
@@ -88,7 +88,7 @@ def test_workspace_formula(L):
     assert n.value == 256 + 100 * 512 * 4
     p = qp(S=100, q_norm=1, k_norm=0, fused_rope=0)   # Q only
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    assert n.value == 256 + 1792 + 100 * 256 * 4   # 2 column tiles of partials, padded to 256
+    assert n.value == 256 + 1792 + 100 * 256 * 4   # 2 partial column blocks, padded to 256
 
 
 def ws_bytes(L, p):
