@@ -342,7 +342,7 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
       return fail(RA_ERR_INVALID_ARG, "V2 (separate kv) supports N in {1, 2, 4, 8}");
     if (!v_optional) return fail(RA_ERR_INVALID_ARG, "V2 needs v_optional");
     if (R > p->Dkv) return fail(RA_ERR_INVALID_ARG, "rope_size exceeds Dkv");
-    if (p->Dv > 8 * 32 * 64) return fail(RA_ERR_INVALID_ARG, "Dv too large");
+    if (p->Dv > 1024) return fail(RA_ERR_INVALID_ARG, "V2 needs Dv <= 1024 in this build");
     rms = p->Dkv;
   } else {
     return fail(RA_ERR_INVALID_ARG, "variant must be 1 or 2");

@@ -13,7 +13,9 @@
 // Quantisation uses the fp32 value (before any bf16 rounding); round() is
 // round-half-to-even.
 //
-// GB300 mapping: one warp per (b, n, s) row.  Every lane moves 16-byte chunks
+// GB300 mapping: persistent warps, each walking (b, n, s) rows with a stride of
+// the whole grid and loading the next row's data while it processes the current
+// one (the op is latency-bound otherwise: a row is only 0.6-1.4 KB).  Every lane moves 16-byte chunks
 // (8 bf16); the RMS reduction is a warp shuffle tree; lane l < rope_size/8
 // owns interleaved pairs 4l..4l+3, whose outputs land at positions 4l and
 // rope_size/2 + 4l of the de-interleaved result, written as 8-byte (bf16) or
@@ -96,6 +98,52 @@ __device__ __forceinline__ void store_vals(void* row_base, int ch, const float* 
   }
 }
 
+// Everything one row needs from HBM, loaded as raw 16/8-byte vectors so the
+// next row's loads can be in flight while the current row is processed.
+template <int CPL>
+struct RowIn {
+  uint4 x[CPL];            // chunks lane + 32 i of the RMSNorm part of kv
+  uint4 xr;                // V1: the lane's chunk of the raw RoPE part
+  uint4 v[CPL];            // V2: chunks lane + 32 i of v_optional
+  uint2 c1, c2, s1, s2;    // cos/sin for pairs 4l..4l+3 at j and R/2 + j
+  int64_t slot;
+};
+
+template <int VARIANT, int CPL>
+__device__ __forceinline__ void load_row(const KvLaunch& p, int64_t row, int lane, int rms,
+                                         int rms_chunks, int v_chunks, int rope_lanes,
+                                         RowIn<CPL>& in) {
+  const uint16_t* x = p.kv + row * p.Dkv;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = lane + 32 * i;
+    in.x[i] = c < rms_chunks ? __ldcs(reinterpret_cast<const uint4*>(x + 8 * c)) : z;
+  }
+  if (VARIANT == 1)
+    in.xr = lane < rope_lanes ? __ldcs(reinterpret_cast<const uint4*>(x + rms + 8 * lane)) : z;
+  if (VARIANT == 2) {
+    const uint16_t* vrow = p.v + row * p.Dv;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      in.v[i] = c < v_chunks ? __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * c)) : z;
+    }
+  }
+  if (lane < rope_lanes) {
+    const int half = p.R / 2;
+    const uint16_t* cs = p.cos + row * p.R;
+    const uint16_t* sn = p.sin + row * p.R;
+    in.c1 = __ldcs(reinterpret_cast<const uint2*>(cs + 4 * lane));
+    in.c2 = __ldcs(reinterpret_cast<const uint2*>(cs + half + 4 * lane));
+    in.s1 = __ldcs(reinterpret_cast<const uint2*>(sn + 4 * lane));
+    in.s2 = __ldcs(reinterpret_cast<const uint2*>(sn + half + 4 * lane));
+  }
+  const int64_t s = row % p.S;
+  const int64_t b = row / (p.S * p.N);
+  in.slot = __ldg(p.index + b * p.S + s);
+}
+
 template <int VARIANT, bool QK, bool QV, int CPL>
 __global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const KvLaunch p) {
   const int lane = threadIdx.x & 31;
@@ -105,48 +153,53 @@ __global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const 
   const int rms_chunks = rms / 8;
   const int kw = VARIANT == 1 ? R : static_cast<int>(p.Dkv);
   const int cw = VARIANT == 1 ? rms : static_cast<int>(p.Dv);
+  const int v_chunks = VARIANT == 2 ? cw / 8 : 0;
   const int64_t slots = p.block_num * p.block_size;
   const size_t k_elt = QK ? 1 : 2, c_elt = QV ? 1 : 2;
 
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); row < rows;
-       row += static_cast<int64_t>(gridDim.x) * kWarps) {
-    const int64_t s = row % p.S;
-    const int64_t bn = row / p.S;
-    const int n = static_cast<int>(bn % p.N);
-    const int64_t b = bn / p.N;
-    const uint16_t* x = p.kv + row * p.Dkv;
+  // gamma is the same for every row: keep the lane's chunks in registers
+  uint4 gam[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = lane + 32 * i;
+    gam[i] = c < rms_chunks ? __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * c))
+                            : make_uint4(0, 0, 0, 0);
+  }
+
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
+  int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  RowIn<CPL> cur;
+  if (row < rows) load_row<VARIANT, CPL>(p, row, lane, rms, rms_chunks, v_chunks, rope_lanes, cur);
+
+  while (row < rows) {
+    const int64_t next = row + stride;
+    RowIn<CPL> nxt;
+    if (next < rows) load_row<VARIANT, CPL>(p, next, lane, rms, rms_chunks, v_chunks, rope_lanes, nxt);
+
+    const int n = static_cast<int>((row / p.S) % p.N);
 
     // (1) RmsNorm
     float y[CPL][8];
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      const int c = lane + 32 * i;
-      if (c < rms_chunks) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(x + 8 * c)), y[i]);
+      unpack8(cur.x[i], y[i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ss = fmaf(y[i][j], y[i][j], ss);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) y[i][j] = 0.f;
-      }
+      for (int j = 0; j < 8; ++j) ss = fmaf(y[i][j], y[i][j], ss);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float inv = rsqrtf(ss / static_cast<float>(rms) + p.eps);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      const int c = lane + 32 * i;
-      if (c < rms_chunks) {
-        float g[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * c)), g);
+      float g[8];
+      unpack8(gam[i], g);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) y[i][j] = y[i][j] * inv * g[j];
-      }
+      for (int j = 0; j < 8; ++j) y[i][j] = y[i][j] * inv * g[j];
     }
 
     // (4) slot of this token
-    const int64_t slot = __ldg(p.index + b * p.S + s);
+    const int64_t slot = cur.slot;
     const bool to_cache = slot >= 0 && slot < slots;
     if (!to_cache && slot != -1 && n == 0 && lane == 0 && p.err_count != nullptr)
       atomicAdd(p.err_count, 1);  // once per token, not per head
@@ -167,21 +220,15 @@ __global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const 
     if (lane < rope_lanes) {
       float r[8];
       if (VARIANT == 1) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(x + rms + 8 * lane)), r);
+        unpack8(cur.xr, r);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) r[j] = y[0][j];
       }
-      const uint16_t* cs = p.cos + row * R;
-      const uint16_t* sn = p.sin + row * R;
-      const uint2 c1 = __ldg(reinterpret_cast<const uint2*>(cs + 4 * lane));
-      const uint2 c2 = __ldg(reinterpret_cast<const uint2*>(cs + half + 4 * lane));
-      const uint2 s1 = __ldg(reinterpret_cast<const uint2*>(sn + 4 * lane));
-      const uint2 s2 = __ldg(reinterpret_cast<const uint2*>(sn + half + 4 * lane));
-      const float cc1[4] = {bf16_lo(c1.x), bf16_hi(c1.x), bf16_lo(c1.y), bf16_hi(c1.y)};
-      const float cc2[4] = {bf16_lo(c2.x), bf16_hi(c2.x), bf16_lo(c2.y), bf16_hi(c2.y)};
-      const float ss1[4] = {bf16_lo(s1.x), bf16_hi(s1.x), bf16_lo(s1.y), bf16_hi(s1.y)};
-      const float ss2[4] = {bf16_lo(s2.x), bf16_hi(s2.x), bf16_lo(s2.y), bf16_hi(s2.y)};
+      const float cc1[4] = {bf16_lo(cur.c1.x), bf16_hi(cur.c1.x), bf16_lo(cur.c1.y), bf16_hi(cur.c1.y)};
+      const float cc2[4] = {bf16_lo(cur.c2.x), bf16_hi(cur.c2.x), bf16_lo(cur.c2.y), bf16_hi(cur.c2.y)};
+      const float ss1[4] = {bf16_lo(cur.s1.x), bf16_hi(cur.s1.x), bf16_lo(cur.s1.y), bf16_hi(cur.s1.y)};
+      const float ss2[4] = {bf16_lo(cur.s2.x), bf16_hi(cur.s2.x), bf16_lo(cur.s2.y), bf16_hi(cur.s2.y)};
       float o1[4], o2[4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -210,19 +257,21 @@ __global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const 
         }
       }
       // ckv <- v_optional
-      const uint16_t* vrow = p.v + row * p.Dv;
-      for (int c = lane; c < cw / 8; c += 32) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(vrow + 8 * c));
-        if (to_cache) {
-          if constexpr (QV) {
-            float f[8];
-            unpack8(u, f);
-            store_vals<true, 8>(c_row, 8 * c, f, vsc, vof);
-          } else {
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(c_row) + 8 * c) = u;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < v_chunks) {
+          if (to_cache) {
+            if constexpr (QV) {
+              float f[8];
+              unpack8(cur.v[i], f);
+              store_vals<true, 8>(c_row, 8 * c, f, vsc, vof);
+            } else {
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(c_row) + 8 * c) = cur.v[i];
+            }
           }
+          if (ckv_row != nullptr) *reinterpret_cast<uint4*>(ckv_row + 8 * c) = cur.v[i];
         }
-        if (ckv_row != nullptr) *reinterpret_cast<uint4*>(ckv_row + 8 * c) = u;
       }
     } else {
       // ckv <- y
@@ -235,18 +284,39 @@ __global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const 
         }
       }
     }
+    cur = nxt;
+    row = next;
   }
 }
 
+// persistent grid: as many blocks as fit on the GPU at once, capped by the row count
+template <typename K>
+unsigned persistent_grid(K kernel, int64_t rows) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t want = (rows + kWarps - 1) / kWarps;
+  const int64_t cap = static_cast<int64_t>(per_sm) * device_sm_count();
+  return static_cast<unsigned>(want < cap ? want : cap);
+}
+
+template <int VARIANT, bool QK, bool QV, int CPL>
+cudaError_t launch_one(const KvLaunch& L, cudaStream_t st) {
+  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, QK, QV, CPL>;
+  const unsigned grid = persistent_grid(kernel, L.B * L.N * L.S);
+  kernel<<<grid, kThreads, 0, st>>>(L);
+  return cudaGetLastError();
+}
+
 template <int VARIANT, bool QK, bool QV>
-cudaError_t launch_cpl(const KvLaunch& L, int cpl, unsigned grid, cudaStream_t st) {
+cudaError_t launch_cpl(const KvLaunch& L, int cpl, unsigned, cudaStream_t st) {
   switch (cpl) {
-    case 1: kv_rms_norm_rope_cache_kernel<VARIANT, QK, QV, 1><<<grid, kThreads, 0, st>>>(L); break;
-    case 2: kv_rms_norm_rope_cache_kernel<VARIANT, QK, QV, 2><<<grid, kThreads, 0, st>>>(L); break;
-    case 4: kv_rms_norm_rope_cache_kernel<VARIANT, QK, QV, 4><<<grid, kThreads, 0, st>>>(L); break;
+    case 1: return launch_one<VARIANT, QK, QV, 1>(L, st);
+    case 2: return launch_one<VARIANT, QK, QV, 2>(L, st);
+    case 4: return launch_one<VARIANT, QK, QV, 4>(L, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 template <int VARIANT>
@@ -262,11 +332,11 @@ cudaError_t launch_variant(const KvLaunch& L, int cpl, unsigned grid, cudaStream
 
 cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream) {
   const int64_t rms = L.variant == 1 ? L.Dkv - L.R : L.Dkv;
-  const int64_t chunks = rms / 8;
+  int64_t chunks = rms / 8;
+  if (L.variant == 2 && L.Dv / 8 > chunks) chunks = L.Dv / 8;  // v_optional rides the same lanes
   const int cpl = chunks <= 32 ? 1 : (chunks <= 64 ? 2 : 4);
-  const int64_t rows = L.B * L.N * L.S;
-  const int64_t want = (rows + kWarps - 1) / kWarps;
-  const unsigned grid = static_cast<unsigned>(want < 0x7fffffff ? want : 0x7fffffff);
+  if (chunks > 128) return cudaErrorInvalidValue;
+  const unsigned grid = 0;
   return L.variant == 1 ? launch_variant<1>(L, cpl, grid, stream)
                         : launch_variant<2>(L, cpl, grid, stream);
 }
