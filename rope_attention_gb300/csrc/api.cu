@@ -6,7 +6,7 @@
 #include <cstdio>
 #include <string>
 
-#include "../../include/rope_attention.h"
+#include "rope_attention.h"
 #include "internal.h"
 
 namespace ra {

@@ -20,7 +20,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/rope_attention.h"
+#include "rope_attention.h"
 #include "internal.h"
 
 namespace {
