@@ -105,9 +105,8 @@ ra_status qkv_cte_mx_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, i
 
 /* Workspace bytes needed by qkv_cte_mx / qkv_cte_mx_project / qkv_cte_mx_norm_rope.
  * The workspace holds a device status word, the per-token sum-of-squares
- * partials, and the un-normalised Q/K columns in fp32 between the two passes
- * (T * width * 4 bytes, width = the Q and/or K segments that are normed or
- * rotated), so that the only bf16 rounding of Q and K is the final one.
+ * partials (8 bytes per token and 128-column block of Q|K) and one exponent
+ * byte per token and 128-column block (see qkv_cte_mx_project).
  * Zero-fill it once after allocation; the calls keep it consistent. */
 ra_status qkv_cte_mx_workspace_bytes(const qkv_cte_mx_params* p, size_t* bytes);
 
@@ -134,19 +133,23 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
                      void* stream);
 
 /* First half of qkv_cte_mx on its own: O = dequant(A) @ dequant(W) + bias, and the
- * per-token Q / K sums of squares (Design 1a) into the workspace.  Columns of O
- * that the second pass rewrites (Q and/or K when normed or rotated) go to the
- * workspace in fp32; all other columns (V, or everything when norms and RoPE
- * are off -- e.g. the V-only call) go to `out` in bf16. */
+ * per-token Q / K sums of squares (Design 1a) into the workspace.  Columns that
+ * the second pass does not touch (V, or everything when norms and RoPE are off
+ * -- e.g. the V-only call) are final bf16 in `out`.  Columns the second pass
+ * rewrites (Q and/or K when normed or rotated) are held in `out` in an internal
+ * encoding until qkv_cte_mx_norm_rope runs: fp16 of O * 2^-e with a
+ * power-of-two e per (token, 128-column block) kept in the workspace, so the
+ * intermediate carries 11 significant bits and the only bf16 rounding of Q and
+ * K is the final one. */
 ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
                              uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Second half on its own (Design 1b-1c, Design 2): reads the sums of squares
- * and the fp32 Q/K columns left in `workspace` by qkv_cte_mx_project, applies
- * inv_rms * gamma and RoPE, and writes Q and K into `out` as bf16.  V is not
- * touched.  This is the seam where a tensor-parallel all-reduce of the sums
- * would go. */
+ * and exponents left in `workspace` and the encoded Q/K columns of `out` by
+ * qkv_cte_mx_project, applies inv_rms * gamma and RoPE, and writes Q and K back
+ * into `out` as bf16.  V is not touched.  This is the seam where a
+ * tensor-parallel all-reduce of the sums would go. */
 ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cache,
                                const float* sin_cache, const float* q_gamma, const float* k_gamma,
                                uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);

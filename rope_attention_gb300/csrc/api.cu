@@ -57,8 +57,9 @@ struct QkvShape {
   int32_t q_w, k_w;
   int32_t q_end, k_end;
   int32_t n_part_tiles;
-  int32_t s_begin, s_end;   // Q/K columns carried in fp32 scratch between the passes
-  size_t scratch_offset;
+  int32_t s_begin, s_end;   // Q/K columns carried as scaled fp16 between the passes
+  int32_t n_exp_blocks;     // 128-column blocks covering [0, s_end)
+  size_t exps_offset;
   size_t workspace;
 };
 
@@ -104,9 +105,11 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   s->s_begin = do_q ? 0 : s->q_w;
   s->s_end = do_k ? s->k_end : (do_q ? s->q_w : s->q_w);
   if (!do_q && !do_k) s->s_begin = s->s_end = 0;
+  s->n_exp_blocks = (s->s_end + ra::kPartCols - 1) / ra::kPartCols;
   const size_t part = static_cast<size_t>(s->n_part_tiles) * T * sizeof(float2);
-  s->scratch_offset = ra::kWorkspaceHeader + ((part + 255) / 256) * 256;
-  s->workspace = s->scratch_offset + static_cast<size_t>(s->s_end - s->s_begin) * T * sizeof(float);
+  const size_t exps = static_cast<size_t>(s->n_exp_blocks) * T;
+  s->exps_offset = ra::kWorkspaceHeader + ((part + 255) / 256) * 256;
+  s->workspace = s->exps_offset + ((exps + 255) / 256) * 256;
   return RA_OK;
 }
 
@@ -163,7 +166,8 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
   L.q_end = s.q_end;
   L.k_end = p->num_kv_heads > 0 ? s.k_end : s.q_end;
   L.n_part_tiles = s.n_part_tiles;
-  L.scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + s.scratch_offset);
+  L.exps = reinterpret_cast<int8_t*>(static_cast<uint8_t*>(workspace) + s.exps_offset);
+  L.n_exp_blocks = s.n_exp_blocks;
   L.s_begin = s.s_begin;
   L.s_end = s.s_end;
   L.wait_ns = g_wait_ns.load();
@@ -196,9 +200,7 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
   L.k_norm = p->k_norm != RA_NORM_NONE;
   L.rope = p->fused_rope;
   L.n_part_tiles = s.n_part_tiles;
-  L.scratch = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + s.scratch_offset);
-  L.s_begin = s.s_begin;
-  L.s_w = s.s_end - s.s_begin;
+  L.exps = reinterpret_cast<const int8_t*>(static_cast<const uint8_t*>(workspace) + s.exps_offset);
   L.eps = p->norm_eps;
   cudaError_t e = ra::launch_qk_norm_rope(L, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm/rope launch");

@@ -23,14 +23,16 @@ struct ProjLaunch {
   const uint8_t* sf;           // packed block-scale images (1 KB per column tile and K stage)
   const float* weight_scales;  // [I] or null
   const uint16_t* bias;        // [I] bf16 or null
-  uint16_t* out;               // [T, I] bf16 (columns outside [s_begin, s_end))
-  float* scratch;              // [T, s_end - s_begin] fp32: the Q/K columns the second pass rewrites
+  uint16_t* out;               // [T, I]: bf16, except columns [s_begin, s_end) (see below)
+  int8_t* exps;                // [n_exp_blocks, T] power-of-two exponent per 128-column block
   float2* partials;            // [n_part_tiles, T] (sum sq Q, sum sq K) per 128-column block
   int32_t* status;
   int64_t T, H, I;
   int32_t q_end, k_end;        // Q = [0, q_end), K = [q_end, k_end) output columns
-  int32_t s_begin, s_end;      // columns kept in fp32 scratch for the norm/RoPE pass
+  int32_t s_begin, s_end;      // Q/K columns the norm/RoPE pass rewrites: stored as fp16 of
+                               // v * 2^-e, e per (row, 128-column block) in `exps`
   int32_t n_part_tiles;
+  int32_t n_exp_blocks;
   int64_t wait_ns;
 };
 cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why);
@@ -42,8 +44,8 @@ cudaError_t launch_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int
 
 // ------------------------------------------------------------ norm + RoPE apply (K2)
 struct NormRopeLaunch {
-  uint16_t* out;               // [T, I] bf16: receives the normed / rotated Q and K columns
-  const float* scratch;        // [T, s_w] fp32 un-normalised Q|K columns from the projection
+  uint16_t* out;               // [T, I]: scaled fp16 Q/K in, bf16 normed / rotated Q/K out
+  const int8_t* exps;          // [n_exp_blocks, T] exponents of the scaled fp16 encoding
   const float2* partials;      // [n_part_tiles, T]
   const float* cos;            // [T, d]
   const float* sin;
@@ -53,7 +55,6 @@ struct NormRopeLaunch {
   int32_t head_dim, num_q_heads, num_k_heads;
   int32_t q_norm, k_norm, rope;
   int32_t n_part_tiles;
-  int32_t s_begin, s_w;
   float eps;
 };
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);

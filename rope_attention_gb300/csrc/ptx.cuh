@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace ra {
 
@@ -229,6 +230,18 @@ __device__ __forceinline__ void tc_mma_pair_mxf8(uint32_t d_tmem, uint64_t adesc
 }
 
 // ---------------------------------------------------------------- small utils
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// 2^k as a float for |k| <= 126, built from the exponent field
+__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
+// e such that x * 2^-e < 2^15 with x's leading bit at 2^14 (x >= 0 finite); clamped to [-100, 100]
+__device__ __forceinline__ int scale_exponent(float x) {
+  const int be = static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu);  // biased exponent, floor(log2 x) + 127
+  int e = be == 0 ? -100 : be - 127 - 14;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

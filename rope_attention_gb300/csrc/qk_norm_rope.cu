@@ -6,9 +6,10 @@
 //   y          = x * inv_rms * gamma          (segment-wide gamma, per channel);
 //   out_lo     = y_lo * cos_lo - y_hi * sin_lo,  out_hi = y_hi * cos_hi + y_lo * sin_hi,
 //                lanes (j, j + d/2) of every head, cos/sin shared by all heads.
-// The un-normalised Q|K columns arrive in fp32 (the projection keeps them in
-// the workspace rather than as bf16 in ``out``, so the only bf16 rounding is
-// the final one); V is never touched.  The per-token sums arrive as per-column-tile partials
+// The un-normalised Q|K columns arrive in ``out`` as fp16 of v * 2^-e, with one
+// power-of-two exponent per (token, 128-column block) in the workspace: 11
+// significant bits in 2 bytes, so the only bf16 rounding is the final one;
+// V is never touched.  The per-token sums arrive as per-column-tile partials
 // written by the projection epilogue; they are reduced here in a fixed order,
 // so the result is deterministic.
 //
@@ -48,12 +49,19 @@ __device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// streaming read of the fp32 scratch (read once, not kept in L1)
-__device__ __forceinline__ void load8s(const float* p, float (&f)[8]) {
-  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+// 8 values of the projection's scaled fp16 encoding: fp16 code * 2^e
+__device__ __forceinline__ void load8h(const uint16_t* p, float up, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+    f[2 * k] = t.x * up;
+    f[2 * k + 1] = t.y * up;
+  }
+}
+__device__ __forceinline__ float block_up(const NormRopeLaunch& p, int64_t t, int64_t col) {
+  return exp2_int(p.exps[static_cast<size_t>(col / kPartCols) * p.T + t]);
 }
 
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLaunch p) {
@@ -113,10 +121,9 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
       for (int tl = 0; tl < ntok; ++tl) {
         const int64_t t = t0 + tl;
         uint16_t* row = p.out + t * p.I;
-        const float* src = p.scratch + t * p.s_w + (col - p.s_begin);
         float xlo[8], xhi[8], clo[8], chi[8], slo[8], shi[8];
-        load8s(src, xlo);
-        load8s(src + half, xhi);
+        load8h(row + col, block_up(p, t, col), xlo);
+        load8h(row + col + half, block_up(p, t, col + half), xhi);
         const float* cs = p.cos + t * d + 8 * u;
         const float* sn = p.sin + t * d + 8 * u;
         load8f(cs, clo);
@@ -148,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
         const int64_t t = t0 + tl;
         uint16_t* row = p.out + t * p.I;
         float x[8];
-        load8s(p.scratch + t * p.s_w + (col - p.s_begin), x);
+        load8h(row + col, block_up(p, t, col), x);
         const float inv = s_inv[tl][is_k ? 1 : 0];
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = x[j] * inv * g[j];

@@ -9,7 +9,10 @@
 //   acc[t, i]     = sum_h e4m3(a[t, h]) * e4m3(w[h, i]) * 2^(e[h/32, i] - 127)
 //   v[t, i]       = acc[t, i] * a_scale[t] * wch[i] + bias[i]
 //   out[t, i]     = bf16(v)  for V (and any segment the second pass leaves alone),
-//   scratch[t, i] = v (fp32) for the Q/K columns the norm/RoPE pass rewrites
+//   out[t, i]     = fp16(v * 2^-e[b, t]) for the Q/K columns the norm/RoPE pass
+//                   rewrites, with one power-of-two exponent per (row, 128-column
+//                   block b) chosen so the block's largest |v| lands in [2^14, 2^15):
+//                   11 significant bits in the 2 bytes the final bf16 needs
 //   partial[j, t] = ( sum of v^2 over the Q columns of 128-column block j,
 //                     sum of v^2 over its K columns )
 //
@@ -94,11 +97,11 @@ struct Params {
   const float* wch;
   const uint16_t* bias;
   uint16_t* out;
-  float* scratch;
+  int8_t* exps;
   float2* partials;
   int32_t* status;
   int32_t T, I, num_k, num_m, num_n;
-  int32_t q_end, k_end, n_part;
+  int32_t q_end, k_end, n_part, n_exp;
   int32_t s_begin, s_end;
   uint64_t wait_ns;
 };
@@ -343,6 +346,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       float ssq = 0.f, ssk = 0.f;
       uint16_t* out_row = p.out + static_cast<size_t>(row_ok ? row : 0) * p.I;
       const int col_base = nt * BN + chalf * EPI_COLS;
+      // pass 1: dequant, channel scale and bias in place; sums of squares; the largest
+      // magnitude among the columns the norm/RoPE pass will rewrite
+      float amax = 0.f;
 #pragma unroll
       for (int c = 0; c < EPI_COLS / 16; ++c) {
         const int col0 = col_base + c * 16;
@@ -375,32 +381,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) bia[j] = 0.f;
         }
-        float v[16];
-        float sq = 0.f;
+        float sq = 0.f, cmax = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          v[j] = fmaf(__uint_as_float(r[c * 16 + j]) * as, wch[j], bia[j]);
-          sq = fmaf(v[j], v[j], sq);
+          const float v = fmaf(__uint_as_float(r[c * 16 + j]) * as, wch[j], bia[j]);
+          r[c * 16 + j] = __float_as_uint(v);
+          sq = fmaf(v, v, sq);
+          cmax = fmaxf(cmax, fabsf(v));
         }
         if (col0 < p.q_end) ssq += sq;
         else if (col0 < p.k_end) ssk += sq;
-        if (row_ok && col0 >= p.s_begin && col0 < p.s_end) {
-          // Q/K columns the norm/RoPE pass will rewrite: keep them in fp32
-          float4* dst = reinterpret_cast<float4*>(
-              p.scratch + static_cast<size_t>(row) * (p.s_end - p.s_begin) + (col0 - p.s_begin));
+        if (col0 >= p.s_begin && col0 < p.s_end) amax = fmaxf(amax, cmax);
+      }
+      // power-of-two scale for the fp16 encoding: |v| * 2^-e < 2^15
+      const int e = scale_exponent(amax);
+      const float down = exp2_int(-e);
+      // pass 2: stores (fp16 of v * 2^-e for the rewritten Q/K columns, bf16 otherwise)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        } else if (row_ok) {
-          uint4 o0, o1;
+      for (int c = 0; c < EPI_COLS / 16; ++c) {
+        const int col0 = col_base + c * 16;
+        if (col0 >= p.I) break;
+        if (!row_ok) continue;
+        const float* v = reinterpret_cast<const float*>(r + c * 16);
+        uint4 o0, o1;
+        if (col0 >= p.s_begin && col0 < p.s_end) {
+          o0.x = pack_f16x2(v[0] * down, v[1] * down);   o0.y = pack_f16x2(v[2] * down, v[3] * down);
+          o0.z = pack_f16x2(v[4] * down, v[5] * down);   o0.w = pack_f16x2(v[6] * down, v[7] * down);
+          o1.x = pack_f16x2(v[8] * down, v[9] * down);   o1.y = pack_f16x2(v[10] * down, v[11] * down);
+          o1.z = pack_f16x2(v[12] * down, v[13] * down); o1.w = pack_f16x2(v[14] * down, v[15] * down);
+        } else {
           o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
           o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
           o1.x = pack_bf16x2(v[8], v[9]);   o1.y = pack_bf16x2(v[10], v[11]);
           o1.z = pack_bf16x2(v[12], v[13]); o1.w = pack_bf16x2(v[14], v[15]);
-          uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
-          dst[0] = o0;
-          dst[1] = o1;
         }
+        uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
+        dst[0] = o0;
+        dst[1] = o1;
       }
+      const int blk = nt * 2 + chalf;
+      if (blk < p.n_exp && row_ok) p.exps[static_cast<size_t>(blk) * p.T + row] = static_cast<int8_t>(e);
       const int part = nt * 2 + chalf;
       if (part < p.n_part && row_ok)
         p.partials[static_cast<size_t>(part) * p.T + row] = make_float2(ssq, ssk);
@@ -527,7 +547,7 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.wch = L.weight_scales;
   p.bias = L.bias;
   p.out = L.out;
-  p.scratch = L.scratch;
+  p.exps = L.exps;
   p.partials = L.partials;
   p.status = L.status;
   p.T = static_cast<int32_t>(L.T);
@@ -538,6 +558,7 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.q_end = L.q_end;
   p.k_end = L.k_end;
   p.n_part = L.n_part_tiles;
+  p.n_exp = L.n_exp_blocks;
   p.s_begin = L.s_begin;
   p.s_end = L.s_end;
   p.wait_ns = static_cast<uint64_t>(L.wait_ns);

@@ -75,20 +75,20 @@ def test_qkv_params_rejected(L, kw, code):
 
 
 def test_workspace_formula(L):
+    pad = lambda b: -(-b // 256) * 256
     n = ctypes.c_size_t()
     p = qp(B=1, S=32760, H=5120, num_heads=40, num_kv_heads=40, head_dim=128)
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    tiles = -(-(80 * 128) // 128)
-    part = tiles * 32760 * 8
-    assert n.value == 256 + -(-part // 256) * 256 + 32760 * 80 * 128 * 4
+    blocks = (80 * 128) // 128          # 128-column blocks over Q|K
+    assert n.value == 256 + pad(blocks * 32760 * 8) + pad(blocks * 32760)
     p = qp(q_norm=0, k_norm=0, fused_rope=0)
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value == 256
-    p = qp(S=100, q_norm=0, k_norm=0, fused_rope=1)   # RoPE only: Q and K still pass through fp32
+    p = qp(S=100, q_norm=0, k_norm=0, fused_rope=1)   # RoPE only: exponents for Q|K, no sums
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    assert n.value == 256 + 100 * 512 * 4
+    assert n.value == 256 + pad(4 * 100)
     p = qp(S=100, q_norm=1, k_norm=0, fused_rope=0)   # Q only
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    assert n.value == 256 + 1792 + 100 * 256 * 4   # 2 partial column blocks, padded to 256
+    assert n.value == 256 + pad(2 * 100 * 8) + pad(2 * 100)
 
 
 def ws_bytes(L, p):
@@ -113,12 +113,15 @@ def qkv_call(L, p, **over):
     (dict(work=A16 + 4), -3), (dict(nwork=16), -4),
 ])
 def test_qkv_call_rejected(L, over, code):
+    if "nwork" in over:
+        assert ws_bytes(L, qp()) > over["nwork"]   # placeholders: the call must be refused
     st, msg = status_and_msg(L, qkv_call(L, qp(), **over))
     assert st == code and msg
 
 
 def test_project_and_norm_rejections(L):
     p = qp()
+    assert ws_bytes(L, p) > 8   # the 8-byte workspace below is always refused
     st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, A16, A16, 8, None)
     assert st == -4
     st = L.qkv_cte_mx_norm_rope(ctypes.byref(p), None, A16, A16, A16, A16, A16, ws_bytes(L, p), None)

@@ -47,9 +47,14 @@ def test_noalloc_matches_workspace_entry_point(kw):
 
 def test_noalloc_rejects_oversized_problem():
     lib = native.load()
-    p = native.QkvCteMxParams(B=1, S=32760, H=5120, num_heads=40, num_kv_heads=40, head_dim=128,
+    p = native.QkvCteMxParams(B=4, S=1 << 20, H=5120, num_heads=40, num_kv_heads=40, head_dim=128,
                               q_norm=1, k_norm=1, fused_rope=1, norm_eps=1e-6, output_layout=0)
-    a16 = 0x10000  # refused before any launch: never dereferenced
+    # the call below passes placeholder addresses: it must be refused before any launch,
+    # so make sure the problem really needs more scratch than the static array holds
+    need = ctypes.c_size_t()
+    assert lib.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(need)) == 0
+    assert need.value > 4 * (32 << 20)
+    a16 = 0x10000  # never dereferenced
     st = lib.qkv_cte_mx_noalloc(ctypes.byref(p), a16, a16, a16, None, a16, a16, a16, a16, a16, a16, None)
     assert st == -4
     assert "static workspace" in lib.ra_last_error().decode()
