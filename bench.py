@@ -197,7 +197,12 @@ def run_ours(args):
     ms = total_ms / K
     flops = qcase.flops
     k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
-    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    # a timed region shorter than about a second runs at full clocks (before the
+    # 1.4 kW power cap pulls them down): compare it with the burst peak, a longer
+    # one with the sustained peak
+    timed_s = total_ms / 1e3
+    burst = timed_s < 1.0
+    fp8_peak = (peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]) * FP8_PER_BF16
     k1_tf = flops / (k1_ms * 1e-3) / 1e12
     k2_bytes = qkv_bytes_k2(qcase)
     k3_bytes = kcase.algorithmic_bytes()
@@ -220,7 +225,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (each step streams > 3 GB)"},
         "roofline": {"bound": "tensor", "achieved": round(k1_tf, 1), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(k1_tf / fp8_peak, 4), "traffic": None,
-                     "peak_note": "FP8 = 2 x measured sustained bf16 cuBLAS (MEASURED_PEAKS.json)"
+                     "peak_note": ("FP8 = 2 x measured %s bf16 cuBLAS (MEASURED_PEAKS.json); timed region %.2f s"
+                                   % ("burst" if burst else "sustained", timed_s))
                      if peaks["source"] == "measured" else "FP8 = 2 x fallback bf16"},
         "passes": {
             "qkv_project": {"ms": round(k1_ms, 4), "tflops": round(k1_tf, 1), "frac_fp8": round(k1_tf / fp8_peak, 4)},

@@ -132,27 +132,32 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
                      const float* k_gamma, uint16_t* out, void* workspace, size_t workspace_bytes,
                      void* stream);
 
-/* First half of qkv_cte_mx on its own: O = dequant(A) @ dequant(W) + bias, and the
- * per-token Q / K sums of squares (Design 1a) into the workspace.  Columns that
- * the second pass does not touch (V, or everything when norms and RoPE are off
- * -- e.g. the V-only call) are final bf16 in `out`.  Columns the second pass
- * rewrites (Q and/or K when normed or rotated) are held in `out` in an internal
- * encoding until qkv_cte_mx_norm_rope runs: fp16 of O * 2^-e with a
- * power-of-two e per (token, 128-column block) kept in the workspace, so the
- * intermediate carries 11 significant bits and the only bf16 rounding of Q and
- * K is the final one. */
+/* First half of qkv_cte_mx on its own: everything that needs no across-heads
+ * statistic.  O = dequant(A) @ dequant(W) + bias, the per-token Q / K sums of
+ * squares of O (Design 1a) into the workspace, and the segment-wide gamma of
+ * each normed segment (Design 1c; inv_rms is one scalar per token and segment
+ * and RoPE is linear, so rot(O * inv_rms * gamma) = inv_rms * rot(O * gamma)).
+ * Columns the second pass does not touch (V, or everything when norms and RoPE
+ * are off -- e.g. the V-only call) are final bf16 in `out`.  Columns it rewrites
+ * (Q and/or K when normed or rotated) are held in `out` in an internal encoding
+ * until qkv_cte_mx_norm_rope runs: fp16 of O * gamma * 2^-e with a power-of-two
+ * e per (token, 128-column block) kept in the workspace, so the intermediate
+ * carries 11 significant bits and the only bf16 rounding of Q and K is the
+ * final one.  Arguments as for qkv_cte_mx. */
 ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
-                             uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+                             const float* q_gamma, const float* k_gamma, uint16_t* out,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
-/* Second half on its own (Design 1b-1c, Design 2): reads the sums of squares
- * and exponents left in `workspace` and the encoded Q/K columns of `out` by
- * qkv_cte_mx_project, applies inv_rms * gamma and RoPE, and writes Q and K back
- * into `out` as bf16.  V is not touched.  This is the seam where a
- * tensor-parallel all-reduce of the sums would go. */
+/* Second half on its own (Design 1b, Design 2): reduces the sums of squares
+ * left in `workspace` by qkv_cte_mx_project for the same `out` into inv_rms per
+ * token and segment, applies it and the rotate-half RoPE (cos/sin required iff
+ * fused_rope) to the encoded Q and K columns and writes them back into `out` as
+ * bf16.  V is not touched.  This is the seam where a tensor-parallel
+ * all-reduce of the sums would go. */
 ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cache,
-                               const float* sin_cache, const float* q_gamma, const float* k_gamma,
-                               uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+                               const float* sin_cache, uint16_t* out, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, reads the workspace status word, clears it, and
  * stores it in *device_status (0 = fine).  Returns RA_ERR_TIMEOUT if a

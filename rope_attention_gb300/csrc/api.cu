@@ -59,6 +59,7 @@ struct QkvShape {
   int32_t n_part_tiles;
   int32_t s_begin, s_end;   // Q/K columns carried as scaled fp16 between the passes
   int32_t n_exp_blocks;     // 128-column blocks covering [0, s_end)
+  int32_t part_stride, exp_stride;  // token-major row strides (16-byte multiples)
   size_t exps_offset;
   size_t workspace;
 };
@@ -106,8 +107,10 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   s->s_end = do_k ? s->k_end : (do_q ? s->q_w : s->q_w);
   if (!do_q && !do_k) s->s_begin = s->s_end = 0;
   s->n_exp_blocks = (s->s_end + ra::kPartCols - 1) / ra::kPartCols;
-  const size_t part = static_cast<size_t>(s->n_part_tiles) * T * sizeof(float2);
-  const size_t exps = static_cast<size_t>(s->n_exp_blocks) * T;
+  s->part_stride = (s->n_part_tiles + 1) / 2 * 2;
+  s->exp_stride = (s->n_exp_blocks + 15) / 16 * 16;
+  const size_t part = static_cast<size_t>(s->part_stride) * T * sizeof(float2);
+  const size_t exps = static_cast<size_t>(s->exp_stride) * T;
   s->exps_offset = ra::kWorkspaceHeader + ((part + 255) / 256) * 256;
   s->workspace = s->exps_offset + ((exps + 255) / 256) * 256;
   return RA_OK;
@@ -115,33 +118,33 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
 
 ra_status check_project_args(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
                              const float* a_scale, const void* w_packed, const float* ws,
-                             const uint16_t* bias, const uint16_t* out, const void* workspace,
-                             size_t workspace_bytes) {
-  (void)p;
+                             const uint16_t* bias, const float* qg, const float* kg,
+                             const uint16_t* out, const void* workspace, size_t workspace_bytes) {
   if (!a || !a_scale || !w_packed || !out || !workspace)
     return fail(RA_ERR_INVALID_ARG, "a, a_scale, w_packed, out and workspace are required");
   if (!aligned16(a) || !aligned16(out) || !aligned16(w_packed) || !aligned16(workspace))
     return fail(RA_ERR_ALIGNMENT, "a, out, w_packed and workspace must be 16-byte aligned");
   if ((ws && !aligned16(ws)) || (bias && !aligned16(bias)))
     return fail(RA_ERR_ALIGNMENT, "weight_scales and bias must be 16-byte aligned");
+  if (p->q_norm && !qg) return fail(RA_ERR_INVALID_ARG, "q_norm requires q_gamma");
+  if (p->k_norm && !kg) return fail(RA_ERR_INVALID_ARG, "k_norm requires k_gamma");
+  if ((qg && !aligned16(qg)) || (kg && !aligned16(kg)))
+    return fail(RA_ERR_ALIGNMENT, "gammas must be 16-byte aligned");
   if (workspace_bytes < s.workspace)
     return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
   return RA_OK;
 }
 
 ra_status check_norm_args(const qkv_cte_mx_params* p, const float* cos, const float* sin,
-                          const float* qg, const float* kg, const uint16_t* out,
-                          const void* workspace, size_t workspace_bytes, const QkvShape& s) {
+                          const uint16_t* out, const void* workspace, size_t workspace_bytes,
+                          const QkvShape& s) {
   if (!out || !workspace) return fail(RA_ERR_INVALID_ARG, "out and workspace are required");
   if (!aligned16(out) || !aligned16(workspace))
     return fail(RA_ERR_ALIGNMENT, "out and workspace must be 16-byte aligned");
   if (p->fused_rope && (!cos || !sin))
     return fail(RA_ERR_INVALID_ARG, "fused_rope requires cos_cache and sin_cache");
-  if (p->q_norm && !qg) return fail(RA_ERR_INVALID_ARG, "q_norm requires q_gamma");
-  if (p->k_norm && !kg) return fail(RA_ERR_INVALID_ARG, "k_norm requires k_gamma");
-  if ((cos && !aligned16(cos)) || (sin && !aligned16(sin)) || (qg && !aligned16(qg)) ||
-      (kg && !aligned16(kg)))
-    return fail(RA_ERR_ALIGNMENT, "cos/sin caches and gammas must be 16-byte aligned");
+  if ((cos && !aligned16(cos)) || (sin && !aligned16(sin)))
+    return fail(RA_ERR_ALIGNMENT, "cos/sin caches must be 16-byte aligned");
   if (workspace_bytes < s.workspace)
     return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
   return RA_OK;
@@ -149,7 +152,8 @@ ra_status check_norm_args(const qkv_cte_mx_params* p, const float* cos, const fl
 
 ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
                       const float* a_scale, const void* w_packed, const float* ws,
-                      const uint16_t* bias, uint16_t* out, void* workspace, cudaStream_t st) {
+                      const uint16_t* bias, const float* qg, const float* kg, uint16_t* out,
+                      void* workspace, cudaStream_t st) {
   ra::ProjLaunch L{};
   L.a = a;
   L.a_scale = a_scale;
@@ -168,8 +172,12 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
   L.n_part_tiles = s.n_part_tiles;
   L.exps = reinterpret_cast<int8_t*>(static_cast<uint8_t*>(workspace) + s.exps_offset);
   L.n_exp_blocks = s.n_exp_blocks;
+  L.part_stride = s.part_stride;
+  L.exp_stride = s.exp_stride;
   L.s_begin = s.s_begin;
   L.s_end = s.s_end;
+  L.q_gamma = p->q_norm ? qg : nullptr;
+  L.k_gamma = p->k_norm ? kg : nullptr;
   L.wait_ns = g_wait_ns.load();
   const char* why = "launch failed";
   cudaError_t e = ra::launch_qkv_project(L, st, &why);
@@ -178,8 +186,7 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
 }
 
 ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const float* cos,
-                        const float* sin, const float* qg, const float* kg, uint16_t* out,
-                        void* workspace, cudaStream_t st) {
+                        const float* sin, uint16_t* out, void* workspace, cudaStream_t st) {
   const bool do_q = p->q_norm || p->fused_rope;
   const bool do_k = p->num_kv_heads > 0 && (p->k_norm || p->fused_rope);
   if (!do_q && !do_k) return RA_OK;
@@ -189,8 +196,6 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
       reinterpret_cast<const float2*>(static_cast<const uint8_t*>(workspace) + ra::kWorkspaceHeader);
   L.cos = cos;
   L.sin = sin;
-  L.q_gamma = qg;
-  L.k_gamma = kg;
   L.T = s.T;
   L.I = s.I;
   L.head_dim = p->head_dim;
@@ -201,6 +206,9 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
   L.rope = p->fused_rope;
   L.n_part_tiles = s.n_part_tiles;
   L.exps = reinterpret_cast<const int8_t*>(static_cast<const uint8_t*>(workspace) + s.exps_offset);
+  L.part_stride = s.part_stride;
+  L.n_exp_blocks = s.n_exp_blocks;
+  L.exp_stride = s.exp_stride;
   L.eps = p->norm_eps;
   cudaError_t e = ra::launch_qk_norm_rope(L, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm/rope launch");
@@ -219,7 +227,7 @@ extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 1; }
+int32_t ra_abi_version(void) { return 2; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
@@ -257,27 +265,28 @@ ra_status qkv_cte_mx_workspace_bytes(const qkv_cte_mx_params* p, size_t* bytes) 
 
 ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
-                             uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+                             const float* q_gamma, const float* k_gamma, uint16_t* out,
+                             void* workspace, size_t workspace_bytes, void* stream) {
   QkvShape s;
   ra_status st = check_params(p, &s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace, workspace_bytes);
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
+                          workspace, workspace_bytes);
   if (st != RA_OK) return st;
-  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace,
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out, workspace,
                    static_cast<cudaStream_t>(stream));
   return st == RA_OK ? ok() : st;
 }
 
 ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cache,
-                               const float* sin_cache, const float* q_gamma, const float* k_gamma,
-                               uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+                               const float* sin_cache, uint16_t* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   QkvShape s;
   ra_status st = check_params(p, &s);
   if (st != RA_OK) return st;
-  st = check_norm_args(p, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace, workspace_bytes, s);
+  st = check_norm_args(p, cos_cache, sin_cache, out, workspace, workspace_bytes, s);
   if (st != RA_OK) return st;
-  st = run_norm_rope(p, s, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace,
-                     static_cast<cudaStream_t>(stream));
+  st = run_norm_rope(p, s, cos_cache, sin_cache, out, workspace, static_cast<cudaStream_t>(stream));
   return st == RA_OK ? ok() : st;
 }
 
@@ -289,14 +298,16 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
   QkvShape s;
   ra_status st = check_params(p, &s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace, workspace_bytes);
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
+                          workspace, workspace_bytes);
   if (st != RA_OK) return st;
-  st = check_norm_args(p, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace, workspace_bytes, s);
+  st = check_norm_args(p, cos_cache, sin_cache, out, workspace, workspace_bytes, s);
   if (st != RA_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, out, workspace, cs);
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out, workspace,
+                   cs);
   if (st != RA_OK) return st;
-  st = run_norm_rope(p, s, cos_cache, sin_cache, q_gamma, k_gamma, out, workspace, cs);
+  st = run_norm_rope(p, s, cos_cache, sin_cache, out, workspace, cs);
   return st == RA_OK ? ok() : st;
 }
 

@@ -24,15 +24,19 @@ struct ProjLaunch {
   const float* weight_scales;  // [I] or null
   const uint16_t* bias;        // [I] bf16 or null
   uint16_t* out;               // [T, I]: bf16, except columns [s_begin, s_end) (see below)
-  int8_t* exps;                // [n_exp_blocks, T] power-of-two exponent per 128-column block
-  float2* partials;            // [n_part_tiles, T] (sum sq Q, sum sq K) per 128-column block
+  int8_t* exps;                // [T, exp_stride] power-of-two exponent per 128-column block
+  float2* partials;            // [T, part_stride] (sum sq Q, sum sq K) per 128-column block
   int32_t* status;
   int64_t T, H, I;
   int32_t q_end, k_end;        // Q = [0, q_end), K = [q_end, k_end) output columns
-  int32_t s_begin, s_end;      // Q/K columns the norm/RoPE pass rewrites: stored as fp16 of
-                               // v * 2^-e, e per (row, 128-column block) in `exps`
-  int32_t n_part_tiles;
-  int32_t n_exp_blocks;
+  int32_t s_begin, s_end;      // Q/K columns the second pass rewrites: stored as fp16 of
+                               // z * 2^-e, e per (row, 128-column block) in `exps`, with
+                               // z = v * gamma
+  int32_t n_part_tiles, part_stride;   // part_stride = n_part_tiles rounded up to even
+  int32_t n_exp_blocks, exp_stride;    // exp_stride = n_exp_blocks rounded up to 16
+  // applied before the encoding (it commutes with inv_rms and the rotation):
+  const float* q_gamma;        // [q_end] gamma of a normed Q segment, or null
+  const float* k_gamma;        // [k_end - q_end] gamma of a normed K segment, or null
   int64_t wait_ns;
 };
 cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why);
@@ -44,17 +48,16 @@ cudaError_t launch_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, int
 
 // ------------------------------------------------------------ norm + RoPE apply (K2)
 struct NormRopeLaunch {
-  uint16_t* out;               // [T, I]: scaled fp16 Q/K in, bf16 normed / rotated Q/K out
-  const int8_t* exps;          // [n_exp_blocks, T] exponents of the scaled fp16 encoding
-  const float2* partials;      // [n_part_tiles, T]
-  const float* cos;            // [T, d]
+  uint16_t* out;               // [T, I]: encoded Q/K in, bf16 normed / rotated Q/K out
+  const int8_t* exps;          // [T, exp_stride] exponents of the scaled fp16 encoding
+  const float2* partials;      // [T, part_stride]
+  const float* cos;            // [T, d], used when rope
   const float* sin;
-  const float* q_gamma;        // [q_w] or null
-  const float* k_gamma;        // [k_w] or null
   int64_t T, I;
   int32_t head_dim, num_q_heads, num_k_heads;
   int32_t q_norm, k_norm, rope;
-  int32_t n_part_tiles;
+  int32_t n_part_tiles, part_stride;
+  int32_t n_exp_blocks, exp_stride;
   float eps;
 };
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);

@@ -9,11 +9,13 @@
 //   acc[t, i]     = sum_h e4m3(a[t, h]) * e4m3(w[h, i]) * 2^(e[h/32, i] - 127)
 //   v[t, i]       = acc[t, i] * a_scale[t] * wch[i] + bias[i]
 //   out[t, i]     = bf16(v)  for V (and any segment the second pass leaves alone),
-//   out[t, i]     = fp16(v * 2^-e[b, t]) for the Q/K columns the norm/RoPE pass
-//                   rewrites, with one power-of-two exponent per (row, 128-column
-//                   block b) chosen so the block's largest |v| lands in [2^14, 2^15):
-//                   11 significant bits in the 2 bytes the final bf16 needs
-//   partial[j, t] = ( sum of v^2 over the Q columns of 128-column block j,
+//   out[t, i]     = fp16(z * 2^-e[t, b]) for the Q/K columns the norm/RoPE pass
+//                   rewrites, z = v * gamma[i] (the segment-wide gamma of Design 1c,
+//                   which commutes with the per-token inv_rms and the rotation), with
+//                   one power-of-two exponent per (row, 128-column block b) chosen so
+//                   the block's largest |z| lands in [2^14, 2^15): 11 significant
+//                   bits in the 2 bytes the final bf16 needs
+//   partial[t, j] = ( sum of v^2 over the Q columns of 128-column block j,
 //                     sum of v^2 over its K columns )
 //
 // GB300 design (not the page's NKI schedule):
@@ -64,7 +66,7 @@ constexpr int SFA_COL = BN;           // 4 columns of A scales
 constexpr int SFB_COL = BN + 8;       // two 8-column slots of W scales
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;  // 10 warps: at most 3 per SM sub-partition, so <= 168 registers each
 constexpr int EPI_COLS = BN / 2;      // columns per epilogue warp
 constexpr int GROUP_M = 8;
 
@@ -101,8 +103,10 @@ struct Params {
   float2* partials;
   int32_t* status;
   int32_t T, I, num_k, num_m, num_n;
-  int32_t q_end, k_end, n_part, n_exp;
+  int32_t q_end, k_end, n_part, n_exp, part_stride, exp_stride;
   int32_t s_begin, s_end;
+  const float* q_gamma;
+  const float* k_gamma;
   uint64_t wait_ns;
 };
 
@@ -346,8 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       float ssq = 0.f, ssk = 0.f;
       uint16_t* out_row = p.out + static_cast<size_t>(row_ok ? row : 0) * p.I;
       const int col_base = nt * BN + chalf * EPI_COLS;
-      // pass 1: dequant, channel scale and bias in place; sums of squares; the largest
-      // magnitude among the columns the norm/RoPE pass will rewrite
+      // pass 1: dequant, channel scale and bias in place; sums of squares (of v, before gamma)
       float amax = 0.f;
 #pragma unroll
       for (int c = 0; c < EPI_COLS / 16; ++c) {
@@ -381,22 +384,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) bia[j] = 0.f;
         }
-        float sq = 0.f, cmax = 0.f;
+        float sq = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float v = fmaf(__uint_as_float(r[c * 16 + j]) * as, wch[j], bia[j]);
           r[c * 16 + j] = __float_as_uint(v);
           sq = fmaf(v, v, sq);
-          cmax = fmaxf(cmax, fabsf(v));
         }
         if (col0 < p.q_end) ssq += sq;
         else if (col0 < p.k_end) ssk += sq;
-        if (col0 >= p.s_begin && col0 < p.s_end) amax = fmaxf(amax, cmax);
       }
-      // power-of-two scale for the fp16 encoding: |v| * 2^-e < 2^15
+      // the segment-wide gamma of the normed segments, on the columns the second
+      // pass rewrites (inv_rms is one scalar per token and segment, and RoPE is
+      // linear, so scaling by gamma here is exact: rot(v * inv * gamma) = inv * rot(v * gamma))
+      const bool rewrite = col_base < p.s_end && col_base + EPI_COLS > p.s_begin;
+      if (rewrite) {
+#pragma unroll
+        for (int c = 0; c < EPI_COLS / 16; ++c) {
+          const int col0 = col_base + c * 16;
+          if (col0 >= p.I) break;
+          if (col0 < p.s_begin || col0 >= p.s_end) continue;
+          const float* g = col0 < p.q_end ? p.q_gamma : p.k_gamma;
+          if (g == nullptr) continue;
+          const float4* g4 = reinterpret_cast<const float4*>(g + (col0 < p.q_end ? col0 : col0 - p.q_end));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 t = __ldg(g4 + j);
+            r[c * 16 + 4 * j] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j]) * t.x);
+            r[c * 16 + 4 * j + 1] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j + 1]) * t.y);
+            r[c * 16 + 4 * j + 2] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j + 2]) * t.z);
+            r[c * 16 + 4 * j + 3] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j + 3]) * t.w);
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < EPI_COLS / 16; ++c) {
+        const int col0 = col_base + c * 16;
+        if (col0 >= p.I) break;
+        if (col0 < p.s_begin || col0 >= p.s_end) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(__uint_as_float(r[c * 16 + j])));
+      }
+      // power-of-two scale for the fp16 encoding: |z| * 2^-e < 2^15
       const int e = scale_exponent(amax);
       const float down = exp2_int(-e);
-      // pass 2: stores (fp16 of v * 2^-e for the rewritten Q/K columns, bf16 otherwise)
+      // pass 2: stores (fp16 of z * 2^-e for the rewritten Q/K columns, bf16 otherwise)
 #pragma unroll
       for (int c = 0; c < EPI_COLS / 16; ++c) {
         const int col0 = col_base + c * 16;
@@ -420,10 +452,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         dst[1] = o1;
       }
       const int blk = nt * 2 + chalf;
-      if (blk < p.n_exp && row_ok) p.exps[static_cast<size_t>(blk) * p.T + row] = static_cast<int8_t>(e);
+      if (blk < p.n_exp && row_ok)
+        p.exps[static_cast<size_t>(row) * p.exp_stride + blk] = static_cast<int8_t>(e);
       const int part = nt * 2 + chalf;
       if (part < p.n_part && row_ok)
-        p.partials[static_cast<size_t>(part) * p.T + row] = make_float2(ssq, ssk);
+        p.partials[static_cast<size_t>(row) * p.part_stride + part] = make_float2(ssq, ssk);
     }
   }
 
@@ -559,8 +592,12 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.k_end = L.k_end;
   p.n_part = L.n_part_tiles;
   p.n_exp = L.n_exp_blocks;
+  p.part_stride = L.part_stride;
+  p.exp_stride = L.exp_stride;
   p.s_begin = L.s_begin;
   p.s_end = L.s_end;
+  p.q_gamma = L.q_gamma;
+  p.k_gamma = L.k_gamma;
   p.wait_ns = static_cast<uint64_t>(L.wait_ns);
 
   static std::once_flag attr_once;

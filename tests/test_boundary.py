@@ -38,7 +38,7 @@ def test_exports_every_declared_function(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in the header but not exported"
     assert sorted(names) == sorted(native.EXPORTS)
-    assert native.ra_abi_version() == 1
+    assert native.ra_abi_version() == 2
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -79,16 +79,16 @@ def test_workspace_formula(L):
     n = ctypes.c_size_t()
     p = qp(B=1, S=32760, H=5120, num_heads=40, num_kv_heads=40, head_dim=128)
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    blocks = (80 * 128) // 128          # 128-column blocks over Q|K
+    blocks = (80 * 128) // 128          # 128-column blocks over Q|K (token-major, padded rows)
     assert n.value == 256 + pad(blocks * 32760 * 8) + pad(blocks * 32760)
     p = qp(q_norm=0, k_norm=0, fused_rope=0)
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value == 256
     p = qp(S=100, q_norm=0, k_norm=0, fused_rope=1)   # RoPE only: exponents for Q|K, no sums
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    assert n.value == 256 + pad(4 * 100)
+    assert n.value == 256 + pad(16 * 100)              # exponent rows padded to 16 bytes
     p = qp(S=100, q_norm=1, k_norm=0, fused_rope=0)   # Q only
     assert L.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
-    assert n.value == 256 + pad(2 * 100 * 8) + pad(2 * 100)
+    assert n.value == 256 + pad(2 * 100 * 8) + pad(16 * 100)
 
 
 def ws_bytes(L, p):
@@ -122,10 +122,13 @@ def test_qkv_call_rejected(L, over, code):
 def test_project_and_norm_rejections(L):
     p = qp()
     assert ws_bytes(L, p) > 8   # the 8-byte workspace below is always refused
-    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, A16, A16, 8, None)
+    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, A16, A16, A16, A16, 8, None)
     assert st == -4
-    st = L.qkv_cte_mx_norm_rope(ctypes.byref(p), None, A16, A16, A16, A16, A16, ws_bytes(L, p), None)
-    assert st == -1
+    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, None, A16, A16, A16,
+                              ws_bytes(L, p), None)
+    assert st == -1                                          # q_norm needs q_gamma
+    st = L.qkv_cte_mx_norm_rope(ctypes.byref(p), None, A16, A16, A16, ws_bytes(L, p), None)
+    assert st == -1                                          # fused_rope needs cos/sin
     v = ctypes.c_int32()
     assert L.qkv_cte_mx_status(None, None, ctypes.byref(v)) == -1
 
