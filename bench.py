@@ -48,6 +48,24 @@ def load_peaks():
             "source": "fallback"}
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one K1 launch,
+# from a one-pass ncu capture of the full-size workload, keyed by the workload
+# and by a digest of the kernel's sources at capture time: once the kernel
+# changes the figure no longer describes it and the bench reports null.
+K1_SOURCES = ("rope_attention_gb300/csrc/qkv_project.cu", "rope_attention_gb300/csrc/ptx.cuh",
+              "rope_attention_gb300/csrc/internal.h")
+K1_DRAM_BYTES = {("wan720", "f119473dac4da707"): 3397418752 + 2350816512}
+
+
+def k1_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in K1_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def workload(name: str):
     from rope_attention_gb300 import synth
     if name == "wan720":
@@ -224,7 +242,8 @@ def run_ours(args):
                    "global_batch": ws * qcase.T, "seq_len": qcase.S, "parallelism": f"replica x{ws}",
                    "l2": "inputs larger than L2 (each step streams > 3 GB)"},
         "roofline": {"bound": "tensor", "achieved": round(k1_tf, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(k1_tf / fp8_peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(k1_tf / fp8_peak, 4),
+                     "traffic": K1_DRAM_BYTES.get((args.workload, k1_source_digest())),
                      "peak_note": ("FP8 = 2 x measured %s bf16 cuBLAS (MEASURED_PEAKS.json); timed region %.2f s"
                                    % ("burst" if burst else "sustained", timed_s))
                      if peaks["source"] == "measured" else "FP8 = 2 x fallback bf16"},

@@ -7,13 +7,13 @@
 // latency-critical serving loop where cudaMalloc's implicit device-wide
 // synchronisation is not acceptable.  Such callers still pass their inputs and
 // the output buffer; the scratch space the two kernels need (status word,
-// per-token sum-of-squares partials, fp32 Q/K between the passes) lives in
+// per-token sum-of-squares partials, the per-block exponents of the Q/K codes) lives in
 // the file-scope device array below.
 //
 // The array is part of the library image: every GPU that loads the library
 // holds kNoAllocWorkspaceBytes of device memory for it until the process
 // exits.  All calls share it and it keeps the last call's contents; the status
-// word is cleared on every call (the partials and the fp32 Q/K are fully
+// word is cleared on every call (the partials and the exponents are fully
 // rewritten before they are read), so calls issued one after another are
 // independent, but calls that overlap on the GPU (different streams or
 // threads without ordering between them) race on the array.
