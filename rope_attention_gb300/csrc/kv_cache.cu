@@ -13,236 +13,253 @@
 // Quantisation uses the fp32 value (before any bf16 rounding); round() is
 // round-half-to-even.
 //
-// GB300 mapping: persistent warps, each walking (b, n, s) rows with a stride of
-// the whole grid and loading the next row's data while it processes the current
-// one (the op is latency-bound otherwise: a row is only 0.6-1.4 KB).  Every lane moves 16-byte chunks
-// (8 bf16); the RMS reduction is a warp shuffle tree; lane l < rope_size/8
-// owns interleaved pairs 4l..4l+3, whose outputs land at positions 4l and
-// rope_size/2 + 4l of the de-interleaved result, written as 8-byte (bf16) or
-// 4-byte (int8) stores.  Cache rows are contiguous, so each scattered slot is
-// written with whole 16-byte vectors.
+// GB300 mapping: an HBM stream of short rows (0.6-1.4 KB), so the kernel is
+// built to keep many bytes in flight with few instructions per byte:
+//  * persistent warps, each owning a contiguous range of (b, n, s) rows and
+//    walking (b, n, s) incrementally (no integer division per row);
+//  * a ring of row buffers in registers per warp: while one row is processed
+//    the next one or two are already being loaded;
+//  * the per-channel quantisation scales and offsets (per head in V2) are
+//    staged once per block in shared memory, laid out so a warp's reads are
+//    conflict-free;
+//  * every lane moves 16-byte chunks (8 bf16); the RMS reduction is a warp
+//    shuffle tree; the arithmetic uses packed fp32x2 operations; int8 codes are
+//    rounded with cvt.rni and packed with saturation by cvt.pack.sat;
+//  * lane l < rope_size/8 owns interleaved pairs 4l..4l+3, whose outputs land at
+//    positions 4l and rope_size/2 + 4l of the de-interleaved result.  Cache rows
+//    are contiguous, so each scattered slot is written with whole vectors.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace ra {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    f[2 * k] = bf16_lo(w[k]);
-    f[2 * k + 1] = bf16_hi(w[k]);
-  }
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
+__device__ __forceinline__ void unpack8(uint4 u, float2 (&f)[4]) {
+  f[0] = bf16x2_to_f2(u.x);
+  f[1] = bf16x2_to_f2(u.y);
+  f[2] = bf16x2_to_f2(u.z);
+  f[3] = bf16x2_to_f2(u.w);
 }
-__device__ __forceinline__ uint4 pack8(const float* f) {
+__device__ __forceinline__ uint4 pack8(const float2 (&f)[4]) {
   uint4 u;
-  u.x = pack_bf16x2(f[0], f[1]);
-  u.y = pack_bf16x2(f[2], f[3]);
-  u.z = pack_bf16x2(f[4], f[5]);
-  u.w = pack_bf16x2(f[6], f[7]);
+  u.x = pack_bf16x2(f[0].x, f[0].y);
+  u.y = pack_bf16x2(f[1].x, f[1].y);
+  u.z = pack_bf16x2(f[2].x, f[2].y);
+  u.w = pack_bf16x2(f[3].x, f[3].y);
   return u;
 }
-__device__ __forceinline__ int q8(float v, float scale, float offset) {
-  const int q = __float2int_rn(fmaf(v, scale, offset));
-  return min(127, max(-128, q));
-}
-__device__ __forceinline__ uint32_t pack_i8x4(int a, int b, int c, int d) {
-  return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
-         ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
-}
-
-// n values starting at channel `ch` of a cache row: int8 (quantised) or bf16
-template <bool QUANT, int NV>
-__device__ __forceinline__ void store_vals(void* row_base, int ch, const float* v, const float* scale,
-                                           const float* offset) {
-  if constexpr (QUANT) {
-    float sc[NV], of[NV];
-#pragma unroll
-    for (int j = 0; j < NV; j += 4) {
-      const float4 s4 = __ldg(reinterpret_cast<const float4*>(scale + ch + j));
-      sc[j] = s4.x; sc[j + 1] = s4.y; sc[j + 2] = s4.z; sc[j + 3] = s4.w;
-      if (offset != nullptr) {
-        const float4 o4 = __ldg(reinterpret_cast<const float4*>(offset + ch + j));
-        of[j] = o4.x; of[j + 1] = o4.y; of[j + 2] = o4.z; of[j + 3] = o4.w;
-      } else {
-        of[j] = of[j + 1] = of[j + 2] = of[j + 3] = 0.f;
-      }
-    }
-    int8_t* dst = static_cast<int8_t*>(row_base) + ch;
-    if constexpr (NV == 8) {
-      uint2 w;
-      w.x = pack_i8x4(q8(v[0], sc[0], of[0]), q8(v[1], sc[1], of[1]), q8(v[2], sc[2], of[2]),
-                      q8(v[3], sc[3], of[3]));
-      w.y = pack_i8x4(q8(v[4], sc[4], of[4]), q8(v[5], sc[5], of[5]), q8(v[6], sc[6], of[6]),
-                      q8(v[7], sc[7], of[7]));
-      *reinterpret_cast<uint2*>(dst) = w;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) =
-          pack_i8x4(q8(v[0], sc[0], of[0]), q8(v[1], sc[1], of[1]), q8(v[2], sc[2], of[2]),
-                    q8(v[3], sc[3], of[3]));
-    }
-  } else {
-    uint16_t* dst = static_cast<uint16_t*>(row_base) + ch;
-    if constexpr (NV == 8) {
-      *reinterpret_cast<uint4*>(dst) = pack8(v);
-    } else {
-      uint2 w;
-      w.x = pack_bf16x2(v[0], v[1]);
-      w.y = pack_bf16x2(v[2], v[3]);
-      *reinterpret_cast<uint2*>(dst) = w;
-    }
-  }
+// four int8 codes round_half_even(v * scale + offset), saturated to [-128, 127],
+// the first channel in the lowest byte.  cvt.rni saturates at the int32 range and
+// cvt.pack.sat (PTX ISA, sm_72+) clamps each value to the int8 range as it packs
+// two of them above the 16 bits taken from its third operand.
+__device__ __forceinline__ uint32_t quant4(float2 v01, float2 v23, float4 sc, float4 of) {
+  const int32_t a = __float2int_rn(fmaf(v01.x, sc.x, of.x));
+  const int32_t b = __float2int_rn(fmaf(v01.y, sc.y, of.y));
+  const int32_t c = __float2int_rn(fmaf(v23.x, sc.z, of.z));
+  const int32_t d = __float2int_rn(fmaf(v23.y, sc.w, of.w));
+  uint32_t hi, r;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(d), "r"(c));
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
+  return r;
 }
 
-// Everything one row needs from HBM, loaded as raw 16/8-byte vectors so the
-// next row's loads can be in flight while the current row is processed.
-template <int CPL>
-struct RowIn {
-  uint4 x[CPL];            // chunks lane + 32 i of the RMSNorm part of kv
-  uint4 xr;                // V1: the lane's chunk of the raw RoPE part
-  uint4 v[CPL];            // V2: chunks lane + 32 i of v_optional
-  uint2 c1, c2, s1, s2;    // cos/sin for pairs 4l..4l+3 at j and R/2 + j
-  int64_t slot;
+// Quantisation tables in shared memory, in units of 4 channels: scale[u] and
+// offset[u] (float4) for channels 4u..4u+3, heads one after another.
+struct QuantTab {
+  const float4* scale;
+  const float4* offset;
 };
 
-template <int VARIANT, int CPL>
-__device__ __forceinline__ void load_row(const KvLaunch& p, int64_t row, int lane, int rms,
-                                         int rms_chunks, int v_chunks, int rope_lanes,
-                                         RowIn<CPL>& in) {
-  const uint16_t* x = p.kv + row * p.Dkv;
-  const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const int c = lane + 32 * i;
-    in.x[i] = c < rms_chunks ? __ldcs(reinterpret_cast<const uint4*>(x + 8 * c)) : z;
+// 8 channels starting at `ch` (a multiple of 8) of a cache row: int8 or bf16
+__device__ __forceinline__ void store8(bool quant, void* row_base, int ch, const float2 (&v)[4],
+                                       QuantTab t) {
+  if (quant) {
+    const int u = ch >> 2;
+    uint2 w;
+    w.x = quant4(v[0], v[1], t.scale[u], t.offset[u]);
+    w.y = quant4(v[2], v[3], t.scale[u + 1], t.offset[u + 1]);
+    *reinterpret_cast<uint2*>(static_cast<int8_t*>(row_base) + ch) = w;
+  } else {
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(row_base) + ch) = pack8(v);
   }
-  if (VARIANT == 1)
-    in.xr = lane < rope_lanes ? __ldcs(reinterpret_cast<const uint4*>(x + rms + 8 * lane)) : z;
-  if (VARIANT == 2) {
-    const uint16_t* vrow = p.v + row * p.Dv;
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      const int c = lane + 32 * i;
-      in.v[i] = c < v_chunks ? __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * c)) : z;
-    }
+}
+// 4 channels starting at `ch` (a multiple of 4)
+__device__ __forceinline__ void store4(bool quant, void* row_base, int ch, float2 v01, float2 v23,
+                                       QuantTab t) {
+  if (quant) {
+    *reinterpret_cast<uint32_t*>(static_cast<int8_t*>(row_base) + ch) =
+        quant4(v01, v23, t.scale[ch >> 2], t.offset[ch >> 2]);
+  } else {
+    uint2 w;
+    w.x = pack_bf16x2(v01.x, v01.y);
+    w.y = pack_bf16x2(v23.x, v23.y);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(row_base) + ch) = w;
   }
-  if (lane < rope_lanes) {
-    const int half = p.R / 2;
-    const uint16_t* cs = p.cos + row * p.R;
-    const uint16_t* sn = p.sin + row * p.R;
-    in.c1 = __ldcs(reinterpret_cast<const uint2*>(cs + 4 * lane));
-    in.c2 = __ldcs(reinterpret_cast<const uint2*>(cs + half + 4 * lane));
-    in.s1 = __ldcs(reinterpret_cast<const uint2*>(sn + 4 * lane));
-    in.s2 = __ldcs(reinterpret_cast<const uint2*>(sn + half + 4 * lane));
-  }
-  const int64_t s = row % p.S;
-  const int64_t b = row / (p.S * p.N);
-  in.slot = __ldg(p.index + b * p.S + s);
 }
 
-template <int VARIANT, bool QK, bool QV, int CPL>
-__global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const KvLaunch p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t rows = p.B * p.N * p.S;
-  const int R = p.R, half = R / 2, rope_lanes = R / 8;
-  const int rms = VARIANT == 1 ? static_cast<int>(p.Dkv) - R : static_cast<int>(p.Dkv);
-  const int rms_chunks = rms / 8;
-  const int kw = VARIANT == 1 ? R : static_cast<int>(p.Dkv);
-  const int cw = VARIANT == 1 ? rms : static_cast<int>(p.Dv);
-  const int v_chunks = VARIANT == 2 ? cw / 8 : 0;
-  const int64_t slots = p.block_num * p.block_size;
-  const size_t k_elt = QK ? 1 : 2, c_elt = QV ? 1 : 2;
+// Launch constants computed on the host.
+struct KvAux {
+  float inv_rms;      // 1 / rms_size
+  int32_t bs_shift;   // log2(block_size) when it is a power of two, else -1
+  int32_t qk, qv;     // int8 k / ckv caches
+};
 
-  // gamma is the same for every row: keep the lane's chunks in registers
-  uint4 gam[CPL];
+// What one lane needs from HBM for its row of a row group, as raw vectors, so
+// that the next group's loads are in flight while this one is processed.
+template <int CPL>
+struct RowIn {
+  uint4 x[CPL];            // kv chunks j + LPR*i of the RMSNorm part
+  uint4 xr;                // V1: chunk j of the raw RoPE part
+  uint4 v[CPL];            // V2: chunks j + LPR*i of v_optional
+  uint2 c1, c2, s1, s2;    // cos/sin of pairs 4j..4j+3, at j and R/2 + j
+  int64_t slot;
+  int32_t n;
+};
+
+// (b, n, s) of one row, advanced without division.
+struct Cursor {
+  int64_t row, tok;        // tok = b * S + s, the entry of `index`
+  int32_t n, s;
+  __device__ __forceinline__ void advance(int32_t step, int32_t N, int32_t S) {
+    row += step;
+    tok += step;
+    s += step;
+    while (s >= S) {
+      s -= S;
+      tok -= S;
+      if (++n == N) {
+        n = 0;
+        tok += S;
+      }
+    }
+  }
+};
+
+// Lane layout: a warp processes 32 / LPR rows at once; lane = g * LPR + j works
+// on row g of the group and owns its 16-byte chunks j + LPR * i, i < CPL.
+template <int VARIANT, int LPR, int CPL>
+struct KvRows {
+  const KvLaunch& p;
+  KvAux aux;
+  int j;
+  int rms, rms_chunks, v_chunks, rope_lanes, half, kw, cw;
+  int64_t slots;
+  const uint4 (&gam)[CPL];
+  QuantTab kt0, vt0;
+
+  __device__ __forceinline__ void load(const Cursor& c, bool valid, RowIn<CPL>& in) const {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    const uint16_t* x = p.kv + c.row * p.Dkv;
 #pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const int c = lane + 32 * i;
-    gam[i] = c < rms_chunks ? __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * c))
-                            : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < CPL; ++i) {
+      const int ch = j + LPR * i;
+      in.x[i] = valid && ch < rms_chunks ? __ldcs(reinterpret_cast<const uint4*>(x + 8 * ch)) : z;
+    }
+    if (VARIANT == 1)
+      in.xr = valid && j < rope_lanes ? __ldcs(reinterpret_cast<const uint4*>(x + rms + 8 * j)) : z;
+    if (VARIANT == 2) {
+      const uint16_t* vrow = p.v + c.row * p.Dv;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int ch = j + LPR * i;
+        in.v[i] = valid && ch < v_chunks ? __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * ch)) : z;
+      }
+    }
+    if (valid && j < rope_lanes) {
+      const uint16_t* cs = p.cos + c.row * p.R;
+      const uint16_t* sn = p.sin + c.row * p.R;
+      in.c1 = __ldcs(reinterpret_cast<const uint2*>(cs + 4 * j));
+      in.c2 = __ldcs(reinterpret_cast<const uint2*>(cs + half + 4 * j));
+      in.s1 = __ldcs(reinterpret_cast<const uint2*>(sn + 4 * j));
+      in.s2 = __ldcs(reinterpret_cast<const uint2*>(sn + half + 4 * j));
+    }
+    in.slot = valid ? __ldg(p.index + c.tok) : int64_t(-1);
+    in.n = c.n;
   }
 
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
-  int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  RowIn<CPL> cur;
-  if (row < rows) load_row<VARIANT, CPL>(p, row, lane, rms, rms_chunks, v_chunks, rope_lanes, cur);
-
-  while (row < rows) {
-    const int64_t next = row + stride;
-    RowIn<CPL> nxt;
-    if (next < rows) load_row<VARIANT, CPL>(p, next, lane, rms, rms_chunks, v_chunks, rope_lanes, nxt);
-
-    const int n = static_cast<int>((row / p.S) % p.N);
-
-    // (1) RmsNorm
-    float y[CPL][8];
-    float ss = 0.f;
+  __device__ __forceinline__ void process(const RowIn<CPL>& in, int64_t row, bool valid) const {
+    const int n = in.n;
+    // (1) RmsNorm over the row's LPR lanes
+    float2 y[CPL][4];
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      unpack8(cur.x[i], y[i]);
+      unpack8(in.x[i], y[i]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ss = fmaf(y[i][j], y[i][j], ss);
+      for (int k = 0; k < 4; ++k) acc = __ffma2_rn(y[i][k], y[i][k], acc);
     }
+    float ss = acc.x + acc.y;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = rsqrtf(ss / static_cast<float>(rms) + p.eps);
+    for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(fmaf(ss, aux.inv_rms, p.eps));
+    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      float g[8];
+      float2 g[4];
       unpack8(gam[i], g);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) y[i][j] = y[i][j] * inv * g[j];
+      for (int k = 0; k < 4; ++k) y[i][k] = __fmul2_rn(__fmul2_rn(y[i][k], inv2), g[k]);
     }
+    if (!valid) return;
 
     // (4) slot of this token
-    const int64_t slot = cur.slot;
+    const int64_t slot = in.slot;
     const bool to_cache = slot >= 0 && slot < slots;
-    if (!to_cache && slot != -1 && n == 0 && lane == 0 && p.err_count != nullptr)
+    if (!to_cache && slot != -1 && n == 0 && j == 0 && p.err_count != nullptr)
       atomicAdd(p.err_count, 1);  // once per token, not per head
-    const int64_t blk = to_cache ? slot / p.block_size : 0;
-    const int64_t off = to_cache ? slot % p.block_size : 0;
+    int64_t blk = 0, off = 0;
+    if (to_cache) {
+      if (aux.bs_shift >= 0) {
+        blk = slot >> aux.bs_shift;
+        off = slot & (p.block_size - 1);
+      } else {
+        blk = slot / p.block_size;
+        off = slot - blk * p.block_size;
+      }
+    }
     const int64_t cache_row = p.mode == 2 ? (blk * p.N + n) * p.block_size + off
                                           : (blk * p.block_size + off) * p.N + n;
-    void* k_row = static_cast<uint8_t*>(p.k_cache) + static_cast<size_t>(cache_row) * kw * k_elt;
-    void* c_row = static_cast<uint8_t*>(p.ckv_cache) + static_cast<size_t>(cache_row) * cw * c_elt;
-    const float* ksc = QK ? p.k_scale + (VARIANT == 2 ? n * kw : 0) : nullptr;
-    const float* kof = (QK && p.k_offset) ? p.k_offset + (VARIANT == 2 ? n * kw : 0) : nullptr;
-    const float* vsc = QV ? p.v_scale + (VARIANT == 2 ? n * cw : 0) : nullptr;
-    const float* vof = (QV && p.v_offset) ? p.v_offset + (VARIANT == 2 ? n * cw : 0) : nullptr;
+    const bool qk = aux.qk != 0, qv = aux.qv != 0;
+    void* k_row = static_cast<uint8_t*>(p.k_cache) + static_cast<size_t>(cache_row) * kw * (qk ? 1 : 2);
+    void* c_row = static_cast<uint8_t*>(p.ckv_cache) + static_cast<size_t>(cache_row) * cw * (qv ? 1 : 2);
+    const QuantTab kt{kt0.scale + (VARIANT == 2 ? n * (kw / 4) : 0), kt0.offset + (VARIANT == 2 ? n * (kw / 4) : 0)};
+    const QuantTab vt{vt0.scale + (VARIANT == 2 ? n * (cw / 4) : 0), vt0.offset + (VARIANT == 2 ? n * (cw / 4) : 0)};
     uint16_t* kr_row = p.out_kv ? p.k_rope + row * kw : nullptr;
     uint16_t* ckv_row = p.out_kv ? p.c_kv + row * cw : nullptr;
 
-    // (2) interleaved RoPE: lane l owns pairs j = 4l .. 4l+3
-    if (lane < rope_lanes) {
-      float r[8];
+    // (2) interleaved RoPE: lane j owns pairs 4j .. 4j+3
+    if (j < rope_lanes) {
+      float2 r[4];
       if (VARIANT == 1) {
-        unpack8(cur.xr, r);
+        unpack8(in.xr, r);
       } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) r[j] = y[0][j];
+        for (int k = 0; k < 4; ++k) r[k] = y[0][k];
       }
-      const float cc1[4] = {bf16_lo(cur.c1.x), bf16_hi(cur.c1.x), bf16_lo(cur.c1.y), bf16_hi(cur.c1.y)};
-      const float cc2[4] = {bf16_lo(cur.c2.x), bf16_hi(cur.c2.x), bf16_lo(cur.c2.y), bf16_hi(cur.c2.y)};
-      const float ss1[4] = {bf16_lo(cur.s1.x), bf16_hi(cur.s1.x), bf16_lo(cur.s1.y), bf16_hi(cur.s1.y)};
-      const float ss2[4] = {bf16_lo(cur.s2.x), bf16_hi(cur.s2.x), bf16_lo(cur.s2.y), bf16_hi(cur.s2.y)};
-      float o1[4], o2[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float x1 = r[2 * m], x2 = r[2 * m + 1];
-        o1[m] = x1 * cc1[m] - x2 * ss1[m];
-        o2[m] = x2 * cc2[m] + x1 * ss2[m];
-      }
+      // r[m] = (x1, x2) of pair 4j + m
+      const float2 c1a = bf16x2_to_f2(in.c1.x), c1b = bf16x2_to_f2(in.c1.y);
+      const float2 c2a = bf16x2_to_f2(in.c2.x), c2b = bf16x2_to_f2(in.c2.y);
+      const float2 s1a = bf16x2_to_f2(in.s1.x), s1b = bf16x2_to_f2(in.s1.y);
+      const float2 s2a = bf16x2_to_f2(in.s2.x), s2b = bf16x2_to_f2(in.s2.y);
+      const float2 x1a = make_float2(r[0].x, r[1].x), x1b = make_float2(r[2].x, r[3].x);
+      const float2 x2a = make_float2(r[0].y, r[1].y), x2b = make_float2(r[2].y, r[3].y);
+      // out_m = x1 cos_m - x2 sin_m ; out_{R/2+m} = x2 cos_{R/2+m} + x1 sin_{R/2+m}
+      const float2 o1a = __ffma2_rn(x1a, c1a, __fmul2_rn(x2a, make_float2(-s1a.x, -s1a.y)));
+      const float2 o1b = __ffma2_rn(x1b, c1b, __fmul2_rn(x2b, make_float2(-s1b.x, -s1b.y)));
+      const float2 o2a = __ffma2_rn(x2a, c2a, __fmul2_rn(x1a, s2a));
+      const float2 o2b = __ffma2_rn(x2b, c2b, __fmul2_rn(x1b, s2b));
       if (to_cache) {
-        store_vals<QK, 4>(k_row, 4 * lane, o1, ksc, kof);
-        store_vals<QK, 4>(k_row, half + 4 * lane, o2, ksc, kof);
+        store4(qk, k_row, 4 * j, o1a, o1b, kt);
+        store4(qk, k_row, half + 4 * j, o2a, o2b, kt);
       }
       if (kr_row != nullptr) {
-        store_vals<false, 4>(kr_row, 4 * lane, o1, nullptr, nullptr);
-        store_vals<false, 4>(kr_row, half + 4 * lane, o2, nullptr, nullptr);
+        store4(false, kr_row, 4 * j, o1a, o1b, kt);
+        store4(false, kr_row, half + 4 * j, o2a, o2b, kt);
       }
     }
 
@@ -250,50 +267,145 @@ __global__ void __launch_bounds__(kThreads) kv_rms_norm_rope_cache_kernel(const 
       // rope_out tail = y[..., rope_size:]
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
-        const int c = lane + 32 * i;
-        if (c >= rope_lanes && c < rms_chunks) {
-          if (to_cache) store_vals<QK, 8>(k_row, 8 * c, y[i], ksc, kof);
-          if (kr_row != nullptr) store_vals<false, 8>(kr_row, 8 * c, y[i], nullptr, nullptr);
+        const int ch = j + LPR * i;
+        if (ch >= rope_lanes && ch < rms_chunks) {
+          if (to_cache) store8(qk, k_row, 8 * ch, y[i], kt);
+          if (kr_row != nullptr) store8(false, kr_row, 8 * ch, y[i], kt);
         }
       }
       // ckv <- v_optional
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
-        const int c = lane + 32 * i;
-        if (c < v_chunks) {
+        const int ch = j + LPR * i;
+        if (ch < v_chunks) {
           if (to_cache) {
-            if constexpr (QV) {
-              float f[8];
-              unpack8(cur.v[i], f);
-              store_vals<true, 8>(c_row, 8 * c, f, vsc, vof);
+            if (qv) {
+              float2 f[4];
+              unpack8(in.v[i], f);
+              store8(true, c_row, 8 * ch, f, vt);
             } else {
-              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(c_row) + 8 * c) = cur.v[i];
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(c_row) + 8 * ch) = in.v[i];
             }
           }
-          if (ckv_row != nullptr) *reinterpret_cast<uint4*>(ckv_row + 8 * c) = cur.v[i];
+          if (ckv_row != nullptr) *reinterpret_cast<uint4*>(ckv_row + 8 * ch) = in.v[i];
         }
       }
     } else {
       // ckv <- y
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
-        const int c = lane + 32 * i;
-        if (c < rms_chunks) {
-          if (to_cache) store_vals<QV, 8>(c_row, 8 * c, y[i], vsc, vof);
-          if (ckv_row != nullptr) store_vals<false, 8>(ckv_row, 8 * c, y[i], nullptr, nullptr);
+        const int ch = j + LPR * i;
+        if (ch < rms_chunks) {
+          if (to_cache) store8(qv, c_row, 8 * ch, y[i], vt);
+          if (ckv_row != nullptr) store8(false, ckv_row, 8 * ch, y[i], vt);
         }
       }
     }
-    cur = nxt;
-    row = next;
+  }
+};
+
+// Shared-memory bytes of the quantisation tables (scale and offset, per head in V2).
+size_t quant_table_bytes(const KvLaunch& L, bool qk, bool qv) {
+  const int64_t heads = L.variant == 2 ? L.N : 1;
+  const int64_t kw = L.variant == 1 ? L.R : L.Dkv;
+  const int64_t cw = L.variant == 1 ? L.Dkv - L.R : L.Dv;
+  return static_cast<size_t>(heads) * ((qk ? kw : 0) + (qv ? cw : 0)) * 2 * sizeof(float);
+}
+
+constexpr int kMinBlocks = 3;  // 12 warps per SM: up to 168 registers per thread
+
+template <int VARIANT, int LPR, int CPL>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    kv_rms_norm_rope_cache_kernel(const KvLaunch p, const KvAux aux) {
+  extern __shared__ float4 tabs[];
+  constexpr int DEPTH = 2;          // row-group buffers per lane: one processed, one loading
+  constexpr int RPG = 32 / LPR;     // rows per warp per step
+  const int lane = threadIdx.x & 31;
+  const int g = lane / LPR, j = lane % LPR;
+  const int64_t rows = p.B * p.N * p.S;
+  const int R = p.R;
+  const int rms = VARIANT == 1 ? static_cast<int>(p.Dkv) - R : static_cast<int>(p.Dkv);
+  const int kw = VARIANT == 1 ? R : static_cast<int>(p.Dkv);
+  const int cw = VARIANT == 1 ? rms : static_cast<int>(p.Dv);
+  const int heads = VARIANT == 2 ? static_cast<int>(p.N) : 1;
+  const int32_t N = static_cast<int32_t>(p.N), S = static_cast<int32_t>(p.S);
+
+  // this warp's contiguous range of rows, a multiple of RPG long
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t per_warp = ((rows + warps - 1) / warps + RPG - 1) / RPG * RPG;
+  const int64_t r_begin = (static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * per_warp;
+  const int64_t r_end = r_begin + per_warp < rows ? r_begin + per_warp : rows;
+
+  uint4 gam[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int ch = j + LPR * i;
+    gam[i] = ch * 8 < rms ? __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * ch)) : make_uint4(0, 0, 0, 0);
+  }
+  const int ku = aux.qk ? heads * kw / 4 : 0, vu = aux.qv ? heads * cw / 4 : 0;
+  float4* ks = tabs;
+  float4* ko = ks + ku;
+  float4* vs = ko + ku;
+  float4* vo = vs + vu;
+  const KvRows<VARIANT, LPR, CPL> w{p, aux, j, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
+                                    p.block_num * p.block_size, gam, QuantTab{ks, ko}, QuantTab{vs, vo}};
+
+  // the lane's load cursor: row r_begin + g, then RPG rows further each step
+  Cursor cur;
+  {
+    int64_t start = r_begin + g;
+    if (start >= rows) start = 0;
+    const int64_t per_b = p.N * p.S;
+    const int64_t b = start / per_b, rem = start - b * per_b;
+    cur.row = start;
+    cur.n = static_cast<int32_t>(rem / p.S);
+    cur.s = static_cast<int32_t>(rem - static_cast<int64_t>(cur.n) * p.S);
+    cur.tok = b * p.S + cur.s;
+    if (r_begin + g >= rows) cur.row = r_begin + g;  // never valid
+  }
+  // start the first groups' loads before staging the tables
+  RowIn<CPL> buf[DEPTH];
+  int64_t next = r_begin;  // first row of the next group to load (warp-uniform)
+#pragma unroll
+  for (int k = 0; k < DEPTH; ++k) {
+    if (next < r_end) {
+      w.load(cur, cur.row < r_end, buf[k]);
+      cur.advance(RPG, N, S);
+      next += RPG;
+    }
+  }
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = threadIdx.x; u < ku; u += kThreads) {
+    ks[u] = __ldg(reinterpret_cast<const float4*>(p.k_scale) + u);
+    ko[u] = p.k_offset ? __ldg(reinterpret_cast<const float4*>(p.k_offset) + u) : zero4;
+  }
+  for (int u = threadIdx.x; u < vu; u += kThreads) {
+    vs[u] = __ldg(reinterpret_cast<const float4*>(p.v_scale) + u);
+    vo[u] = p.v_offset ? __ldg(reinterpret_cast<const float4*>(p.v_offset) + u) : zero4;
+  }
+  __syncthreads();
+
+  for (int64_t base = r_begin; base < r_end; base += DEPTH * RPG) {
+#pragma unroll
+    for (int k = 0; k < DEPTH; ++k) {
+      const int64_t grp = base + k * RPG;
+      if (grp < r_end) {
+        w.process(buf[k], grp + g, grp + g < r_end);
+        if (next < r_end) {
+          w.load(cur, cur.row < r_end, buf[k]);
+          cur.advance(RPG, N, S);
+          next += RPG;
+        }
+      }
+    }
   }
 }
 
 // persistent grid: as many blocks as fit on the GPU at once, capped by the row count
 template <typename K>
-unsigned persistent_grid(K kernel, int64_t rows) {
+unsigned persistent_grid(K kernel, int64_t rows, size_t smem) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   const int64_t want = (rows + kWarps - 1) / kWarps;
@@ -301,31 +413,39 @@ unsigned persistent_grid(K kernel, int64_t rows) {
   return static_cast<unsigned>(want < cap ? want : cap);
 }
 
-template <int VARIANT, bool QK, bool QV, int CPL>
-cudaError_t launch_one(const KvLaunch& L, cudaStream_t st) {
-  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, QK, QV, CPL>;
-  const unsigned grid = persistent_grid(kernel, L.B * L.N * L.S);
-  kernel<<<grid, kThreads, 0, st>>>(L);
+template <int VARIANT, int LPR, int CPL>
+cudaError_t launch_one(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
+  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL>;
+  const size_t smem = quant_table_bytes(L, aux.qk != 0, aux.qv != 0);
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned grid = persistent_grid(kernel, L.B * L.N * L.S, smem);
+  kernel<<<grid, kThreads, smem, st>>>(L, aux);
   return cudaGetLastError();
 }
 
-template <int VARIANT, bool QK, bool QV>
-cudaError_t launch_cpl(const KvLaunch& L, int cpl, unsigned, cudaStream_t st) {
+template <int VARIANT, int LPR>
+cudaError_t launch_cpl(const KvLaunch& L, const KvAux& aux, int cpl, cudaStream_t st) {
   switch (cpl) {
-    case 1: return launch_one<VARIANT, QK, QV, 1>(L, st);
-    case 2: return launch_one<VARIANT, QK, QV, 2>(L, st);
-    case 4: return launch_one<VARIANT, QK, QV, 4>(L, st);
+    case 1: return launch_one<VARIANT, LPR, 1>(L, aux, st);
+    case 2: return launch_one<VARIANT, LPR, 2>(L, aux, st);
+    case 3: return launch_one<VARIANT, LPR, 3>(L, aux, st);
+    case 4: return launch_one<VARIANT, LPR, 4>(L, aux, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int VARIANT>
-cudaError_t launch_variant(const KvLaunch& L, int cpl, unsigned grid, cudaStream_t st) {
-  const bool qk = L.k_scale != nullptr, qv = L.v_scale != nullptr;
-  if (qk && qv) return launch_cpl<VARIANT, true, true>(L, cpl, grid, st);
-  if (qk) return launch_cpl<VARIANT, true, false>(L, cpl, grid, st);
-  if (qv) return launch_cpl<VARIANT, false, true>(L, cpl, grid, st);
-  return launch_cpl<VARIANT, false, false>(L, cpl, grid, st);
+cudaError_t launch_variant(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st) {
+  switch (lpr) {
+    case 8: return launch_cpl<VARIANT, 8>(L, aux, cpl, st);
+    case 16: return launch_cpl<VARIANT, 16>(L, aux, cpl, st);
+    case 32: return launch_cpl<VARIANT, 32>(L, aux, cpl, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -334,11 +454,28 @@ cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream
   const int64_t rms = L.variant == 1 ? L.Dkv - L.R : L.Dkv;
   int64_t chunks = rms / 8;
   if (L.variant == 2 && L.Dv / 8 > chunks) chunks = L.Dv / 8;  // v_optional rides the same lanes
-  const int cpl = chunks <= 32 ? 1 : (chunks <= 64 ? 2 : 4);
-  if (chunks > 128) return cudaErrorInvalidValue;
-  const unsigned grid = 0;
-  return L.variant == 1 ? launch_variant<1>(L, cpl, grid, stream)
-                        : launch_variant<2>(L, cpl, grid, stream);
+  const int64_t rope_lanes = L.R / 8;
+  // the fewest lanes per row that hold the RoPE pairs and at most 4 chunks each
+  int lpr = 0, cpl = 0;
+  for (int cand : {8, 16, 32}) {
+    const int64_t c = (chunks + cand - 1) / cand;
+    if (cand >= rope_lanes && c <= 4) {
+      lpr = cand;
+      cpl = static_cast<int>(c);
+      break;
+    }
+  }
+  if (lpr == 0) return cudaErrorInvalidValue;
+  KvAux aux{};
+  aux.inv_rms = 1.0f / static_cast<float>(rms);
+  aux.bs_shift = -1;
+  if ((L.block_size & (L.block_size - 1)) == 0)
+    for (aux.bs_shift = 0; (int64_t(1) << aux.bs_shift) < L.block_size; ++aux.bs_shift) {
+    }
+  aux.qk = L.k_scale != nullptr;
+  aux.qv = L.v_scale != nullptr;
+  return L.variant == 1 ? launch_variant<1>(L, aux, lpr, cpl, stream)
+                        : launch_variant<2>(L, aux, lpr, cpl, stream);
 }
 
 }  // namespace ra

@@ -42,6 +42,23 @@ SMALL = [
     ("v2_vq_only_n2", dict(variant=2, B=2, N=2, S=40, Dkv=192, Dv=128, block_size=32, block_num=4,
                            quant_v=True)),
     ("v2_n1_wide", dict(variant=2, B=1, N=1, S=50, Dkv=384, Dv=256, block_size=16, block_num=4)),
+    # several rows per warp step: groups that cross head and batch boundaries (S smaller
+    # than the rows a warp handles at once), and fewer rows than lanes
+    ("v2_s1_n8", dict(variant=2, B=3, N=8, S=1, Dkv=192, Dv=128, block_size=32, block_num=1,
+                      quant_k=True, quant_v=True)),
+    ("v2_s3_n8_narrow", dict(variant=2, B=2, N=8, S=3, Dkv=64, Dv=64, block_size=32, block_num=1,
+                             quant_k=True)),
+    # block_size that is not a power of two (division path for the slot)
+    ("v2_bs48", dict(variant=2, B=2, N=2, S=30, Dkv=192, Dv=128, block_size=48, block_num=3)),
+    # every lane of the row holds RoPE pairs
+    ("v2_rope256", dict(variant=2, B=1, N=2, S=20, Dkv=256, Dv=64, rope_size=256, block_size=32,
+                        block_num=1, quant_k=True, quant_v=True)),
+    # v wider than kv, small rope
+    ("v2_v_wider", dict(variant=2, B=2, N=1, S=13, Dkv=64, Dv=512, rope_size=32, block_size=32,
+                        block_num=1, quant_v=True)),
+    # rms_size 1024: four chunks per lane at 32 lanes per row
+    ("v1_wide", dict(variant=1, B=1, N=1, S=17, Dkv=1088, Dv=1024, block_size=32, block_num=1,
+                     quant_k=True, quant_v=True)),
 ]
 
 
