@@ -13,21 +13,22 @@
 // Quantisation uses the fp32 value (before any bf16 rounding); round() is
 // round-half-to-even.
 //
-// GB300 mapping: an HBM stream of short rows (0.6-1.4 KB), so the kernel is
-// built to keep many bytes in flight with few instructions per byte:
+// GB300 mapping: an HBM stream of short rows (0.6-1.4 KB); the kernel is built
+// to keep bytes in flight with few instructions per byte:
 //  * persistent warps, each owning a contiguous range of (b, n, s) rows and
 //    walking (b, n, s) incrementally (no integer division per row);
-//  * a ring of row buffers in registers per warp: while one row is processed
-//    the next one or two are already being loaded;
+//  * a warp works on 32 / LPR rows at once, LPR = 8, 16 or 32 lanes per row
+//    (the fewest that hold the RoPE pairs with at most four 16-byte chunks per
+//    lane), so every lane has work in every phase and per-row costs (slot
+//    lookup, addressing, the RMS shuffle tree) are shared;
+//  * two row groups in registers per lane: one is processed while the next loads;
 //  * the per-channel quantisation scales and offsets (per head in V2) are
-//    staged once per block in shared memory, laid out so a warp's reads are
-//    conflict-free;
-//  * every lane moves 16-byte chunks (8 bf16); the RMS reduction is a warp
-//    shuffle tree; the arithmetic uses packed fp32x2 operations; int8 codes are
-//    rounded with cvt.rni and packed with saturation by cvt.pack.sat;
-//  * lane l < rope_size/8 owns interleaved pairs 4l..4l+3, whose outputs land at
-//    positions 4l and rope_size/2 + 4l of the de-interleaved result.  Cache rows
-//    are contiguous, so each scattered slot is written with whole vectors.
+//    staged once per block in shared memory;
+//  * packed fp32x2 arithmetic; int8 codes are rounded with cvt.rni and packed
+//    with saturation by cvt.pack.sat;
+//  * lane j < rope_size/8 of a row owns interleaved pairs 4j..4j+3, whose outputs
+//    land at positions 4j and rope_size/2 + 4j of the de-interleaved result.
+//    Cache rows are contiguous, so each scattered slot is written with whole vectors.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -140,8 +141,10 @@ struct Cursor {
   }
 };
 
-// Lane layout: a warp processes 32 / LPR rows at once; lane = g * LPR + j works
-// on row g of the group and owns its 16-byte chunks j + LPR * i, i < CPL.
+// Lane layout: a warp processes RPG = 32 / LPR rows at once; lane = j * RPG + g
+// works on row g of the group and owns its 16-byte chunks j + LPR * i, i < CPL
+// (the rows of a group are interleaved across lanes, so lanes that read the same
+// quantisation-table entry sit next to each other).
 template <int VARIANT, int LPR, int CPL>
 struct KvRows {
   const KvLaunch& p;
@@ -195,7 +198,7 @@ struct KvRows {
     }
     float ss = acc.x + acc.y;
 #pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    for (int o = 16; o >= 32 / LPR; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float inv = rsqrtf(fmaf(ss, aux.inv_rms, p.eps));
     const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   constexpr int DEPTH = 2;          // row-group buffers per lane: one processed, one loading
   constexpr int RPG = 32 / LPR;     // rows per warp per step
   const int lane = threadIdx.x & 31;
-  const int g = lane / LPR, j = lane % LPR;
+  const int g = lane % RPG, j = lane / RPG;
   const int64_t rows = p.B * p.N * p.S;
   const int R = p.R;
   const int rms = VARIANT == 1 ? static_cast<int>(p.Dkv) - R : static_cast<int>(p.Dkv);
