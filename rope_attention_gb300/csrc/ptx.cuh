@@ -187,6 +187,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* map, 
       "l"(map), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
+// same, with an L2 cache-eviction policy for the loaded lines
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* map, uint32_t bar_cluster,
+                                                      int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+// L2 policy that keeps the lines it is applied to ahead of normal lines on eviction
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
@@ -244,6 +259,7 @@ __device__ __forceinline__ int scale_exponent(float x) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) { return make_float2(bf16_lo(v), bf16_hi(v)); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -278,6 +278,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (leader && lane == 0) {
       tc_cp_pair_32x128b_warpx4(tmem + SFA_COL, sdesc_scale_rows(sSFA));
+      // shared-memory descriptors of stage 0; a stage or a 32-byte K step only moves
+      // the start-address field (bits [0,14), in 16-byte units, no carry out of it
+      // since every address here is below 2^18), so the loop steps them by addition
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sA);
+      const uint64_t b_desc0 = sdesc_kmajor_sw128(sB);
+      const uint64_t sf_desc0 = sdesc_scale_rows(sSF);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -295,16 +301,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sfb = tmem + SFB_COL + (kb & 1) * 8;
-          const uint32_t sf_s = sSF + stage * SF_BYTES;
-          tc_cp_pair_32x128b_warpx4(sfb, sdesc_scale_rows(sf_s));
-          tc_cp_pair_32x128b_warpx4(sfb + 4, sdesc_scale_rows(sf_s + kSfChunkBytes));
-          const uint32_t a_s = sA + stage * A_BYTES;
-          const uint32_t b_s = sB + stage * B_BYTES;
+          const uint64_t sfd = sf_desc0 + static_cast<uint64_t>(stage * (SF_BYTES >> 4));
+          tc_cp_pair_32x128b_warpx4(sfb, sfd);
+          tc_cp_pair_32x128b_warpx4(sfb + 4, sfd + (kSfChunkBytes >> 4));
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4));
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4));
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint32_t idesc = kIdesc | (uint32_t(kk) << 29) | (uint32_t(kk) << 4);
-            tc_mma_pair_mxf8(tmem + ACC_COL, sdesc_kmajor_sw128(a_s + kk * 32),
-                             sdesc_kmajor_sw128(b_s + kk * 32), idesc, tmem + SFA_COL, sfb,
+            tc_mma_pair_mxf8(tmem + ACC_COL, ad + 2 * kk, bd + 2 * kk, idesc, tmem + SFA_COL, sfb,
                              (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair_multicast(empty_bar(stage), 0x3);
@@ -350,106 +355,107 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       float ssq = 0.f, ssk = 0.f;
       uint16_t* out_row = p.out + static_cast<size_t>(row_ok ? row : 0) * p.I;
       const int col_base = nt * BN + chalf * EPI_COLS;
-      // pass 1: dequant, channel scale and bias in place; sums of squares (of v, before gamma)
-      float amax = 0.f;
+      // pass 1: dequant, channel scale and bias in place (packed fp32x2 arithmetic);
+      // sums of squares of v, before gamma
+      const float2 as2 = make_float2(as, as);
 #pragma unroll
       for (int c = 0; c < EPI_COLS / 16; ++c) {
         const int col0 = col_base + c * 16;
         if (col0 >= p.I) break;  // ragged last column tile; warp-uniform
-        float wch[16], bia[16];
+        float2 bia[8];
+        if (p.bias != nullptr) {
+          const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + col0);
+          const uint4 t0 = __ldg(b4), t1 = __ldg(b4 + 1);
+          bia[0] = bf16x2_to_float2(t0.x); bia[1] = bf16x2_to_float2(t0.y);
+          bia[2] = bf16x2_to_float2(t0.z); bia[3] = bf16x2_to_float2(t0.w);
+          bia[4] = bf16x2_to_float2(t1.x); bia[5] = bf16x2_to_float2(t1.y);
+          bia[6] = bf16x2_to_float2(t1.z); bia[7] = bf16x2_to_float2(t1.w);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) bia[k] = make_float2(0.f, 0.f);
+        }
+        float2 sq2 = make_float2(0.f, 0.f);
         if (p.wch != nullptr) {
           const float4* w4 = reinterpret_cast<const float4*>(p.wch + col0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 t = __ldg(w4 + j);
-            wch[4 * j] = t.x; wch[4 * j + 1] = t.y; wch[4 * j + 2] = t.z; wch[4 * j + 3] = t.w;
-          }
-        } else {
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 w = __ldg(w4 + k4);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) wch[j] = 1.f;
-        }
-        if (p.bias != nullptr) {
-          const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + col0);
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint4 t = __ldg(b4 + j);
-            const uint32_t u[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              bia[8 * j + 2 * k] = bf16_lo(u[k]);
-              bia[8 * j + 2 * k + 1] = bf16_hi(u[k]);
+            for (int h = 0; h < 2; ++h) {
+              const int k = 2 * k4 + h;
+              const float2 acc = make_float2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
+              const float2 v = __ffma2_rn(__fmul2_rn(acc, as2), h ? make_float2(w.z, w.w) : make_float2(w.x, w.y), bia[k]);
+              r[c * 16 + 2 * k] = __float_as_uint(v.x);
+              r[c * 16 + 2 * k + 1] = __float_as_uint(v.y);
+              sq2 = __ffma2_rn(v, v, sq2);
             }
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) bia[j] = 0.f;
+          for (int k = 0; k < 8; ++k) {
+            const float2 acc = make_float2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
+            const float2 v = __ffma2_rn(acc, as2, bia[k]);
+            r[c * 16 + 2 * k] = __float_as_uint(v.x);
+            r[c * 16 + 2 * k + 1] = __float_as_uint(v.y);
+            sq2 = __ffma2_rn(v, v, sq2);
+          }
         }
-        float sq = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float v = fmaf(__uint_as_float(r[c * 16 + j]) * as, wch[j], bia[j]);
-          r[c * 16 + j] = __float_as_uint(v);
-          sq = fmaf(v, v, sq);
-        }
-        if (col0 < p.q_end) ssq += sq;
-        else if (col0 < p.k_end) ssk += sq;
+        if (col0 < p.q_end) ssq += sq2.x + sq2.y;
+        else if (col0 < p.k_end) ssk += sq2.x + sq2.y;
       }
       // the segment-wide gamma of the normed segments, on the columns the second
       // pass rewrites (inv_rms is one scalar per token and segment, and RoPE is
-      // linear, so scaling by gamma here is exact: rot(v * inv * gamma) = inv * rot(v * gamma))
-      const bool rewrite = col_base < p.s_end && col_base + EPI_COLS > p.s_begin;
-      if (rewrite) {
-#pragma unroll
-        for (int c = 0; c < EPI_COLS / 16; ++c) {
-          const int col0 = col_base + c * 16;
-          if (col0 >= p.I) break;
-          if (col0 < p.s_begin || col0 >= p.s_end) continue;
-          const float* g = col0 < p.q_end ? p.q_gamma : p.k_gamma;
-          if (g == nullptr) continue;
-          const float4* g4 = reinterpret_cast<const float4*>(g + (col0 < p.q_end ? col0 : col0 - p.q_end));
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 t = __ldg(g4 + j);
-            r[c * 16 + 4 * j] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j]) * t.x);
-            r[c * 16 + 4 * j + 1] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j + 1]) * t.y);
-            r[c * 16 + 4 * j + 2] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j + 2]) * t.z);
-            r[c * 16 + 4 * j + 3] = __float_as_uint(__uint_as_float(r[c * 16 + 4 * j + 3]) * t.w);
-          }
-        }
-      }
+      // linear, so scaling by gamma here is exact: rot(v * inv * gamma) = inv * rot(v * gamma)),
+      // and the largest |z| of the rewritten columns
+      float amax = 0.f;
 #pragma unroll
       for (int c = 0; c < EPI_COLS / 16; ++c) {
         const int col0 = col_base + c * 16;
         if (col0 >= p.I) break;
         if (col0 < p.s_begin || col0 >= p.s_end) continue;
+        const float* g = col0 < p.q_end ? p.q_gamma : p.k_gamma;
+        if (g != nullptr) {
+          const float4* g4 = reinterpret_cast<const float4*>(g + (col0 < p.q_end ? col0 : col0 - p.q_end));
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 t = __ldg(g4 + k4);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int k = 2 * k4 + h;
+              const float2 v = make_float2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
+              const float2 z = __fmul2_rn(v, h ? make_float2(t.z, t.w) : make_float2(t.x, t.y));
+              r[c * 16 + 2 * k] = __float_as_uint(z.x);
+              r[c * 16 + 2 * k + 1] = __float_as_uint(z.y);
+            }
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(__uint_as_float(r[c * 16 + j])));
       }
       // power-of-two scale for the fp16 encoding: |z| * 2^-e < 2^15
       const int e = scale_exponent(amax);
-      const float down = exp2_int(-e);
+      const float2 down2 = make_float2(exp2_int(-e), exp2_int(-e));
       // pass 2: stores (fp16 of z * 2^-e for the rewritten Q/K columns, bf16 otherwise)
 #pragma unroll
       for (int c = 0; c < EPI_COLS / 16; ++c) {
         const int col0 = col_base + c * 16;
         if (col0 >= p.I) break;
         if (!row_ok) continue;
-        const float* v = reinterpret_cast<const float*>(r + c * 16);
-        uint4 o0, o1;
+        uint32_t o[8];
         if (col0 >= p.s_begin && col0 < p.s_end) {
-          o0.x = pack_f16x2(v[0] * down, v[1] * down);   o0.y = pack_f16x2(v[2] * down, v[3] * down);
-          o0.z = pack_f16x2(v[4] * down, v[5] * down);   o0.w = pack_f16x2(v[6] * down, v[7] * down);
-          o1.x = pack_f16x2(v[8] * down, v[9] * down);   o1.y = pack_f16x2(v[10] * down, v[11] * down);
-          o1.z = pack_f16x2(v[12] * down, v[13] * down); o1.w = pack_f16x2(v[14] * down, v[15] * down);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float2 z = __fmul2_rn(make_float2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1])), down2);
+            o[k] = pack_f16x2(z.x, z.y);
+          }
         } else {
-          o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
-          o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
-          o1.x = pack_bf16x2(v[8], v[9]);   o1.y = pack_bf16x2(v[10], v[11]);
-          o1.z = pack_bf16x2(v[12], v[13]); o1.w = pack_bf16x2(v[14], v[15]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k] = pack_bf16x2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
         }
         uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
-        dst[0] = o0;
-        dst[1] = o1;
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
       }
       const int blk = nt * 2 + chalf;
       if (blk < p.n_exp && row_ok)
