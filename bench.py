@@ -54,7 +54,7 @@ def load_peaks():
 # changes the figure no longer describes it and the bench reports null.
 K1_SOURCES = ("rope_attention_gb300/csrc/qkv_project.cu", "rope_attention_gb300/csrc/ptx.cuh",
               "rope_attention_gb300/csrc/internal.h")
-K1_DRAM_BYTES = {("wan720", "64617c3ecdbb4167"): 3443099904 + 2355922432}
+K1_DRAM_BYTES = {("wan720", "5f249bc50742a291"): 2644123904 + 2364468992}
 
 
 def k1_source_digest() -> str:

@@ -191,6 +191,15 @@ ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_t* a, const
  * projection kernel (default 2e9).  Values < 1000 are raised to 1000. */
 void ra_set_wait_timeout_ns(int64_t ns);
 
+/* Test hook for failure detection.  The next projection launch (qkv_cte_mx or
+ * qkv_cte_mx_project) issues none of its TMA loads, so the waits of its
+ * pipeline run out after the time limit above; every CTA then records the
+ * timeout in the workspace status word, releases its tensor memory and exits,
+ * and qkv_cte_mx_status reports RA_ERR_TIMEOUT.  Nothing is in flight when the
+ * waits give up, so the CUDA context stays usable.  The output of that launch
+ * is undefined.  Applies to one launch, then clears itself. */
+void ra_test_stall_next_projection(void);
+
 /* ========================================================================
  * (b) kv_rms_norm_rope_cache
  * ======================================================================== */

@@ -29,6 +29,7 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<int64_t> g_wait_ns{2000000000LL};
+std::atomic<int> g_stall_next{0};  // ra_test_stall_next_projection
 
 ra_status fail(ra_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ra_status fail(ra_status code, const char* fmt, ...) {
@@ -179,6 +180,7 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
   L.q_gamma = p->q_norm ? qg : nullptr;
   L.k_gamma = p->k_norm ? kg : nullptr;
   L.wait_ns = g_wait_ns.load();
+  L.stall_loads = g_stall_next.exchange(0);
   const char* why = "launch failed";
   cudaError_t e = ra::launch_qkv_project(L, st, &why);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "qkv projection: %s (%s)", why, cudaGetErrorString(e));
@@ -230,6 +232,8 @@ const char* ra_last_error(void) { return g_last_error.c_str(); }
 int32_t ra_abi_version(void) { return 2; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
+
+void ra_test_stall_next_projection(void) { g_stall_next.store(1); }
 
 ra_status qkv_cte_mx_packed_weight_bytes(int64_t H, int64_t I, size_t* bytes) {
   if (!bytes) return fail(RA_ERR_INVALID_ARG, "bytes is NULL");

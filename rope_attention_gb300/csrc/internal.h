@@ -38,6 +38,7 @@ struct ProjLaunch {
   const float* q_gamma;        // [q_end] gamma of a normed Q segment, or null
   const float* k_gamma;        // [k_end - q_end] gamma of a normed K segment, or null
   int64_t wait_ns;
+  int32_t stall_loads;         // test hook: issue no TMA loads, so the pipeline waits run out
 };
 cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why);
 

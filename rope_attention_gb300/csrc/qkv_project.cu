@@ -68,7 +68,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;  // 10 warps: at most 3 per SM sub-partition, so <= 168 registers each
 constexpr int EPI_COLS = BN / 2;      // columns per epilogue warp
-constexpr int GROUP_M = 8;
+constexpr int GROUP_M = 16;          // M-tiles per raster group: W is read from HBM once per group
 
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
@@ -108,6 +108,7 @@ struct Params {
   const float* q_gamma;
   const float* k_gamma;
   uint64_t wait_ns;
+  int32_t stall_loads;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_tile) {
@@ -238,7 +239,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0) {
+    if (lane == 0 && !p.stall_loads) {
       const uint32_t leader_full0 = map_to_rank(full_bar(0), 0);
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
@@ -605,6 +606,7 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.q_gamma = L.q_gamma;
   p.k_gamma = L.k_gamma;
   p.wait_ns = static_cast<uint64_t>(L.wait_ns);
+  p.stall_loads = L.stall_loads;
 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;

@@ -24,7 +24,7 @@ RA_NORM_NONE, RA_NORM_RMS_ACROSS_HEADS = 0, 1
 RA_LAYOUT_BSD, RA_LAYOUT_NBSD = 0, 1
 RA_CACHE_PA, RA_CACHE_PA_BNSD = 1, 2
 
-EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns",
+EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns", "ra_test_stall_next_projection",
            "qkv_cte_mx_packed_weight_bytes", "qkv_cte_mx_pack_weight", "qkv_cte_mx_workspace_bytes",
            "qkv_cte_mx", "qkv_cte_mx_project", "qkv_cte_mx_norm_rope", "qkv_cte_mx_status",
            "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache"]
@@ -72,6 +72,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "ra_last_error": (ctypes.c_char_p, []),
         "ra_abi_version": (i32, []),
         "ra_set_wait_timeout_ns": (None, [i64]),
+        "ra_test_stall_next_projection": (None, []),
         "qkv_cte_mx_packed_weight_bytes": (i32, [i64, i64, ctypes.POINTER(sz)]),
         "qkv_cte_mx_pack_weight": (i32, [P, P, i64, i64, P, sz, P]),
         "qkv_cte_mx_workspace_bytes": (i32, [ctypes.POINTER(QkvCteMxParams), ctypes.POINTER(sz)]),
@@ -127,6 +128,11 @@ def ra_abi_version() -> int:
 
 def ra_set_wait_timeout_ns(ns: int) -> None:
     load().ra_set_wait_timeout_ns(int(ns))
+
+
+def ra_test_stall_next_projection() -> None:
+    """Test hook: the next projection launch issues no loads, so its waits time out."""
+    load().ra_test_stall_next_projection()
 
 
 # ---------------------------------------------------------------- qkv_cte_mx

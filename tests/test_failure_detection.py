@@ -1,0 +1,44 @@
+"""Failure detection in the projection pipeline, without a GPU fault.
+
+Every wait in the projection kernel's pipeline (TMA stage barriers, the
+accumulator hand-over between the MMA issuer and the epilogue) has a time
+limit.  The test hook ra_test_stall_next_projection makes the next launch issue
+none of its loads, so its waits run out with nothing in flight.  The kernel must
+record the timeout in the workspace status word (read on the host through
+qkv_cte_mx_status, which also clears it), release its tensor memory and exit;
+the CUDA context must stay usable, and the next call, with the hook cleared,
+must give the correct result.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from parity_util import as_f64, check_qkv, qkv_reference
+from rope_attention_gb300 import native, runner, synth
+
+pytestmark = pytest.mark.gpu
+
+DEFAULT_WAIT_NS = 2_000_000_000
+
+
+def test_stalled_pipeline_reports_timeout_and_context_survives():
+    case = synth.qkv_tiny()
+    run = runner.QkvRun(case)
+    native.ra_set_wait_timeout_ns(2_000_000)  # 2 ms per wait
+    try:
+        native.ra_test_stall_next_projection()
+        run.project()
+        # the status word is set by every CTA that gave up; the C entry point reports it
+        v = ctypes.c_int32()
+        st = native.load().qkv_cte_mx_status(ctypes.c_void_p(run.workspace.data_ptr()), None,
+                                             ctypes.byref(v))
+        assert st == -6 and v.value == 1, (st, v.value)
+        assert "ran out of time" in native.load().ra_last_error().decode()
+        # the word was cleared by the read, and the hook applied to one launch only
+        run.run()
+        torch.cuda.synchronize()
+        assert run.status() == 0
+    finally:
+        native.ra_set_wait_timeout_ns(DEFAULT_WAIT_NS)
+    check_qkv(case, as_f64(run.out), qkv_reference(case), "call after a timed-out launch")
