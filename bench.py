@@ -145,15 +145,14 @@ class Clocks:
 
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    from rope_attention_gb300 import dist
+    e = dist.env()
+    return e.world, e.rank, e.local_rank
 
 
 def run_ours(args):
     import torch
-    from rope_attention_gb300 import build, native, runner
+    from rope_attention_gb300 import build, dist, native, runner
 
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -208,10 +207,7 @@ def run_ours(args):
     k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     k3 = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
-    if ws > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = dist.max_over_ranks(total_ms, device="cuda")  # the slowest rank's time
     ms = total_ms / K
     flops = qcase.flops
     k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
@@ -227,7 +223,7 @@ def run_ours(args):
     k2_gbs = k2_bytes / (k2_ms * 1e-3) / 1e9
     k3_gbs = k3_bytes / (k3_ms * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
-    value = ws * flops / (ms * 1e-3) / 1e12
+    value = dist.job_rate(flops, ws, ms * 1e-3) / 1e12
 
     e2e = None
     if not args.no_e2e:
@@ -274,7 +270,7 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
     step i+1 and the download of step i-1: two sets of device buffers, and three
     streams (host->device, compute, device->host) ordered by events."""
     import torch
-    from rope_attention_gb300 import runner
+    from rope_attention_gb300 import dist, runner
     q2, k2 = runner.QkvRun(qcase), runner.KvRun(kcase)
     runs = [(q, k), (q2, k2)]
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
@@ -335,12 +331,9 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
     end.record(s_h2d)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / K
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = dist.max_over_ranks(ms, device="cuda")
     del q2, k2
-    return {"value": round(ws * qcase.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(dist.job_rate(qcase.flops, ws, ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "overlap": "uploads, kernels and downloads of consecutive steps on three streams"}
 
