@@ -18,6 +18,8 @@ qkv_cte   : fused QKV projection + across-heads RMSNorm + rotate-half RoPE
             Design 1a-1c, Design 2, Design 5).
 kv_cache  : KvRmsNormRopeCache (CANN ops-transformer "KvRmsNormRopeCache",
             formulas (1)-(5)).
+row_quant : row FP8 quantisation of the activation into the row-packed layout
+            (AWS Neuron "Kernel reference: qkv_cte", Interface).
 
 Every function is pinned by ``tests/test_oracle_pins.py``; no function here is
 "parity unpinned".
@@ -25,3 +27,4 @@ Every function is pinned by ``tests/test_oracle_pins.py``; no function here is
 from .codes import decode_bf16, decode_e4m3, decode_ue8m0  # noqa: F401
 from .kv_cache import kv_rms_norm_rope_cache  # noqa: F401
 from .qkv_cte import qkv_cte_mx  # noqa: F401
+from .row_quant import row_quantize, row_quantize_packed  # noqa: F401

@@ -18,7 +18,7 @@ import pytest
 import torch
 import torch.nn.functional as F
 
-from oracle import codes, kv_cache as okv, qkv_cte as oq
+from oracle import codes, kv_cache as okv, qkv_cte as oq, row_quant as orq
 from rope_attention_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -444,6 +444,92 @@ def test_generator_encodings():
 
 
 # ---------------------------------------------------------------------------
+# row FP8 quantisation (qkv_cte page, Interface: row-packed activation)
+# ---------------------------------------------------------------------------
+def _torch_e4m3_code(v):
+    return torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def check_e4m3_encoder_vs_torch():
+    """The encoder agrees with torch's float8_e4m3fn cast (round-half-even) on every
+    representable value, every midpoint between neighbours, and random values."""
+    mags = codes.decode_e4m3(np.arange(127, dtype=np.uint8))
+    mids = (mags[:-1] + mags[1:]) / 2  # exact in fp32: at most 5 significant bits
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([mags, mids, rng.uniform(-448, 448, 20000), rng.normal(0, 0.01, 5000),
+                           np.array([0.0, -0.0, 2.0 ** -10, -(2.0 ** -10), 2.0 ** -9 * 1.5])])
+    vals = np.concatenate([vals, -vals]).astype(np.float32)
+    assert np.array_equal(orq.encode_e4m3_rne_sat(vals), _torch_e4m3_code(vals))
+
+
+def check_e4m3_encoder_saturates():
+    """Magnitudes above the largest finite value (448) saturate to it, keeping the sign."""
+    big = np.array([448.0001, 464.0, 479.9, 480.0, 1e6, 3e38], dtype=np.float32)
+    assert np.all(orq.encode_e4m3_rne_sat(big) == 0x7E)
+    assert np.all(orq.encode_e4m3_rne_sat(-big) == 0xFE)
+
+
+def check_row_quant_hand():
+    """x = [1, -2, 0.5, 0, ...]: amax 2, inv 224, products [224, -448, 112, 0]:
+    codes 0.1110.110, 1.1111.110, 0.1101.110, 0; scale = 2 / 448 in fp32."""
+    x = np.zeros((1, 16), np.float32)
+    x[0, :4] = [1.0, -2.0, 0.5, 0.0]
+    c, sc = orq.row_quantize(synth.encode_bf16(x))
+    assert list(c[0, :4]) == [0x76, 0xFE, 0x6E, 0x00] and not c[0, 4:].any()
+    assert sc.dtype == np.float32 and sc[0] == np.float32(2.0) / np.float32(448.0)
+
+
+def check_row_quant_zero_row():
+    """A row of zeros has scale 1 and zero codes with the input's sign."""
+    x = np.zeros((2, 16), np.float32)
+    x[1, 3] = -0.0
+    bits = synth.encode_bf16(x)
+    bits[1, 5] = 0x8000  # -0.0
+    c, sc = orq.row_quantize(bits)
+    assert np.all(sc == 1.0)
+    expect = np.zeros((2, 16), np.uint8)
+    expect[1, 5] = 0x80
+    expect[1, 3] = 0x80 if np.signbit(x[1, 3]) else 0
+    assert np.array_equal(c, expect)
+
+
+def check_row_quant_roundtrip():
+    """Dequantised codes reproduce x: the row maximum maps to +-448 exactly, and every
+    value in E4M3's normal range is within half a unit of its 3-bit mantissa."""
+    rng = np.random.default_rng(12)
+    x = (rng.normal(0, 1, (32, 512)) * np.exp2(rng.integers(-12, 12, 32))[:, None]).astype(np.float32)
+    bits = synth.encode_bf16(x)
+    xb = codes.decode_bf16(bits)
+    c, sc = orq.row_quantize(bits)
+    y = codes.decode_e4m3(c) * sc.astype(np.float64)[:, None]
+    amax = np.max(np.abs(xb), axis=1)
+    i = np.argmax(np.abs(xb), axis=1)
+    assert np.all((c[np.arange(32), i] & 0x7F) == 0x7E)
+    normal = np.abs(xb) * (448.0 / amax)[:, None] >= 2.0 ** -6
+    rel = np.abs(y - xb)[normal] / np.abs(xb)[normal]
+    assert rel.max() <= 2.0 ** -4 * (1 + 1e-5)
+    assert np.allclose(sc, amax / 448.0, rtol=2 ** -23, atol=0)
+
+
+def check_row_quant_packed():
+    """The packed row: H codes, then the fp32 scale's four bytes."""
+    rng = np.random.default_rng(13)
+    bits = synth.encode_bf16(rng.normal(0, 3, (5, 48)).astype(np.float32))
+    pk = orq.row_quantize_packed(bits)
+    c, sc = orq.row_quantize(bits)
+    assert pk.shape == (5, 52) and np.array_equal(pk[:, :48], c)
+    assert np.array_equal(np.ascontiguousarray(pk[:, 48:]).view("<f4").ravel(), sc)
+
+
+@pytest.mark.parametrize("check", [check_e4m3_encoder_vs_torch, check_e4m3_encoder_saturates,
+                                   check_row_quant_hand, check_row_quant_zero_row,
+                                   check_row_quant_roundtrip, check_row_quant_packed])
+def test_row_quant(check):
+    check()
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: every mutant must be caught by at least one check
 # ---------------------------------------------------------------------------
 ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_block_scales,
@@ -451,7 +537,9 @@ ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_blo
               check_qkv_norm_segments, check_qkv_single_segment, check_qkv_norm_then_rope,
               check_rotate_half_invariants, check_interleave_rope, check_quant_hand,
               check_kv_v1_bf16, check_kv_v1_int8, check_kv_v2_int8, check_kv_v2_pa_bf16,
-              check_kv_bad_index]
+              check_kv_bad_index, check_e4m3_encoder_vs_torch, check_e4m3_encoder_saturates,
+              check_row_quant_hand, check_row_quant_zero_row, check_row_quant_roundtrip,
+              check_row_quant_packed]
 
 
 def mutants():
@@ -507,7 +595,33 @@ def mutants():
         rms = np.sqrt(np.sum(x * x, axis=-1, keepdims=True) / n + eps)
         return x / rms * g
 
-    return [(oq, "rope_rotate_half", rh_sign), (oq, "rms_norm_across_heads", norm_no_eps),
+    orig_enc = orq.encode_e4m3_rne_sat
+    orig_rq = orq.row_quantize
+
+    def enc_half_away(v):                   # E4M3 ties rounded away from zero
+        v = np.asarray(v, np.float32)
+        c = orig_enc(v)
+        up = orig_enc(np.nextafter(np.abs(v), np.float32(np.inf)) * np.where(np.signbit(v), -1, 1))
+        mags = codes.decode_e4m3(np.arange(127, dtype=np.uint8))
+        mids = (mags[:-1] + mags[1:]) / 2
+        tie = np.isin(np.abs(v).astype(np.float64), mids)
+        return np.where(tie, up, c).astype(np.uint8)
+
+    def enc_no_saturation(v):               # out-of-range magnitudes become NaN codes
+        v = np.asarray(v, np.float32)
+        c = orig_enc(v)
+        return np.where(np.abs(v) > 448, (c & 0x80) | 0x7F, c).astype(np.uint8)
+
+    def rq_fnuz_range(bits):                # scaled onto +-240 instead of +-448
+        c, sc = orig_rq(bits)
+        x = codes.decode_bf16(np.asarray(bits, np.uint16)).astype(np.float32)
+        amax = np.max(np.abs(x), axis=1).astype(np.float32)
+        safe = np.where(amax == 0, np.float32(1), amax)
+        return orig_enc(x * (np.float32(240) / safe)[:, None]), (safe / np.float32(240)).astype(np.float32)
+
+    return [(orq, "encode_e4m3_rne_sat", enc_half_away), (orq, "encode_e4m3_rne_sat", enc_no_saturation),
+            (orq, "row_quantize", rq_fnuz_range),
+            (oq, "rope_rotate_half", rh_sign), (oq, "rms_norm_across_heads", norm_no_eps),
             (oq, "rms_norm_across_heads", norm_pre_gamma_width), (oq, "dequant_weight", dw_transposed_blocks),
             (okv, "interleave_rope", il_no_deinterleave), (okv, "quantize", q_half_away),
             (okv, "quantize", q_offset_after_round), (codes, "decode_e4m3", e4m3_bias8),
