@@ -225,6 +225,8 @@ def run_ours(args):
     hbm = peaks["hbm_gbs"]
     value = dist.job_rate(flops, ws, ms * 1e-3) / 1e12
 
+    nxt = {} if args.no_next else {"row_quantize_e4m3": time_row_quantize(qcase, args, hbm)}
+
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(q, k, qcase, kcase, args, ws)
@@ -252,6 +254,7 @@ def run_ours(args):
         },
         "clocks": clk.summary(),
         "gpu_launches": 3 * K,
+        "next": nxt,
     }
     if e2e is not None:
         line["e2e"] = e2e
@@ -261,6 +264,33 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def time_row_quantize(qcase, args, hbm_gbs):
+    """The row FP8 quantiser (the step before the projection) on the workload's bf16
+    hidden state [T, H], timed alone: CUDA events over K launches after W warm-ups."""
+    import torch
+    from rope_attention_gb300 import native, runner, synth
+    T, H = qcase.T, qcase.H
+    x = runner.to_dev(synth.hidden_bf16(4, T, H))
+    codes = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    scale = torch.empty((T,), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        native.row_quantize_e4m3(x, codes, scale)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        native.row_quantize_e4m3(x, codes, scale)
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    nbytes = T * H * 2 + T * H + T * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del x, codes, scale
+    return {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4),
+            "input": f"bf16 hidden state [{T}, {H}] (N(0,1), row factors 2^U(-3,3), 1% outlier channels x8)",
+            "note": "measured alone, not part of the step"}
 
 
 def measure_e2e(q, k, qcase, kcase, args, ws):
@@ -413,6 +443,7 @@ def main():
     ap.add_argument("--oracle-rows", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the rows measured outside the step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -201,6 +201,35 @@ void ra_set_wait_timeout_ns(int64_t ns);
 void ra_test_stall_next_projection(void);
 
 /* ========================================================================
+ * Row FP8 quantisation of the activation (the step before qkv_cte_mx)
+ * ======================================================================== */
+
+/* AWS Neuron "Kernel reference: qkv_cte", section "Interface": the projection's
+ * input is a row-packed activation -- H FP8 (E4M3) codes followed by a 4-byte
+ * fp32 dequantisation scale per row -- made by a row quantiser from the bf16
+ * hidden state.  The page gives no formula; this library computes, per row t,
+ *   m = max(max_h |x[t,h]|, 2^-100),  scale[t] = m / 448,
+ *   code[t,h] = E4M3(x[t,h] * (448 / m)),
+ * every step in fp32 rounded to nearest-even, the E4M3 rounding half-to-even and
+ * saturated to +-448 (the sign of zero is kept); the floor keeps 448 / m finite
+ * for rows of zeros or of bf16 subnormals.  Inputs must be finite.
+ *
+ * row_quantize_e4m3: the split form qkv_cte_mx reads (`a` and `a_scale`).
+ *   x      [T, H] bf16 bit patterns, device, 16-byte aligned
+ *   codes  [T, H] E4M3 codes, device, 8-byte aligned (written)
+ *   scale  [T] fp32 dequantisation scales, device, 4-byte aligned (written)
+ * row_quantize_e4m3_packed: the page's row-packed layout.
+ *   packed [T, H + 4] bytes, device, 4-byte aligned (written): row t holds its H
+ *          codes, then its scale as a little-endian IEEE binary32.
+ * T >= 1; H a positive multiple of 8.  All buffers are caller-owned; the call is
+ * asynchronous on `stream` and allocates nothing.  Errors: RA_ERR_INVALID_ARG
+ * (NULL pointer, bad size), RA_ERR_ALIGNMENT, RA_ERR_CUDA (launch failure). */
+ra_status row_quantize_e4m3(const uint16_t* x, int64_t T, int64_t H, uint8_t* codes, float* scale,
+                            void* stream);
+ra_status row_quantize_e4m3_packed(const uint16_t* x, int64_t T, int64_t H, uint8_t* packed,
+                                   void* stream);
+
+/* ========================================================================
  * (b) kv_rms_norm_rope_cache
  * ======================================================================== */
 

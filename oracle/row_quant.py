@@ -7,13 +7,14 @@ a row quantiser (row_quantize_packed); the projection kernel itself does not
 quantise.  The page names the operation and its output layout but gives no
 formula.  The reading used here is symmetric absmax scaling onto the E4M3 range:
 
-    amax[t]   = max_h |x[t, h]|                   (exact: x is bf16)
-    scale[t]  = amax[t] / 448                     fp32, rounded to nearest -- the dequant scale
-    inv[t]    = 448 / amax[t]                     fp32, rounded to nearest
+    m[t]      = max(max_h |x[t, h]|, 2^-100)      (exact: x is bf16; the floor keeps
+                                                  448 / m finite for rows of zeros or of
+                                                  bf16 subnormals)
+    scale[t]  = m[t] / 448                        fp32, rounded to nearest -- the dequant scale
+    inv[t]    = 448 / m[t]                        fp32, rounded to nearest
     code[t,h] = E4M3(x[t, h] * inv[t])            the fp32 product rounded to nearest, then
                                                   rounded to E4M3 half-to-even, saturated
                                                   to +-448, the sign of zero kept
-    a row of zeros has scale 1 and inv 0 (all its codes are zeros of x's sign).
 
 The codes are integers that floating point decides, so every step is taken in
 fp32, the precision the definition above fixes (numpy float32 arithmetic is
@@ -26,6 +27,7 @@ import numpy as np
 from .codes import decode_bf16, decode_e4m3
 
 E4M3_MAX = 448.0
+AMAX_FLOOR = 2.0 ** -100
 
 # the 127 non-negative finite E4M3 magnitudes, in code order (codes 0x00..0x7E);
 # they increase with the code
@@ -50,11 +52,9 @@ def encode_e4m3_rne_sat(v: np.ndarray) -> np.ndarray:
 def row_quantize(x_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     """bf16 bit patterns [T, H] -> (E4M3 codes [T, H] uint8, dequant scale [T] float32)."""
     x = decode_bf16(np.asarray(x_bits, dtype=np.uint16)).astype(np.float32)
-    amax = np.max(np.abs(x), axis=1).astype(np.float32)
-    zero = amax == np.float32(0)
-    safe = np.where(zero, np.float32(1), amax).astype(np.float32)
-    scale = np.where(zero, np.float32(1), safe / np.float32(E4M3_MAX)).astype(np.float32)
-    inv = np.where(zero, np.float32(0), np.float32(E4M3_MAX) / safe).astype(np.float32)
+    m = np.maximum(np.max(np.abs(x), axis=1), np.float32(AMAX_FLOOR)).astype(np.float32)
+    scale = (m / np.float32(E4M3_MAX)).astype(np.float32)
+    inv = (np.float32(E4M3_MAX) / m).astype(np.float32)
     prod = (x * inv[:, None]).astype(np.float32)
     return encode_e4m3_rne_sat(prod), scale
 

@@ -24,7 +24,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "librope_attention.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "qkv_project.cu", "qk_norm_rope.cu", "kv_cache.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "qkv_project.cu", "qk_norm_rope.cu", "kv_cache.cu", "noalloc.cu", "row_quant.cu"]
 
 
 def nvcc() -> str:

@@ -8,6 +8,7 @@
 
 #include "rope_attention.h"
 #include "internal.h"
+#include "row_quant.h"
 
 namespace ra {
 
@@ -327,6 +328,31 @@ ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_statu
   *device_status = v;
   if (v != 0) return fail(RA_ERR_TIMEOUT, "a projection pipeline wait ran out of time (status %d)", v);
   return ok();
+}
+
+static ra_status row_quantize_common(const uint16_t* x, int64_t T, int64_t H, uint8_t* codes,
+                                     float* scale, bool packed, void* stream) {
+  if (!x || !codes || (!packed && !scale)) return fail(RA_ERR_INVALID_ARG, "x, codes (and scale) are required");
+  if (T < 1 || H < 8 || H % 8 != 0 || H > (int64_t(1) << 30))
+    return fail(RA_ERR_INVALID_ARG, "T >= 1 and H a positive multiple of 8 are required");
+  if (!aligned16(x)) return fail(RA_ERR_ALIGNMENT, "x must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(codes) & (packed ? 3u : 7u)) != 0 ||
+      (scale && (reinterpret_cast<uintptr_t>(scale) & 3u) != 0))
+    return fail(RA_ERR_ALIGNMENT, packed ? "packed must be 4-byte aligned"
+                                         : "codes must be 8-byte and scale 4-byte aligned");
+  cudaError_t e = ra::launch_row_quantize(x, T, H, codes, scale, packed, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "row_quantize launch");
+  return ok();
+}
+
+ra_status row_quantize_e4m3(const uint16_t* x, int64_t T, int64_t H, uint8_t* codes, float* scale,
+                            void* stream) {
+  return row_quantize_common(x, T, H, codes, scale, false, stream);
+}
+
+ra_status row_quantize_e4m3_packed(const uint16_t* x, int64_t T, int64_t H, uint8_t* packed,
+                                   void* stream) {
+  return row_quantize_common(x, T, H, packed, nullptr, true, stream);
 }
 
 ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const uint16_t* kv,

@@ -27,7 +27,7 @@ RA_CACHE_PA, RA_CACHE_PA_BNSD = 1, 2
 EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns", "ra_test_stall_next_projection",
            "qkv_cte_mx_packed_weight_bytes", "qkv_cte_mx_pack_weight", "qkv_cte_mx_workspace_bytes",
            "qkv_cte_mx", "qkv_cte_mx_project", "qkv_cte_mx_norm_rope", "qkv_cte_mx_status",
-           "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache"]
+           "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache", "row_quantize_e4m3", "row_quantize_e4m3_packed"]
 
 
 class RAError(RuntimeError):
@@ -83,6 +83,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qkv_cte_mx_noalloc": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, P, P]),
         "kv_rms_norm_rope_cache": (i32, [ctypes.POINTER(KvRmsNormRopeCacheParams), P, P, P, P, P,
                                          P, P, P, P, P, P, P, P, P, P, P]),
+        "row_quantize_e4m3": (i32, [P, i64, i64, P, P, P]),
+        "row_quantize_e4m3_packed": (i32, [P, i64, i64, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -222,3 +224,18 @@ def kv_rms_norm_rope_cache(params, kv, gamma, cos, sin, index, k_cache, ckv_cach
         _ptr(_bits16(v_optional), None, "v_optional"), _ptr(_bits16(k_rope), None, "k_rope"),
         _ptr(_bits16(c_kv), None, "c_kv"), _ptr(dev_error_count, torch.int32, "dev_error_count"),
         _stream(stream)))
+
+
+# ---------------------------------------------------------------- row quantisation
+def row_quantize_e4m3(x: torch.Tensor, codes: torch.Tensor, scale: torch.Tensor, stream=None) -> None:
+    """x [T, H] bf16 -> codes [T, H] uint8 (E4M3) and scale [T] float32, on the device."""
+    T, H = x.shape
+    _check(load().row_quantize_e4m3(_ptr(x, torch.bfloat16, "x"), T, H, _ptr(codes, torch.uint8, "codes"),
+                                    _ptr(scale, torch.float32, "scale"), _stream(stream)))
+
+
+def row_quantize_e4m3_packed(x: torch.Tensor, packed: torch.Tensor, stream=None) -> None:
+    """x [T, H] bf16 -> packed [T, H + 4] uint8 (codes, then the fp32 scale's bytes)."""
+    T, H = x.shape
+    _check(load().row_quantize_e4m3_packed(_ptr(x, torch.bfloat16, "x"), T, H,
+                                           _ptr(packed, torch.uint8, "packed"), _stream(stream)))

@@ -227,6 +227,24 @@ def qkv_wan720(seed: int = 4) -> QKVCase:
     return qkv_wan_self(seed, wan_latent_grid(81, 720, 1280), "qkv_wan720")
 
 
+def hidden_bf16(seed: int, T: int, H: int, *, k: int = 20, rows_per_chunk: int = 4096) -> np.ndarray:
+    """bf16 hidden state [T, H] (bit patterns) for the row quantiser: N(0,1) entries,
+    a per-row factor 2^U(-3,3), and 1 % of the channels (a fixed set) scaled by 8,
+    the outlier channels of transformer activations.  Generated in row chunks so
+    that full-size inputs need little host memory."""
+    g = stream(seed, k)
+    outliers = g.choice(H, max(1, H // 100), replace=False)
+    col = np.ones(H, np.float32)
+    col[outliers] = 8.0
+    out = np.empty((T, H), np.uint16)
+    for r0 in range(0, T, rows_per_chunk):
+        r1 = min(T, r0 + rows_per_chunk)
+        x = g.standard_normal((r1 - r0, H), dtype=np.float32)
+        x *= np.exp2(g.uniform(-3, 3, (r1 - r0, 1))).astype(np.float32) * col[None, :]
+        out[r0:r1] = encode_bf16(x)
+    return out
+
+
 def qkv_wan_cross(seed: int = 2) -> list[QKVCase]:
     """Wan2.2-A14B cross-attention: three single-segment calls (num_kv_heads=0).
 

@@ -188,3 +188,30 @@ def kv_call(L, p, **over):
 def test_kv_rejected(L, pkw, over, code):
     st, msg = status_and_msg(L, kv_call(L, kp(**pkw), **over))
     assert st == code and msg, (st, msg)
+
+
+# ---------------------------------------------------------------- row quantiser
+@pytest.mark.parametrize("what,args,status,msg", [
+    ("null x", (None, 4, 64, A16, A16), -1, "required"),
+    ("null codes", (A16, 4, 64, None, A16), -1, "required"),
+    ("null scale", (A16, 4, 64, A16, None), -1, "required"),
+    ("no rows", (A16, 0, 64, A16, A16), -1, "multiple of 8"),
+    ("H not a multiple of 8", (A16, 4, 60, A16, A16), -1, "multiple of 8"),
+    ("x misaligned", (A16 + 8, 4, 64, A16, A16), -3, "x must be"),
+    ("codes misaligned", (A16, 4, 64, A16 + 4, A16), -3, "aligned"),
+    ("scale misaligned", (A16, 4, 64, A16, A16 + 2), -3, "aligned"),
+])
+def test_row_quantize_rejections(L, what, args, status, msg):
+    x, T, H, codes, scale = args
+    st = L.row_quantize_e4m3(x, T, H, codes, scale, None)
+    assert st == status, what
+    assert msg in L.ra_last_error().decode(), what
+
+
+@pytest.mark.parametrize("what,args,status", [
+    ("null packed", (A16, 4, 64, None), -1),
+    ("H not a multiple of 8", (A16, 4, 12, A16), -1),
+    ("packed misaligned", (A16, 4, 64, A16 + 2), -3),
+])
+def test_row_quantize_packed_rejections(L, what, args, status):
+    assert L.row_quantize_e4m3_packed(*args, None) == status, what

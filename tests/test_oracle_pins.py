@@ -481,17 +481,21 @@ def check_row_quant_hand():
 
 
 def check_row_quant_zero_row():
-    """A row of zeros has scale 1 and zero codes with the input's sign."""
+    """A row of zeros: zero codes with the input's sign, scale 2^-100 / 448; a row of
+    bf16 subnormals (amax below the 2^-100 floor) stays finite and small."""
     x = np.zeros((2, 16), np.float32)
-    x[1, 3] = -0.0
     bits = synth.encode_bf16(x)
     bits[1, 5] = 0x8000  # -0.0
     c, sc = orq.row_quantize(bits)
-    assert np.all(sc == 1.0)
+    assert np.all(sc == np.float32(2.0 ** -100) / np.float32(448))
     expect = np.zeros((2, 16), np.uint8)
     expect[1, 5] = 0x80
-    expect[1, 3] = 0x80 if np.signbit(x[1, 3]) else 0
     assert np.array_equal(c, expect)
+    sub = np.zeros((1, 16), np.uint16)
+    sub[0, :3] = [0x0001, 0x8040, 0x007F]  # subnormal bf16 values, |x| < 2^-126
+    c, sc = orq.row_quantize(sub)
+    assert np.isfinite(sc).all() and not np.any((c & 0x7F) == 0x7F)
+    assert np.all((c & 0x7F) <= 0x08)  # tiny codes: |x| * 448 * 2^100 < 2^-6
 
 
 def check_row_quant_roundtrip():
@@ -615,8 +619,7 @@ def mutants():
     def rq_fnuz_range(bits):                # scaled onto +-240 instead of +-448
         c, sc = orig_rq(bits)
         x = codes.decode_bf16(np.asarray(bits, np.uint16)).astype(np.float32)
-        amax = np.max(np.abs(x), axis=1).astype(np.float32)
-        safe = np.where(amax == 0, np.float32(1), amax)
+        safe = np.maximum(np.max(np.abs(x), axis=1), np.float32(2.0 ** -100)).astype(np.float32)
         return orig_enc(x * (np.float32(240) / safe)[:, None]), (safe / np.float32(240)).astype(np.float32)
 
     return [(orq, "encode_e4m3_rne_sat", enc_half_away), (orq, "encode_e4m3_rne_sat", enc_no_saturation),
