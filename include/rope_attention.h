@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
   RA_OK = 0,
   RA_ERR_INVALID_ARG = -1,   /* bad shape, null pointer, illegal combination          */
-  RA_ERR_UNSUPPORTED = -2,   /* legal on the pages but not built here (e.g. NBSd)      */
+  RA_ERR_UNSUPPORTED = -2,   /* legal on the pages but not built here                  */
   RA_ERR_ALIGNMENT = -3,     /* pointer or stride violates a 16-byte alignment rule    */
   RA_ERR_WORKSPACE = -4,     /* workspace / packed-weight buffer too small             */
   RA_ERR_CUDA = -5,          /* a CUDA runtime call failed                             */
@@ -86,7 +86,10 @@ typedef struct {
   int32_t k_norm;         /* RA_NORM_* for the K segment; must be NONE when num_kv_heads == 0 */
   int32_t fused_rope;     /* 1 = rotate-half RoPE on Q and K; needs cos/sin caches    */
   float norm_eps;         /* epsilon inside the square root                           */
-  int32_t output_layout;  /* RA_LAYOUT_BSD only; RA_LAYOUT_NBSD -> RA_ERR_UNSUPPORTED  */
+  int32_t output_layout;  /* RA_LAYOUT_BSD: out [B, S, I]; RA_LAYOUT_NBSD: out
+                           * [I / head_dim, B, S, head_dim], heads in column order (Q
+                           * heads, then K, then V), the layout the page gives the
+                           * cross-attention calls ("Interface", output_layout) */
 } qkv_cte_mx_params;
 
 /* Size in bytes of the packed weight for an [H, I] MX weight. */

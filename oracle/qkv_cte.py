@@ -109,3 +109,15 @@ def qkv_cte_mx(a, a_scale, w, w_block_exp, *, num_heads: int, num_kv_heads: int,
             y = rope_rotate_half(y, cos, sin, head_dim)
         out[:, lo:hi] = y
     return out
+
+
+def to_nbsd(out: np.ndarray, B: int, S: int, head_dim: int) -> np.ndarray:
+    """The NBSd output layout (qkv_cte page, "Interface": output_layout NBSd for the
+    cross-attention calls): [B*S, I] -> [I / head_dim, B, S, head_dim], head n being
+    columns [n*head_dim, (n+1)*head_dim) in the order Q heads, K heads, V heads."""
+    T, I = out.shape
+    n = I // head_dim
+    res = np.empty((n, B, S, head_dim), dtype=out.dtype)
+    for h in range(n):
+        res[h] = out[:, h * head_dim:(h + 1) * head_dim].reshape(B, S, head_dim)
+    return res

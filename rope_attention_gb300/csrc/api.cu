@@ -85,9 +85,8 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   if (p->fused_rope != 0 && p->fused_rope != 1) return fail(RA_ERR_INVALID_ARG, "fused_rope must be 0 or 1");
   if (!(p->norm_eps >= 0.f) || !std::isfinite(p->norm_eps))
     return fail(RA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
-  if (p->output_layout == RA_LAYOUT_NBSD)
-    return fail(RA_ERR_UNSUPPORTED, "output_layout NBSd is not built; use BSD");
-  if (p->output_layout != RA_LAYOUT_BSD) return fail(RA_ERR_INVALID_ARG, "unknown output_layout");
+  if (p->output_layout != RA_LAYOUT_BSD && p->output_layout != RA_LAYOUT_NBSD)
+    return fail(RA_ERR_INVALID_ARG, "unknown output_layout");
   const int64_t T = p->B * p->S;
   const int64_t I = static_cast<int64_t>(p->num_heads + 2 * p->num_kv_heads) * p->head_dim;
   if (T > 0x7fffffffLL || I > 0x7fffffffLL || p->H > 0x7fffffffLL || T * I > (1LL << 40))
@@ -182,6 +181,8 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
   L.k_gamma = p->k_norm ? kg : nullptr;
   L.wait_ns = g_wait_ns.load();
   L.stall_loads = g_stall_next.exchange(0);
+  L.head_dim = p->head_dim;
+  L.nbsd = p->output_layout == RA_LAYOUT_NBSD;
   const char* why = "launch failed";
   cudaError_t e = ra::launch_qkv_project(L, st, &why);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "qkv projection: %s (%s)", why, cudaGetErrorString(e));
@@ -213,6 +214,7 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
   L.n_exp_blocks = s.n_exp_blocks;
   L.exp_stride = s.exp_stride;
   L.eps = p->norm_eps;
+  L.nbsd = p->output_layout == RA_LAYOUT_NBSD;
   cudaError_t e = ra::launch_qk_norm_rope(L, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm/rope launch");
   return RA_OK;

@@ -39,6 +39,8 @@ struct ProjLaunch {
   const float* k_gamma;        // [k_end - q_end] gamma of a normed K segment, or null
   int64_t wait_ns;
   int32_t stall_loads;         // test hook: issue no TMA loads, so the pipeline waits run out
+  int32_t head_dim;
+  int32_t nbsd;                // out is [I / head_dim, T, head_dim] instead of [T, I]
 };
 cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why);
 
@@ -60,6 +62,7 @@ struct NormRopeLaunch {
   int32_t n_part_tiles, part_stride;
   int32_t n_exp_blocks, exp_stride;
   float eps;
+  int32_t nbsd;                // out is [I / head_dim, T, head_dim] instead of [T, I]
 };
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);
 

@@ -104,12 +104,15 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
     const int seg = col < q_end ? 0 : 1;
     const int blk_lo = col / kPartCols, blk_hi = (col + half) / kPartCols;
     const int jc = rotate ? 8 * u : 0;  // lane of the head for cos/sin
+    // where token t's columns [col, col + 8) live: BSD [T, I], or NBSd [I / d, T, d]
+    const int64_t base = p.nbsd ? static_cast<int64_t>(col / d) * p.T * d + col % d : col;
+    const int64_t tstride = p.nbsd ? d : p.I;
     for (int tb = 0; tb < ntok; tb += kUnroll) {
       uint4 cl[kUnroll], ch[kUnroll];
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
         if (tb + k < ntok) {
-          const uint16_t* src = p.out + (t0 + tb + k) * p.I + col;
+          const uint16_t* src = p.out + (t0 + tb + k) * tstride + base;
           cl[k] = __ldcs(reinterpret_cast<const uint4*>(src));
           if (rotate) ch[k] = __ldcs(reinterpret_cast<const uint4*>(src + half));
         }
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
         const int64_t t = t0 + tb + k;
         const int8_t* ex = p.exps + t * p.exp_stride;
         const float inv = s_inv[tb + k][seg];
-        uint16_t* dst = p.out + t * p.I + col;
+        uint16_t* dst = p.out + t * tstride + base;
         float2 y_lo[4];
         decode8(cl[k], inv * exp2_int(ex[blk_lo]), y_lo);
         if (rotate) {

@@ -109,6 +109,7 @@ struct Params {
   const float* k_gamma;
   uint64_t wait_ns;
   int32_t stall_loads;
+  int32_t head_dim, nbsd;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_tile) {
@@ -354,7 +355,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const bool row_ok = row < p.T;
       const float as = row_ok ? __ldg(p.a_scale + row) : 0.f;
       float ssq = 0.f, ssk = 0.f;
-      uint16_t* out_row = p.out + static_cast<size_t>(row_ok ? row : 0) * p.I;
+      const size_t orow = static_cast<size_t>(row_ok ? row : 0);
+      uint16_t* out_row = p.out + orow * p.I;
       const int col_base = nt * BN + chalf * EPI_COLS;
       // pass 1: dequant, channel scale and bias in place (packed fp32x2 arithmetic);
       // sums of squares of v, before gamma
@@ -454,7 +456,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < 8; ++k)
             o[k] = pack_bf16x2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
         }
-        uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
+        // BSD: [T, I]; NBSd: [I / head_dim, T, head_dim] (a 16-column chunk never crosses a head)
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.nbsd ? p.out + (static_cast<size_t>(col0 / p.head_dim) * p.T + orow) * p.head_dim + col0 % p.head_dim
+                   : out_row + col0);
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
       }
@@ -607,6 +612,8 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.k_gamma = L.k_gamma;
   p.wait_ns = static_cast<uint64_t>(L.wait_ns);
   p.stall_loads = L.stall_loads;
+  p.head_dim = L.head_dim;
+  p.nbsd = L.nbsd;
 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;

@@ -28,7 +28,8 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 class QkvRun:
     """Device buffers for one qkv_cte_mx call of a synth.QKVCase."""
 
-    def __init__(self, case: synth.QKVCase, device: str = "cuda", stream=None):
+    def __init__(self, case: synth.QKVCase, device: str = "cuda", stream=None,
+                 layout: int = native.RA_LAYOUT_BSD):
         self.case = case
         c = case
         self.params = native.QkvCteMxParams(
@@ -36,7 +37,7 @@ class QkvRun:
             head_dim=c.head_dim,
             q_norm=native.RA_NORM_RMS_ACROSS_HEADS if c.q_norm else native.RA_NORM_NONE,
             k_norm=native.RA_NORM_RMS_ACROSS_HEADS if c.k_norm else native.RA_NORM_NONE,
-            fused_rope=1 if c.fused_rope else 0, norm_eps=c.eps, output_layout=native.RA_LAYOUT_BSD)
+            fused_rope=1 if c.fused_rope else 0, norm_eps=c.eps, output_layout=layout)
         self.a = to_dev(c.a, device)
         self.a_scale = to_dev(c.a_scale, device)
         w = to_dev(c.w, device)
@@ -50,7 +51,8 @@ class QkvRun:
         self.sin = to_dev(c.sin, device) if c.fused_rope else None
         self.q_gamma = to_dev(c.q_gamma, device) if c.q_norm else None
         self.k_gamma = to_dev(c.k_gamma, device) if c.k_norm else None
-        self.out = torch.empty((c.T, c.I), dtype=torch.bfloat16, device=device)
+        shape = (c.T, c.I) if layout == native.RA_LAYOUT_BSD else (c.I // c.head_dim, c.T, c.head_dim)
+        self.out = torch.empty(shape, dtype=torch.bfloat16, device=device)
         nws = native.qkv_cte_mx_workspace_bytes(self.params)
         self.workspace = torch.zeros(nws, dtype=torch.uint8, device=device)
 

@@ -65,7 +65,7 @@ def status_and_msg(L, st):
 @pytest.mark.parametrize("kw,code", [
     (dict(H=100), -1), (dict(H=0), -1), (dict(B=0), -1), (dict(S=0), -1), (dict(num_heads=0), -1),
     (dict(num_kv_heads=-1), -1), (dict(head_dim=24), -1), (dict(q_norm=3), -1),
-    (dict(num_kv_heads=0, k_norm=1), -1), (dict(output_layout=1), -2), (dict(output_layout=7), -1),
+    (dict(num_kv_heads=0, k_norm=1), -1), (dict(output_layout=2), -1), (dict(output_layout=7), -1),
     (dict(norm_eps=-1.0), -1), (dict(norm_eps=float("nan")), -1), (dict(fused_rope=2), -1),
 ])
 def test_qkv_params_rejected(L, kw, code):

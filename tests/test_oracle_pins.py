@@ -533,6 +533,24 @@ def test_row_quant(check):
     check()
 
 
+def check_nbsd_layout():
+    """NBSd puts token (b, s)'s head h at [h, b, s, :]: checked against an
+    explicit index formula on a tensor whose entries encode their position."""
+    B, S, d, n = 2, 3, 4, 5
+    out = np.arange(B * S * n * d, dtype=np.float64).reshape(B * S, n * d)
+    r = oq.to_nbsd(out, B, S, d)
+    assert r.shape == (n, B, S, d)
+    for h in range(n):
+        for b in range(B):
+            for s_ in range(S):
+                for j in range(d):
+                    assert r[h, b, s_, j] == (b * S + s_) * n * d + h * d + j
+
+
+def test_nbsd_layout():
+    check_nbsd_layout()
+
+
 # ---------------------------------------------------------------------------
 # planted mistakes: every mutant must be caught by at least one check
 # ---------------------------------------------------------------------------
@@ -543,7 +561,7 @@ ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_blo
               check_kv_v1_bf16, check_kv_v1_int8, check_kv_v2_int8, check_kv_v2_pa_bf16,
               check_kv_bad_index, check_e4m3_encoder_vs_torch, check_e4m3_encoder_saturates,
               check_row_quant_hand, check_row_quant_zero_row, check_row_quant_roundtrip,
-              check_row_quant_packed]
+              check_row_quant_packed, check_nbsd_layout]
 
 
 def mutants():

@@ -11,14 +11,15 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from parity_util import as_f64, check_bf16, check_qkv, qkv_reference
-from rope_attention_gb300 import runner, synth
+from rope_attention_gb300 import native, runner, synth
 
 pytestmark = pytest.mark.gpu
 
 
-def run_full(case, split=False):
-    r = runner.QkvRun(case)
+def run_full(case, split=False, layout=native.RA_LAYOUT_BSD):
+    r = runner.QkvRun(case, layout=layout)
     if split:
         r.project()
         r.norm_rope()
@@ -58,6 +59,32 @@ def test_small(name, kw):
     case = synth.make_qkv(name, 200 + len(name), **kw)
     r = run_full(case)
     check_qkv(case, as_f64(r.out), qkv_reference(case), name)
+
+
+NBSD = [
+    ("tiny_qkv", dict(S=128, H=256, num_heads=2, num_kv_heads=2, head_dim=64)),
+    ("batch2_ragged", dict(B=2, S=100, H=256, num_heads=2, num_kv_heads=2, head_dim=128)),
+    ("cross_q", dict(S=300, H=512, num_heads=6, num_kv_heads=0, head_dim=128, rope=None)),
+    ("cross_v", dict(S=77, H=256, num_heads=2, num_kv_heads=0, head_dim=128, rope=None, q_norm=False)),
+    ("d16_one_row", dict(S=1, H=128, num_heads=1, num_kv_heads=1, head_dim=16)),
+]
+
+
+@pytest.mark.parametrize("name,kw", NBSD, ids=[s[0] for s in NBSD])
+@pytest.mark.parametrize("split", [False, True], ids=["fused", "split"])
+def test_nbsd_layout(name, kw, split):
+    """output_layout NBSd: out [I/d, B, S, d].  The result, read back into [T, I]
+    order, passes parity and equals the BSD run bit for bit (same arithmetic); the
+    read-back is checked to invert the oracle's NBSd layout map."""
+    case = synth.make_qkv(name, 300 + len(name), **kw)
+    T, I, d = case.T, case.I, case.head_dim
+    r = run_full(case, split=split, layout=native.RA_LAYOUT_NBSD)
+    g = r.out.view(torch.int16).cpu().numpy()               # [n, T, d] bf16 bits
+    back = g.transpose(1, 0, 2).reshape(T, I)                 # -> [T, I]
+    assert np.array_equal(oracle.qkv_cte.to_nbsd(back, case.B, case.S, d).reshape(g.shape), g)
+    bsd = run_full(case, split=split)
+    assert np.array_equal(back, bsd.out.view(torch.int16).cpu().numpy()), "NBSd != BSD"
+    check_qkv(case, as_f64(torch.from_numpy(back).view(torch.bfloat16)), qkv_reference(case), name)
 
 
 def test_split_entry_points_match_fused():
