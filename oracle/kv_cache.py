@@ -24,6 +24,24 @@ For kv [B, N, S, Dkv] (and v_optional [B, N, S, Dv] in the separate-kv mode):
     offset p % block_size.
 (5) When is_output_kv: k_rope = rope_out and c_kv = y (V1) or v (V2).
 
+Cache modes (cache/index constraint table):
+  * Norm: caches [B, N, Scache, D]; index [B, S] holds each token's offset in its
+    batch's cache, -1 = skip; values may repeat across batches.
+  * PA / PA_BNSD: token index as above.
+  * PA_BLK_BNSD: caches as PA_BNSD; index [B * ceil(S / block_size)] holds the
+    start slot of each block of block_size tokens (-1 = skip the block); token s
+    of batch b goes to slot index[b, s // block_size] + s % block_size.
+  Out-of-range slots are neither written nor trapped; they are counted.
+Outputs (5) exist in every PA mode; in Norm mode only for V2 with quantisation
+(the "Norm" row of the input-combination table); V1 in Norm mode takes no
+quantisation parameters.
+cos/sin may be [B, N, 1, R], broadcast over S (the "S-axis broadcast" of the
+input-combination table).  Inputs are bf16 or fp16 (the parameter table); a
+non-quantised cache has the input's dtype.  A quantised cache is int8 (formula
+(3)) or FP8 E4M3 / E5M2: for FP8 the reading is the same x * scale + offset,
+rounded to the nearest FP8 value (ties to even) and saturated at the largest
+finite value, in place of round().clamp(-128, 127).
+
 Quant scales/offsets are per channel: shape [D] for V1, [N, D] for V2.
 Values are computed in float64; bf16 caches receive the unrounded value (the
 comparison applies the bf16 tolerance), int8 caches receive the int code, and
@@ -33,7 +51,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .codes import decode_bf16
+from .codes import decode_bf16, decode_fp16, encode_fp8
 
 
 def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
@@ -50,8 +68,9 @@ def interleave_rope(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarr
     return part1 * cos + part2 * sin
 
 
-def quantize(x: np.ndarray, scale, offset, n_axis_param: bool):
-    """Returns (value, pre_round).  ``value`` is int64 codes when a scale is given."""
+def quantize(x: np.ndarray, scale, offset, n_axis_param: bool, qtype: str = "int8"):
+    """Returns (value, pre_round).  ``value`` is int64 codes when a scale is given
+    (int8 values, or the FP8 code bytes for qtype "e4m3" / "e5m2")."""
     if scale is None:
         return x, None
     sc = np.asarray(scale, dtype=np.float64)
@@ -63,24 +82,56 @@ def quantize(x: np.ndarray, scale, offset, n_axis_param: bool):
         if n_axis_param:
             of = of[None, :, None, :]
         v = v + of
-    return np.clip(np.rint(v), -128, 127).astype(np.int64), v
+    if qtype == "int8":
+        return np.clip(np.rint(v), -128, 127).astype(np.int64), v
+    return encode_fp8(v, qtype).astype(np.int64), v
+
+
+def token_slots(index, cache_mode: str, b: np.ndarray, s: np.ndarray, S: int, block_size: int) -> np.ndarray:
+    """Slot of each token (b, s) from ``index``, per the cache/index constraint
+    table: the token's own entry (Norm: an offset in batch b's cache; PA modes: a
+    slot of the paged cache), or for PA_BLK_BNSD its block's start slot plus its
+    position in the block.  -1 = skip; -2 marks an illegal negative block start."""
+    idx = np.asarray(index, dtype=np.int64).reshape(-1)
+    if cache_mode in ("Norm", "PA", "PA_BNSD"):
+        return idx[b * S + s]
+    if cache_mode == "PA_BLK_BNSD":
+        nb = -(-S // block_size)
+        first = idx[b * nb + s // block_size]
+        return np.where(first == -1, -1, np.where(first < -1, -2, first + s % block_size))
+    raise ValueError(cache_mode)
+
+
+def cache_rows(cache_mode: str, b: np.ndarray, p: np.ndarray, block_size: int):
+    """Index of the (all-heads) cache rows of token slots p: Norm [B, N, Scache, D]
+    at (b, :, p); PA_BNSD / PA_BLK_BNSD [block_num, N, block_size, D] at
+    (p // block_size, :, p % block_size); PA [block_num, block_size, N, D] at
+    (p // block_size, p % block_size)."""
+    if cache_mode == "Norm":
+        return (b, slice(None), p)
+    if cache_mode in ("PA_BNSD", "PA_BLK_BNSD"):
+        return (p // block_size, slice(None), p % block_size)
+    return (p // block_size, p % block_size)
 
 
 def kv_rms_norm_rope_cache(kv, gamma, cos, sin, index, k_cache, ckv_cache, *, variant: int,
                            rope_size: int, block_size: int, cache_mode: str = "PA_BNSD",
                            epsilon: float = 1e-5, k_scale=None, k_offset=None, v_scale=None,
-                           v_offset=None, v=None, is_output_kv: bool = False) -> dict:
+                           v_offset=None, v=None, is_output_kv: bool = False, dtype: str = "bf16",
+                           k_qtype: str = "int8", v_qtype: str = "int8") -> dict:
     """Run the operator on host arrays.
 
-    kv, gamma, cos, sin, v: bf16 bit patterns (uint16).  index: int64 [B*S].
-    k_cache / ckv_cache: the caches before the call (uint16 bf16 bits, or int8).
+    kv, gamma, cos, sin, v: bf16 or fp16 bit patterns (uint16), ``dtype``.  index:
+    int64 (shape per cache mode, see the module docstring).  k_cache / ckv_cache: the
+    caches before the call (uint16 bit patterns, int8 values, or uint8 FP8 codes).
     Returns a dict with float64 ``k_cache`` / ``ckv_cache`` (int64 codes for
-    int8 caches; untouched slots decoded from the input), the pre-rounding
+    quantised caches; untouched slots decoded from the input), the pre-rounding
     values ``k_pre`` / ``ckv_pre`` (NaN where nothing was written), the boolean
     ``k_written`` / ``ckv_written`` slot masks, ``k_rope`` / ``c_kv`` (float64,
-    when is_output_kv) and ``bad_index`` (count of out-of-range slots).
+    when they are output) and ``bad_index`` (count of out-of-range slots).
     """
-    x_all = decode_bf16(kv)
+    dec = {"bf16": decode_bf16, "fp16": decode_fp16}[dtype]
+    x_all = dec(kv)
     B, N, S, Dkv = x_all.shape
     R = rope_size
     if variant == 1:
@@ -89,52 +140,50 @@ def kv_rms_norm_rope_cache(kv, gamma, cos, sin, index, k_cache, ckv_cache, *, va
         rms_size = Dkv
     else:
         raise ValueError("variant must be 1 or 2")
+    quant = k_scale is not None or v_scale is not None
+    if cache_mode == "Norm" and variant == 1 and quant:
+        raise ValueError("V1 in Norm mode takes no quantisation parameters")
 
     # (1) RmsNorm
     x = x_all[..., :rms_size]
-    y = rms_norm(x, decode_bf16(gamma), epsilon)
+    y = rms_norm(x, dec(gamma), epsilon)
 
-    # (2) interleaved RoPE
+    # (2) interleaved RoPE (cos/sin [B, N, S or 1, R] broadcast over S)
     xr = x_all[..., rms_size:] if variant == 1 else y[..., :R]
-    y_rope = interleave_rope(xr, decode_bf16(cos), decode_bf16(sin))
+    y_rope = interleave_rope(xr, dec(cos), dec(sin))
     rope_out = y_rope if variant == 1 else np.concatenate([y_rope, y[..., R:]], axis=-1)
-    v_src = y if variant == 1 else decode_bf16(v)
+    v_src = y if variant == 1 else dec(v)
 
     # (3) Quant
     per_head = variant == 2
-    k_val, k_pre = quantize(rope_out, k_scale, k_offset, per_head)
-    c_val, c_pre = quantize(v_src, v_scale, v_offset, per_head)
+    k_val, k_pre = quantize(rope_out, k_scale, k_offset, per_head, k_qtype)
+    c_val, c_pre = quantize(v_src, v_scale, v_offset, per_head, v_qtype)
 
-    # (4) Scatter
-    def start(cache, quant):
-        if quant:
+    # (4) Scatter: for every token (b, s) the cache row of head n, or none
+    def start(cache, q):
+        if q:
             return np.asarray(cache).astype(np.int64), np.full(cache.shape, np.nan)
-        return decode_bf16(cache), None
+        return dec(cache), None
 
     k_out, k_pre_out = start(k_cache, k_scale is not None)
     c_out, c_pre_out = start(ckv_cache, v_scale is not None)
     k_written = np.zeros(k_out.shape, dtype=bool)
     c_written = np.zeros(c_out.shape, dtype=bool)
-    slots = k_out.shape[0] * block_size
-    idx = np.asarray(index, dtype=np.int64)
-    tok = np.nonzero((idx >= 0) & (idx < slots))[0]
-    bad = int(np.count_nonzero((idx != -1) & ((idx < -1) | (idx >= slots))))
-    b, s = tok // S, tok % S
-    blk, off = idx[tok] // block_size, idx[tok] % block_size
+    limit = k_out.shape[2] if cache_mode == "Norm" else k_out.shape[0] * block_size
+    bb, ss = np.meshgrid(np.arange(B), np.arange(S), indexing="ij")
+    bb, ss = bb.reshape(-1), ss.reshape(-1)  # token t = b * S + s
+    p = token_slots(index, cache_mode, bb, ss, S, block_size)
+    ok = (p >= 0) & (p < limit)
+    bad = int(np.count_nonzero((p != -1) & ~ok))
+    tok = np.nonzero(ok)[0]
+    b, s_, pt = bb[tok], ss[tok], p[tok]
+    at = cache_rows(cache_mode, b, pt, block_size)
 
     def put(dst, src, mask, pre_dst, pre_src):
-        if cache_mode == "PA_BNSD":      # [block_num, N, block_size, D]
-            dst[blk, :, off, :] = src[b, :, s, :]
-            mask[blk, :, off, :] = True
-            if pre_dst is not None:
-                pre_dst[blk, :, off, :] = pre_src[b, :, s, :]
-        elif cache_mode == "PA":         # [block_num, block_size, N, D]
-            dst[blk, off, :, :] = src[b, :, s, :]
-            mask[blk, off, :, :] = True
-            if pre_dst is not None:
-                pre_dst[blk, off, :, :] = pre_src[b, :, s, :]
-        else:
-            raise ValueError(cache_mode)
+        dst[at] = src[b, :, s_]
+        mask[at] = True
+        if pre_dst is not None:
+            pre_dst[at] = pre_src[b, :, s_]
 
     put(k_out, k_val, k_written, k_pre_out, k_pre)
     put(c_out, c_val, c_written, c_pre_out, c_pre)
@@ -142,7 +191,7 @@ def kv_rms_norm_rope_cache(kv, gamma, cos, sin, index, k_cache, ckv_cache, *, va
     res = {"k_cache": k_out, "ckv_cache": c_out, "k_pre": k_pre_out, "ckv_pre": c_pre_out,
            "k_written": k_written, "ckv_written": c_written, "bad_index": bad}
     # (5) optional outputs
-    if is_output_kv:
+    if is_output_kv and (cache_mode != "Norm" or (variant == 2 and quant)):
         res["k_rope"] = rope_out
         res["c_kv"] = v_src
     return res

@@ -55,6 +55,11 @@ def encode_e4m3(x: np.ndarray) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
 
 
+def encode_fp16(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+
+
 def encode_bf16(x: np.ndarray) -> np.ndarray:
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
@@ -303,6 +308,14 @@ class KVCase:
     v: np.ndarray | None     # [B,N,S,Dv] uint16 (V2)
     eps: float
     is_output_kv: bool
+    dtype: str = "bf16"       # kv / gamma / cos / sin / v (and non-quantised caches): bf16 or fp16
+    k_qtype: str = "int8"     # quantised k cache: int8, e4m3 or e5m2
+    v_qtype: str = "int8"
+    cache_seq: int = 0        # Norm mode: Scache
+
+    @property
+    def rope_broadcast(self) -> bool:
+        return self.cos.shape[2] == 1 and self.S > 1
 
     @property
     def rms_size(self) -> int:
@@ -321,11 +334,17 @@ class KVCase:
         b = self.kv.nbytes + self.cos.nbytes + self.sin.nbytes + self.index.nbytes + self.gamma.nbytes
         if self.v is not None:
             b += self.v.nbytes
-        valid = int(np.count_nonzero(self.index >= 0)) * self.N
+        if self.cache_mode == "PA_BLK_BNSD":
+            starts = self.index.reshape(self.B, -1)
+            s_blk = np.arange(self.S) // self.block_size
+            valid = int(np.count_nonzero(starts[:, s_blk] >= 0)) * self.N
+        else:
+            valid = int(np.count_nonzero(self.index >= 0)) * self.N
         kb = 1 if self.k_scale is not None else 2
         cb = 1 if self.v_scale is not None else 2
         b += valid * (self.k_width * kb + self.ckv_width * cb)
-        if self.is_output_kv:
+        quant = self.k_scale is not None or self.v_scale is not None
+        if self.is_output_kv and (self.cache_mode != "Norm" or (self.variant == 2 and quant)):
             b += rows * (self.k_width + self.ckv_width) * 2
         for p in (self.k_scale, self.k_offset, self.v_scale, self.v_offset):
             if p is not None:
@@ -334,57 +353,89 @@ class KVCase:
 
 
 K_SENTINEL_BF16 = 0x7FBF  # a bf16 NaN pattern the op never writes
+K_SENTINEL_FP16 = 0x7FBF  # an fp16 NaN pattern the op never writes
 K_SENTINEL_I8 = -77
+K_SENTINEL_FP8 = 0x7F     # NaN in both E4M3 and E5M2
 
 
 def make_kv(name: str, seed: int, *, variant: int, B: int, N: int, S: int, Dkv: int, Dv: int,
             rope_size: int = 64, block_size: int = 128, block_num: int | None = None,
             cache_mode: str = "PA_BNSD", quant_k: bool = False, quant_v: bool = False,
             offsets: bool = True, with_v: bool | None = None, eps: float = 1e-5,
-            is_output_kv: bool = True, skip_frac: float = 0.0) -> KVCase:
+            is_output_kv: bool = True, skip_frac: float = 0.0, dtype: str = "bf16",
+            k_qtype: str = "int8", v_qtype: str = "int8", rope_broadcast: bool = False,
+            cache_seq: int | None = None) -> KVCase:
     """Synthetic KvRmsNormRopeCache call.
 
-    kv, v ~ N(0,1) in bf16; gamma ~ U(0.5,1.5) bf16; cos/sin from position s with
-    ladder theta=1e4 (same values for every b and n); index = the first B*S entries
-    of a random permutation of block_num*block_size slots, with a fraction
-    ``skip_frac`` replaced by -1; quant scales ~ U(10,40), offsets ~ U(-2,2).
+    kv, v ~ N(0,1); gamma ~ U(0.5,1.5); cos/sin from position s with ladder
+    theta=1e4 (same values for every b and n; with ``rope_broadcast`` one row
+    [B, N, 1, R] at position S-1, broadcast over S); all of them in ``dtype``
+    (bf16 or fp16).  index, per ``cache_mode``:
+      PA / PA_BNSD: the first B*S entries of a random permutation of the
+        block_num*block_size slots;
+      Norm: per batch, the first S entries of a random permutation of the
+        cache_seq (Scache) offsets, shape [B, S];
+      PA_BLK_BNSD: per block of block_size tokens, the start slot of a distinct
+        random cache block (block id * block_size), shape [B * ceil(S / block_size)];
+    a fraction ``skip_frac`` of the entries replaced by -1.  Quant scales
+    ~ U(10,40), offsets ~ U(-2,2); a quantised cache is int8 or FP8 (``k_qtype``,
+    ``v_qtype``).  Caches start filled with a sentinel the op never writes.
     """
+    enc = {"bf16": encode_bf16, "fp16": encode_fp16}[dtype]
     rms = Dkv - rope_size if variant == 1 else Dkv
     kw = rope_size if variant == 1 else Dkv
     cw = rms if variant == 1 else Dv
+    nb = -(-S // block_size)
     if block_num is None:
-        block_num = -(-B * S // block_size)
-    kv = encode_bf16(stream(seed, 0).standard_normal((B, N, S, Dkv), dtype=np.float32))
-    gamma = encode_bf16(stream(seed, 1).uniform(0.5, 1.5, rms).astype(np.float32))
+        block_num = B * nb if cache_mode == "PA_BLK_BNSD" else -(-B * S // block_size)
+    if cache_mode == "Norm" and cache_seq is None:
+        cache_seq = S
+    kv = enc(stream(seed, 0).standard_normal((B, N, S, Dkv), dtype=np.float32))
+    gamma = enc(stream(seed, 1).uniform(0.5, 1.5, rms).astype(np.float32))
     c, s = rope_interleaved_table(S, rope_size)
-    cos = np.broadcast_to(encode_bf16(c.astype(np.float32)), (B, N, S, rope_size)).copy()
-    sin = np.broadcast_to(encode_bf16(s.astype(np.float32)), (B, N, S, rope_size)).copy()
-    perm = stream(seed, 2).permutation(block_num * block_size)[: B * S].astype(np.int64)
+    rows = slice(S - 1, S) if rope_broadcast else slice(0, S)
+    srope = 1 if rope_broadcast else S
+    cos = np.broadcast_to(enc(c[rows].astype(np.float32)), (B, N, srope, rope_size)).copy()
+    sin = np.broadcast_to(enc(s[rows].astype(np.float32)), (B, N, srope, rope_size)).copy()
+    g2 = stream(seed, 2)
+    if cache_mode in ("PA", "PA_BNSD"):
+        index = g2.permutation(block_num * block_size)[: B * S].astype(np.int64)
+    elif cache_mode == "Norm":
+        index = np.stack([g2.permutation(cache_seq)[:S] for _ in range(B)]).astype(np.int64)
+    elif cache_mode == "PA_BLK_BNSD":
+        index = (g2.permutation(block_num)[: B * nb] * block_size).astype(np.int64)
+    else:
+        raise ValueError(cache_mode)
     if skip_frac > 0:
-        drop = stream(seed, 3).random(B * S) < skip_frac
-        perm[drop] = -1
+        drop = stream(seed, 3).random(index.shape) < skip_frac
+        index[drop] = -1
     v = None
     if with_v if with_v is not None else (variant == 2):
-        v = encode_bf16(stream(seed, 4).standard_normal((B, N, S, Dv), dtype=np.float32))
+        v = enc(stream(seed, 4).standard_normal((B, N, S, Dv), dtype=np.float32))
     qshape_k = (kw,) if variant == 1 else (N, kw)
     qshape_v = (cw,) if variant == 1 else (N, cw)
     ks = stream(seed, 5).uniform(10, 40, qshape_k).astype(np.float32) if quant_k else None
     ko = stream(seed, 6).uniform(-2, 2, qshape_k).astype(np.float32) if (quant_k and offsets) else None
     vs = stream(seed, 7).uniform(10, 40, qshape_v).astype(np.float32) if quant_v else None
     vo = stream(seed, 8).uniform(-2, 2, qshape_v).astype(np.float32) if (quant_v and offsets) else None
-    if cache_mode == "PA_BNSD":
+    if cache_mode in ("PA_BNSD", "PA_BLK_BNSD"):
         kshape, cshape = (block_num, N, block_size, kw), (block_num, N, block_size, cw)
     elif cache_mode == "PA":
         kshape, cshape = (block_num, block_size, N, kw), (block_num, block_size, N, cw)
-    else:
-        raise ValueError(cache_mode)
-    k_cache = (np.full(kshape, K_SENTINEL_I8, np.int8) if quant_k
-               else np.full(kshape, K_SENTINEL_BF16, np.uint16))
-    ckv_cache = (np.full(cshape, K_SENTINEL_I8, np.int8) if quant_v
-                 else np.full(cshape, K_SENTINEL_BF16, np.uint16))
-    return KVCase(name, variant, B, N, S, Dkv, Dv, rope_size, kv, gamma, cos, sin, perm,
-                  cache_mode, block_num, block_size, k_cache, ckv_cache, ks, ko, vs, vo, v,
-                  eps, is_output_kv)
+    else:  # Norm
+        kshape, cshape = (B, N, cache_seq, kw), (B, N, cache_seq, cw)
+
+    def cache(shape, quant, qtype):
+        if not quant:
+            return np.full(shape, K_SENTINEL_BF16 if dtype == "bf16" else K_SENTINEL_FP16, np.uint16)
+        if qtype == "int8":
+            return np.full(shape, K_SENTINEL_I8, np.int8)
+        return np.full(shape, K_SENTINEL_FP8, np.uint8)
+
+    return KVCase(name, variant, B, N, S, Dkv, Dv, rope_size, kv, gamma, cos, sin, index,
+                  cache_mode, block_num, block_size, cache(kshape, quant_k, k_qtype),
+                  cache(cshape, quant_v, v_qtype), ks, ko, vs, vo, v, eps, is_output_kv,
+                  dtype, k_qtype, v_qtype, cache_seq or 0)
 
 
 def kv_mla_v1(seed: int = 3, quant: bool = False) -> KVCase:

@@ -11,6 +11,7 @@ The ``check_*`` helpers raise AssertionError on a mismatch; ``test_mutants``
 plants plausible mistakes in the oracle (sign flips, transposed operands,
 wrong widths, dropped terms) and confirms that some check catches each one.
 """
+import dataclasses
 import os
 
 import numpy as np
@@ -31,6 +32,10 @@ def torch_e4m3(a):
 
 def torch_bf16(b):
     return torch.from_numpy(np.ascontiguousarray(b, np.uint16).view(np.int16)).view(torch.bfloat16).to(F64).numpy()
+
+
+def torch_fp16(b):
+    return torch.from_numpy(np.ascontiguousarray(b, np.uint16).view(np.int16)).view(torch.float16).to(F64).numpy()
 
 
 def finite_e4m3_codes(rng, shape):
@@ -314,18 +319,20 @@ def run_kv(case):
         case.kv, case.gamma, case.cos, case.sin, case.index, case.k_cache, case.ckv_cache,
         variant=case.variant, rope_size=case.rope_size, block_size=case.block_size,
         cache_mode=case.cache_mode, epsilon=case.eps, k_scale=case.k_scale, k_offset=case.k_offset,
-        v_scale=case.v_scale, v_offset=case.v_offset, v=case.v, is_output_kv=True)
+        v_scale=case.v_scale, v_offset=case.v_offset, v=case.v, is_output_kv=True,
+        dtype=case.dtype, k_qtype=case.k_qtype, v_qtype=case.v_qtype)
 
 
 def expected_kv_rows(case):
     """Per (b, n, s) rows built from library routines: F.rms_norm, complex rotation, torch.round."""
-    x = torch_bf16(case.kv)
+    dec = torch_bf16 if case.dtype == "bf16" else torch_fp16
+    x = dec(case.kv)
     B, N, S, Dkv = x.shape
     R = case.rope_size
     rms = case.rms_size
-    g = torch.from_numpy(torch_bf16(case.gamma))
+    g = torch.from_numpy(dec(case.gamma))
     y = F.rms_norm(torch.from_numpy(x[..., :rms].copy()), (rms,), g, case.eps).numpy()
-    cos, sin = torch_bf16(case.cos), torch_bf16(case.sin)
+    cos, sin = dec(case.cos), dec(case.sin)
     theta = np.arctan2(sin[..., : R // 2], cos[..., : R // 2])
     radius = np.hypot(sin[..., : R // 2], cos[..., : R // 2])  # bf16 tables are not exactly unit
     def rot(v):
@@ -334,7 +341,7 @@ def expected_kv_rows(case):
     if case.variant == 1:
         k_rows, c_rows = rot(x[..., rms:]), y
     else:
-        k_rows, c_rows = np.concatenate([rot(y[..., :R]), y[..., R:]], axis=-1), torch_bf16(case.v)
+        k_rows, c_rows = np.concatenate([rot(y[..., :R]), y[..., R:]], axis=-1), dec(case.v)
 
     def q(v, sc, of):
         if sc is None:
@@ -552,6 +559,175 @@ def test_nbsd_layout():
 
 
 # ---------------------------------------------------------------------------
+# KvRmsNormRopeCache variants: Norm and PA_BLK_BNSD cache modes, S-broadcast
+# cos/sin, fp16 inputs, FP8 caches
+# ---------------------------------------------------------------------------
+TORCH_FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+
+
+def torch_fp8_code(v, fmt):
+    return torch.from_numpy(np.ascontiguousarray(v, np.float64)).to(TORCH_FP8[fmt]).view(torch.uint8) \
+        .numpy().astype(np.int64)
+
+
+def check_fp8_encoders_vs_torch():
+    """encode_fp8 agrees with torch's float8 casts (round-half-even) on every finite
+    value, every midpoint between neighbours and random values, and saturates."""
+    rng = np.random.default_rng(21)
+    for fmt, top in (("e4m3", 0x7F), ("e5m2", 0x7C)):
+        dec = codes.decode_e4m3 if fmt == "e4m3" else codes.decode_e5m2
+        mags = dec(np.arange(top, dtype=np.uint8))
+        mids = (mags[:-1] + mags[1:]) / 2
+        vals = np.concatenate([mags, mids, rng.uniform(-FP8_MAX[fmt], FP8_MAX[fmt], 20000),
+                               rng.normal(0, 0.05, 5000)])
+        vals = np.concatenate([vals, -vals])
+        assert np.array_equal(codes.encode_fp8(vals, fmt).astype(np.int64), torch_fp8_code(vals, fmt)), fmt
+        big = np.array([FP8_MAX[fmt] * 1.01, FP8_MAX[fmt] * 1.2, 1e9])
+        assert np.all(codes.encode_fp8(big, fmt) == top - 1) and np.all(codes.encode_fp8(-big, fmt) == 0x80 | (top - 1))
+
+
+def brute_scatter(case, k_rows, c_rows):
+    """Per-token loops over the cache/index constraint table: the expected caches
+    (float64 values or codes) and the number of written (token, head) rows."""
+    dec = codes.decode_bf16 if case.dtype == "bf16" else codes.decode_fp16
+    k_exp = dec(case.k_cache) if case.k_scale is None else case.k_cache.astype(np.float64)
+    c_exp = dec(case.ckv_cache) if case.v_scale is None else case.ckv_cache.astype(np.float64)
+    k_exp, c_exp = k_exp.copy(), c_exp.copy()
+    B, N, S, bs = case.B, case.N, case.S, case.block_size
+    nb = -(-S // bs)
+    written = 0
+    for b in range(B):
+        for s_ in range(S):
+            if case.cache_mode == "Norm":
+                p = int(case.index[b, s_])
+                if not 0 <= p < case.cache_seq:
+                    continue
+                at = [(b, n, p) for n in range(N)]
+            else:
+                if case.cache_mode == "PA_BLK_BNSD":
+                    first = int(case.index[b * nb + s_ // bs])
+                    if first < 0:
+                        continue
+                    p = first + s_ % bs
+                else:
+                    p = int(case.index[b * S + s_])
+                if not 0 <= p < case.block_num * bs:
+                    continue
+                blk, off = divmod(p, bs)
+                at = [(blk, off, n) if case.cache_mode == "PA" else (blk, n, off) for n in range(N)]
+            for n, a in enumerate(at):
+                k_exp[a], c_exp[a] = k_rows[b, n, s_], c_rows[b, n, s_]
+                written += 1
+    return k_exp, c_exp, written
+
+
+def quant_rows(case, rows, scale, offset, qtype):
+    if scale is None:
+        return rows
+    sc = scale if case.variant == 1 else scale[None, :, None, :]
+    pre = torch.from_numpy(rows) * torch.from_numpy(np.asarray(sc, np.float64))
+    if offset is not None:
+        of = offset if case.variant == 1 else offset[None, :, None, :]
+        pre = pre + torch.from_numpy(np.asarray(of, np.float64))
+    if qtype == "int8":
+        return torch.round(pre).clamp(-128, 127).numpy()
+    m = FP8_MAX[qtype]
+    return torch_fp8_code(pre.clamp(-m, m).numpy(), qtype).astype(np.float64)
+
+
+def check_kv_mode(case, expect_outputs=True):
+    res = run_kv(case)
+    k_rows, c_rows, *_ = expected_kv_rows(case)
+    kq = quant_rows(case, k_rows, case.k_scale, case.k_offset, case.k_qtype)
+    cq = quant_rows(case, c_rows, case.v_scale, case.v_offset, case.v_qtype)
+    k_exp, c_exp, written = brute_scatter(case, kq, cq)
+    assert_close(res["k_cache"], k_exp, 1e-12, 1e-12)
+    assert_close(res["ckv_cache"], c_exp, 1e-12, 1e-12)
+    assert res["k_written"].sum() == written * case.k_width
+    assert ("k_rope" in res) == expect_outputs
+    return res
+
+
+def check_kv_norm_mode():
+    """Norm mode: caches [B, N, Scache, D], index [B, S] of per-batch offsets (values
+    repeat across batches); V2 with int8 quantisation writes k_rope / c_kv."""
+    case = synth.make_kv("norm", 31, variant=2, B=2, N=2, S=5, Dkv=24, Dv=16, rope_size=8,
+                         cache_mode="Norm", cache_seq=7, quant_k=True, quant_v=True, skip_frac=0.2)
+    case.index[1, :] = case.index[0, :]  # the same offsets in another batch are legal
+    case.index[0, 2] = 7                 # out of range: counted, not written
+    res = check_kv_mode(case)
+    assert res["bad_index"] == 1
+
+
+def check_kv_norm_v1_no_outputs():
+    """Norm mode, V1, no quantisation: the caches are written, k_rope / c_kv are not."""
+    case = synth.make_kv("norm1", 32, variant=1, B=2, N=1, S=5, Dkv=24, Dv=16, rope_size=8,
+                         cache_mode="Norm", cache_seq=6, skip_frac=0.2)
+    check_kv_mode(case, expect_outputs=False)
+
+
+def check_kv_blk_mode():
+    """PA_BLK_BNSD: one start slot per block of block_size tokens; a skipped block
+    skips all its tokens; the last block of a batch may be partial."""
+    case = synth.make_kv("blk", 33, variant=2, B=2, N=2, S=10, Dkv=24, Dv=16, rope_size=8,
+                         block_size=4, block_num=8, cache_mode="PA_BLK_BNSD")
+    case.index[1] = -1
+    check_kv_mode(case)
+
+
+def check_kv_rope_broadcast():
+    """cos/sin [B, N, 1, R] act as that row repeated along S."""
+    case = synth.make_kv("bc", 34, variant=2, B=2, N=2, S=5, Dkv=24, Dv=16, rope_size=8,
+                         block_size=4, block_num=4, rope_broadcast=True, quant_k=True)
+    assert case.cos.shape[2] == 1
+    res = run_kv(case)
+    rep = dataclasses.replace(case, cos=np.repeat(case.cos, case.S, axis=2), sin=np.repeat(case.sin, case.S, axis=2))
+    res2 = run_kv(rep)
+    for key in ("k_cache", "ckv_cache", "k_rope", "c_kv"):
+        assert np.array_equal(res[key], res2[key], equal_nan=True), key
+    check_kv_mode(case)
+
+
+def check_kv_fp16_inputs():
+    """fp16 inputs whose values bf16 also holds exactly give the same result as bf16."""
+    rng = np.random.default_rng(35)
+    base = synth.make_kv("f16", 35, variant=2, B=2, N=2, S=5, Dkv=24, Dv=16, rope_size=8,
+                         block_size=4, block_num=4)
+    def grid(shape, lo, hi):  # multiples of 1/16: exact in both formats
+        return (rng.integers(int(lo * 16), int(hi * 16) + 1, shape) / 16).astype(np.float32)
+    half = base.cos.shape[:-1] + (base.rope_size // 2,)
+    dup = lambda h: np.concatenate([h, h], axis=-1)  # cos[j] = cos[j + R/2], as the tables are built
+    vals = dict(kv=grid(base.kv.shape, -4, 4), gamma=grid(base.gamma.shape, 0.5, 1.5),
+                cos=dup(grid(half, -1, 1)), sin=dup(grid(half, -1, 1)), v=grid(base.v.shape, -4, 4))
+    b16 = dataclasses.replace(base, **{k: synth.encode_bf16(x) for k, x in vals.items()})
+    f16 = dataclasses.replace(base, dtype="fp16", k_cache=np.full(base.k_cache.shape, 0x7FBF, np.uint16),
+                              ckv_cache=np.full(base.ckv_cache.shape, 0x7FBF, np.uint16),
+                              **{k: synth.encode_fp16(x) for k, x in vals.items()})
+    r16, rb = run_kv(f16), run_kv(b16)
+    for key in ("k_rope", "c_kv"):
+        assert np.array_equal(r16[key], rb[key]), key
+    check_kv_mode(f16)
+
+
+def check_kv_fp8_caches():
+    """k cache E4M3, ckv cache E5M2: the codes are torch's float8 casts of the
+    saturated x * scale + offset."""
+    case = synth.make_kv("fp8", 36, variant=2, B=2, N=2, S=5, Dkv=24, Dv=16, rope_size=8,
+                         block_size=4, block_num=4, quant_k=True, quant_v=True, k_qtype="e4m3",
+                         v_qtype="e5m2", skip_frac=0.2)
+    case.k_scale *= 20.0  # reach the E4M3 saturation point on some channels
+    check_kv_mode(case)
+
+
+@pytest.mark.parametrize("check", [check_fp8_encoders_vs_torch, check_kv_norm_mode, check_kv_norm_v1_no_outputs,
+                                   check_kv_blk_mode, check_kv_rope_broadcast, check_kv_fp16_inputs,
+                                   check_kv_fp8_caches])
+def test_kv_variants(check):
+    check()
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: every mutant must be caught by at least one check
 # ---------------------------------------------------------------------------
 ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_block_scales,
@@ -561,7 +737,9 @@ ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_blo
               check_kv_v1_bf16, check_kv_v1_int8, check_kv_v2_int8, check_kv_v2_pa_bf16,
               check_kv_bad_index, check_e4m3_encoder_vs_torch, check_e4m3_encoder_saturates,
               check_row_quant_hand, check_row_quant_zero_row, check_row_quant_roundtrip,
-              check_row_quant_packed, check_nbsd_layout]
+              check_row_quant_packed, check_nbsd_layout, check_fp8_encoders_vs_torch,
+              check_kv_norm_mode, check_kv_norm_v1_no_outputs, check_kv_blk_mode,
+              check_kv_rope_broadcast, check_kv_fp16_inputs, check_kv_fp8_caches]
 
 
 def mutants():
@@ -595,14 +773,14 @@ def mutants():
         out[..., 0::2], out[..., 1::2] = r[..., :h], r[..., h:]
         return out
 
-    def q_half_away(x, sc, of, nax):        # rounding half away from zero
-        v, pre = orig_q(x, sc, of, nax)
+    def q_half_away(x, sc, of, nax, qtype="int8"):   # rounding half away from zero
+        v, pre = orig_q(x, sc, of, nax, qtype)
         if pre is None:
             return v, pre
         return np.clip(np.sign(pre) * np.floor(np.abs(pre) + 0.5), -128, 127).astype(np.int64), pre
 
-    def q_offset_after_round(x, sc, of, nax):
-        v, pre = orig_q(x, sc, None, nax)
+    def q_offset_after_round(x, sc, of, nax, qtype="int8"):
+        v, pre = orig_q(x, sc, None, nax, qtype)
         if pre is None or of is None:
             return v, pre
         o = np.asarray(of, np.float64)
@@ -640,7 +818,27 @@ def mutants():
         safe = np.maximum(np.max(np.abs(x), axis=1), np.float32(2.0 ** -100)).astype(np.float32)
         return orig_enc(x * (np.float32(240) / safe)[:, None]), (safe / np.float32(240)).astype(np.float32)
 
-    return [(orq, "encode_e4m3_rne_sat", enc_half_away), (orq, "encode_e4m3_rne_sat", enc_no_saturation),
+    orig_slots = okv.token_slots
+    orig_rows = okv.cache_rows
+    orig_fp8 = codes.encode_fp8
+
+    def slots_blk_per_token(index, mode, b, s, S, bs):   # PA_BLK_BNSD index read per token
+        if mode == "PA_BLK_BNSD":
+            idx = np.asarray(index, np.int64).reshape(-1)
+            return idx[np.minimum(b * S + s, idx.size - 1)]
+        return orig_slots(index, mode, b, s, S, bs)
+
+    def rows_norm_ignores_batch(mode, b, p, bs):          # Norm: every batch into batch 0's cache
+        return orig_rows(mode, np.zeros_like(b) if mode == "Norm" else b, p, bs)
+
+    def fp8_no_saturation(v, fmt):                       # out-of-range magnitudes become NaN codes
+        c = orig_fp8(v, fmt)
+        top = 448.0 if fmt == "e4m3" else 57344.0
+        return np.where(np.abs(np.asarray(v, np.float64)) > top, (c & 0x80) | 0x7F, c).astype(np.uint8)
+
+    return [(okv, "token_slots", slots_blk_per_token), (okv, "cache_rows", rows_norm_ignores_batch),
+            (codes, "encode_fp8", fp8_no_saturation),
+            (orq, "encode_e4m3_rne_sat", enc_half_away), (orq, "encode_e4m3_rne_sat", enc_no_saturation),
             (orq, "row_quantize", rq_fnuz_range),
             (oq, "rope_rotate_half", rh_sign), (oq, "rms_norm_across_heads", norm_no_eps),
             (oq, "rms_norm_across_heads", norm_pre_gamma_width), (oq, "dequant_weight", dw_transposed_blocks),
@@ -653,8 +851,10 @@ def mutants():
 def test_mutants(i, monkeypatch):
     mod, name, fn = mutants()[i]
     monkeypatch.setattr(mod, name, fn)
-    if mod is codes:  # decode_e4m3 is also bound by name in qkv_cte
-        monkeypatch.setattr(oq, name, fn)
+    if mod is codes:  # the code helpers are also bound by name in the oracle modules
+        for m in (oq, okv):
+            if hasattr(m, name):
+                monkeypatch.setattr(m, name, fn)
     caught = []
     for check in ALL_CHECKS:
         try:
