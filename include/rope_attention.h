@@ -59,7 +59,11 @@ typedef enum {
   RA_ERR_INDEX = -7          /* reserved: index out of range reported by the host      */
 } ra_status;
 
-typedef enum { RA_BF16 = 0, RA_FP16 = 1, RA_INT8 = 2, RA_FP32 = 3 } ra_dtype;
+typedef enum {
+  RA_BF16 = 0, RA_FP16 = 1, RA_INT8 = 2, RA_FP32 = 3,
+  RA_FP8_E4M3 = 4,   /* OCP FP8 E4M3 (largest finite 448)                          */
+  RA_FP8_E5M2 = 5    /* OCP FP8 E5M2 (largest finite 57344)                        */
+} ra_dtype;
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* ra_last_error(void);
@@ -236,9 +240,17 @@ ra_status row_quantize_e4m3_packed(const uint16_t* x, int64_t T, int64_t H, uint
  * (b) kv_rms_norm_rope_cache
  * ======================================================================== */
 
-/* cache_mode, from the page's constraint table.  PA = [block_num, block_size, N, D];
- * PA_BNSD = [block_num, N, block_size, D]. */
-enum { RA_CACHE_PA = 1, RA_CACHE_PA_BNSD = 2 };
+/* cache_mode, from the page's cache/index constraint table:
+ *   NORM        caches [B, N, cache_seq_len, D]; index [B, S] holds each token's
+ *               offset in its batch's cache (values may repeat across batches).
+ *   PA          caches [block_num, block_size, N, D]; index [B*S], one slot per token.
+ *   PA_BNSD     caches [block_num, N, block_size, D]; index [B*S], one slot per token.
+ *   PA_BLK_BNSD caches as PA_BNSD; index [B * ceil(S / block_size)] holds the start
+ *               slot of each block of block_size tokens: token s of batch b goes to
+ *               index[b, s / block_size] + s % block_size (-1 skips the block).
+ *   PA_NZ, PA_BLK_NZ (FRACTAL_NZ layouts for Ascend's cube unit): RA_ERR_UNSUPPORTED. */
+enum { RA_CACHE_NORM = 0, RA_CACHE_PA = 1, RA_CACHE_PA_BNSD = 2, RA_CACHE_PA_NZ = 3,
+       RA_CACHE_PA_BLK_BNSD = 4, RA_CACHE_PA_BLK_NZ = 5 };
 
 typedef struct {
   int64_t B, N, S;        /* kv is [B, N, S, Dkv]                                     */
@@ -246,30 +258,43 @@ typedef struct {
   int64_t Dv;             /* V1: rms_size (= Dkv - rope_size); V2: last dim of v_optional */
   int32_t rope_size;      /* RoPE width (64 in both of the page's modes); even        */
   int32_t variant;        /* 1 = V1 combined kv (N == 1), 2 = V2 separate kv (N in 1,2,4,8) */
-  int32_t cache_mode;     /* RA_CACHE_PA or RA_CACHE_PA_BNSD                          */
-  int64_t block_num;      /* paged cache blocks                                       */
-  int64_t block_size;     /* slots per block; %16 (bf16 caches), %32 (int8 caches)    */
-  int32_t kv_dtype;       /* RA_BF16 (kv, gamma, cos, sin, v_optional share it)       */
-  int32_t k_cache_dtype;  /* RA_BF16, or RA_INT8 when k_rope_scale is given           */
-  int32_t ckv_cache_dtype;/* RA_BF16, or RA_INT8 when c_kv_scale is given             */
+  int32_t cache_mode;     /* RA_CACHE_*                                               */
+  int64_t block_num;      /* paged cache blocks (PA modes)                            */
+  int64_t block_size;     /* slots per block (PA modes); %16 for 2-byte caches, %32 for
+                           * 1-byte caches (both when the two caches differ)          */
+  int32_t kv_dtype;       /* RA_BF16 or RA_FP16 (kv, gamma, cos, sin, v_optional share it) */
+  int32_t k_cache_dtype;  /* = kv_dtype, or RA_INT8 / RA_FP8_E4M3 / RA_FP8_E5M2 when
+                           * k_rope_scale is given                                    */
+  int32_t ckv_cache_dtype;/* likewise with c_kv_scale                                  */
   float epsilon;          /* RMSNorm epsilon (page default 1e-5)                      */
-  int32_t is_output_kv;   /* 1 = also write k_rope and c_kv                           */
+  int32_t is_output_kv;   /* 1 = also write k_rope and c_kv (in NORM mode only for V2
+                           * with quantisation, per the page's combination table)    */
+  int32_t rope_s_broadcast;  /* 1 = cos/sin are [B, N, 1, rope_size], broadcast over S */
+  int64_t cache_seq_len;  /* NORM mode: Scache (>= S); ignored otherwise             */
 } kv_rms_norm_rope_cache_params;
 
 /* One call of KvRmsNormRopeCache.
- *   kv          [B, N, S, Dkv] bf16.
- *   gamma       [rms_size] bf16 (rms_size = Dkv - rope_size in V1, Dkv in V2).
- *   cos, sin    [B, N, S, rope_size] bf16 (interleaved-RoPE tables).
- *   index       [B*S] int64 slot per token; -1 = skip.  Slots must be unique.
+ *   kv          [B, N, S, Dkv] bf16 or fp16 (kv_dtype).
+ *   gamma       [rms_size] (rms_size = Dkv - rope_size in V1, Dkv in V2).
+ *   cos, sin    [B, N, S, rope_size], or [B, N, 1, rope_size] with rope_s_broadcast
+ *               (interleaved-RoPE tables).
+ *   index       int64, shaped by cache_mode (see RA_CACHE_*); -1 = skip.  Slots
+ *               (PA modes: block starts / block_size) must be unique.
  *   k_cache     paged cache of width k_w = rope_size (V1) or Dkv (V2), updated in place.
  *   ckv_cache   paged cache of width c_w = rms_size (V1) or Dv (V2), updated in place.
  *   k_rope_scale / k_rope_offset  fp32 per channel: [k_w] (V1) or [N, k_w] (V2); NULL = absent.
  *   c_kv_scale   / c_kv_offset    fp32 per channel: [c_w] (V1) or [N, c_w] (V2); NULL = absent.
  *               An offset without its scale is rejected.
  *   v_optional  [B, N, S, Dv] bf16; required in V2, must be NULL in V1.
- *   k_rope      [B, N, S, k_w] bf16 and c_kv [B, N, S, c_w] bf16: written iff is_output_kv.
+ *   k_rope      [B, N, S, k_w] and c_kv [B, N, S, c_w], kv_dtype: written iff outputs
+ *               are on (see is_output_kv).
+ *   Quantised caches hold round_half_even(x * scale + offset) clamped to [-128, 127]
+ *   (int8, formula (3)), or x * scale + offset rounded to the nearest FP8 value,
+ *   ties to even, saturated at the largest finite value (FP8 caches).
  *   dev_error_count  optional int32 device counter: incremented once per token whose
- *               index lies outside [-1, block_num*block_size); such tokens are not written.
+ *               slot lies outside the cache (any negative index other than -1, or
+ *               beyond block_num*block_size / cache_seq_len); such tokens are not written.
+ * V1 in NORM mode takes no quantisation parameters.
  * All row pointers 16-byte aligned; Dkv, Dv and rope_size multiples of 8. */
 ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const uint16_t* kv,
                                  const uint16_t* gamma, const uint16_t* cos, const uint16_t* sin,

@@ -8,6 +8,7 @@
 
 #include "rope_attention.h"
 #include "internal.h"
+#include "kv_cache.h"
 #include "row_quant.h"
 
 namespace ra {
@@ -232,7 +233,7 @@ extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 2; }
+int32_t ra_abi_version(void) { return 3; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
@@ -369,8 +370,8 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
     return fail(RA_ERR_INVALID_ARG, "kv, gamma, cos, sin, index, k_cache and ckv_cache are required");
   if (p->B < 1 || p->N < 1 || p->S < 1 || p->Dkv < 1)
     return fail(RA_ERR_INVALID_ARG, "empty tensors are not supported");
-  if (p->kv_dtype == RA_FP16) return fail(RA_ERR_UNSUPPORTED, "fp16 kv is not built; use bf16");
-  if (p->kv_dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "kv dtype must be bf16 or fp16");
+  if (p->kv_dtype != RA_BF16 && p->kv_dtype != RA_FP16)
+    return fail(RA_ERR_INVALID_ARG, "kv dtype must be bf16 or fp16");
   const int64_t R = p->rope_size;
   if (R < 8 || R % 8 != 0 || R > 256)
     return fail(RA_ERR_INVALID_ARG, "rope_size must be even; this build needs a multiple of 8 in [8, 256]");
@@ -396,25 +397,38 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
   if ((k_rope_offset && !k_rope_scale) || (c_kv_offset && !c_kv_scale))
     return fail(RA_ERR_INVALID_ARG, "an offset without its scale is illegal");
   const bool qk = k_rope_scale != nullptr, qv = c_kv_scale != nullptr;
-  if (qk ? p->k_cache_dtype != RA_INT8 : p->k_cache_dtype != p->kv_dtype)
-    return fail(qk && p->k_cache_dtype != RA_INT8 && p->k_cache_dtype != RA_BF16 ? RA_ERR_UNSUPPORTED
-                                                                                 : RA_ERR_INVALID_ARG,
-                "k_cache dtype must be int8 with a k scale, else equal to the kv dtype");
-  if (qv ? p->ckv_cache_dtype != RA_INT8 : p->ckv_cache_dtype != p->kv_dtype)
-    return fail(qv && p->ckv_cache_dtype != RA_INT8 && p->ckv_cache_dtype != RA_BF16 ? RA_ERR_UNSUPPORTED
-                                                                                     : RA_ERR_INVALID_ARG,
-                "ckv_cache dtype must be int8 with a c_kv scale, else equal to the kv dtype");
-  if (p->cache_mode != RA_CACHE_PA && p->cache_mode != RA_CACHE_PA_BNSD)
-    return fail(RA_ERR_UNSUPPORTED, "cache_mode must be PA or PA_BNSD in this build");
-  if (p->block_num < 1 || p->block_size <= 1)
-    return fail(RA_ERR_INVALID_ARG, "block_num >= 1 and block_size > 1 are required");
-  if ((qk || qv) && p->block_size % 32 != 0)
-    return fail(RA_ERR_INVALID_ARG, "int8 caches need block_size %% 32 == 0");
-  if ((!qk || !qv) && p->block_size % 16 != 0)
-    return fail(RA_ERR_INVALID_ARG, "bf16 caches need block_size %% 16 == 0");
+  auto quant_type = [](int32_t d) -> int32_t {
+    return d == RA_INT8 ? ra::kQuantInt8 : d == RA_FP8_E4M3 ? ra::kQuantE4m3 : d == RA_FP8_E5M2 ? ra::kQuantE5m2 : -1;
+  };
+  const int32_t kq = qk ? quant_type(p->k_cache_dtype) : 0;
+  const int32_t vq = qv ? quant_type(p->ckv_cache_dtype) : 0;
+  if (qk ? kq < 0 : p->k_cache_dtype != p->kv_dtype)
+    return fail(RA_ERR_INVALID_ARG, "k_cache dtype must be int8 or fp8 with a k scale, else equal to the kv dtype");
+  if (qv ? vq < 0 : p->ckv_cache_dtype != p->kv_dtype)
+    return fail(RA_ERR_INVALID_ARG, "ckv_cache dtype must be int8 or fp8 with a c_kv scale, else equal to the kv dtype");
+  const int32_t mode = p->cache_mode;
+  if (mode == RA_CACHE_PA_NZ || mode == RA_CACHE_PA_BLK_NZ)
+    return fail(RA_ERR_UNSUPPORTED, "FRACTAL_NZ cache modes are not built");
+  if (mode != RA_CACHE_NORM && mode != RA_CACHE_PA && mode != RA_CACHE_PA_BNSD && mode != RA_CACHE_PA_BLK_BNSD)
+    return fail(RA_ERR_INVALID_ARG, "unknown cache_mode");
+  if (mode == RA_CACHE_NORM) {
+    if (p->cache_seq_len < p->S) return fail(RA_ERR_INVALID_ARG, "NORM mode needs cache_seq_len >= S");
+    if (p->variant == 1 && (qk || qv))
+      return fail(RA_ERR_INVALID_ARG, "V1 in NORM mode takes no quantisation parameters");
+  } else {
+    if (p->block_num < 1 || p->block_size <= 1)
+      return fail(RA_ERR_INVALID_ARG, "block_num >= 1 and block_size > 1 are required");
+    if ((qk || qv) && p->block_size % 32 != 0)
+      return fail(RA_ERR_INVALID_ARG, "1-byte caches need block_size %% 32 == 0");
+    if ((!qk || !qv) && p->block_size % 16 != 0)
+      return fail(RA_ERR_INVALID_ARG, "2-byte caches need block_size %% 16 == 0");
+  }
+  if (p->rope_s_broadcast != 0 && p->rope_s_broadcast != 1)
+    return fail(RA_ERR_INVALID_ARG, "rope_s_broadcast must be 0 or 1");
   if (!(p->epsilon >= 0.f) || !std::isfinite(p->epsilon))
     return fail(RA_ERR_INVALID_ARG, "epsilon must be finite and >= 0");
-  if (p->is_output_kv && (!k_rope || !c_kv))
+  const bool outputs = p->is_output_kv && (mode != RA_CACHE_NORM || (p->variant == 2 && (qk || qv)));
+  if (outputs && (!k_rope || !c_kv))
     return fail(RA_ERR_INVALID_ARG, "is_output_kv requires k_rope and c_kv");
   if (!aligned16(kv) || !aligned16(gamma) || !aligned16(cos) || !aligned16(sin) ||
       !aligned16(k_cache) || !aligned16(ckv_cache) || (v_optional && !aligned16(v_optional)) ||
@@ -424,6 +438,8 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
       (reinterpret_cast<uintptr_t>(index) & 7u))
     return fail(RA_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned (index 8-byte)");
   if (p->B * p->N * p->S > (1LL << 40)) return fail(RA_ERR_INVALID_ARG, "too many rows");
+  if (mode == RA_CACHE_NORM && p->cache_seq_len > (1LL << 31)) return fail(RA_ERR_INVALID_ARG, "cache_seq_len too large");
+  if (p->S > (1LL << 31)) return fail(RA_ERR_INVALID_ARG, "S too large");
 
   ra::KvLaunch L{};
   L.kv = kv;
@@ -452,7 +468,12 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
   L.block_num = p->block_num;
   L.block_size = p->block_size;
   L.eps = p->epsilon;
-  L.out_kv = p->is_output_kv;
+  L.out_kv = outputs;
+  L.f16 = p->kv_dtype == RA_FP16;
+  L.kq = kq;
+  L.vq = vq;
+  L.rope_bcast = p->rope_s_broadcast;
+  L.cache_seq = mode == RA_CACHE_NORM ? p->cache_seq_len : 0;
   cudaError_t e = ra::launch_kv_rms_norm_rope_cache(L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_rms_norm_rope_cache launch");
   return ok();

@@ -66,33 +66,6 @@ struct NormRopeLaunch {
 };
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);
 
-// ------------------------------------------------------------ KV cache (K3)
-struct KvLaunch {
-  const uint16_t* kv;
-  const uint16_t* gamma;
-  const uint16_t* cos;
-  const uint16_t* sin;
-  const int64_t* index;
-  void* k_cache;
-  void* ckv_cache;
-  const float* k_scale;
-  const float* k_offset;
-  const float* v_scale;
-  const float* v_offset;
-  const uint16_t* v;
-  uint16_t* k_rope;
-  uint16_t* c_kv;
-  int32_t* err_count;
-  int64_t B, N, S, Dkv, Dv;
-  int32_t R;                   // rope size
-  int32_t variant;             // 1 or 2
-  int32_t mode;                // 1 = PA, 2 = PA_BNSD
-  int64_t block_num, block_size;
-  float eps;
-  int32_t out_kv;
-};
-cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream);
-
 int device_sm_count();
 
 // Sets the thread-local message returned by ra_last_error() ("where: what").

@@ -29,7 +29,10 @@
 //  * lane j < rope_size/8 of a row owns interleaved pairs 4j..4j+3, whose outputs
 //    land at positions 4j and rope_size/2 + 4j of the de-interleaved result.
 //    Cache rows are contiguous, so each scattered slot is written with whole vectors.
+#include <cuda_fp8.h>
+
 #include "internal.h"
+#include "kv_cache.h"
 #include "ptx.cuh"
 
 namespace ra {
@@ -38,35 +41,53 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
-
-__device__ __forceinline__ void unpack8(uint4 u, float2 (&f)[4]) {
-  f[0] = bf16x2_to_f2(u.x);
-  f[1] = bf16x2_to_f2(u.y);
-  f[2] = bf16x2_to_f2(u.z);
-  f[3] = bf16x2_to_f2(u.w);
+// 16-bit input elements: bf16 or fp16 (F16), two per 32-bit word, first in the low half
+template <bool F16>
+__device__ __forceinline__ float2 to_f2(uint32_t w) {
+  if constexpr (F16) return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  else return make_float2(bf16_lo(w), bf16_hi(w));
 }
+template <bool F16>
+__device__ __forceinline__ uint32_t from_f2(float a, float b) {
+  if constexpr (F16) return pack_f16x2(a, b);
+  else return pack_bf16x2(a, b);
+}
+template <bool F16>
+__device__ __forceinline__ void unpack8(uint4 u, float2 (&f)[4]) {
+  f[0] = to_f2<F16>(u.x);
+  f[1] = to_f2<F16>(u.y);
+  f[2] = to_f2<F16>(u.z);
+  f[3] = to_f2<F16>(u.w);
+}
+template <bool F16>
 __device__ __forceinline__ uint4 pack8(const float2 (&f)[4]) {
   uint4 u;
-  u.x = pack_bf16x2(f[0].x, f[0].y);
-  u.y = pack_bf16x2(f[1].x, f[1].y);
-  u.z = pack_bf16x2(f[2].x, f[2].y);
-  u.w = pack_bf16x2(f[3].x, f[3].y);
+  u.x = from_f2<F16>(f[0].x, f[0].y);
+  u.y = from_f2<F16>(f[1].x, f[1].y);
+  u.z = from_f2<F16>(f[2].x, f[2].y);
+  u.w = from_f2<F16>(f[3].x, f[3].y);
   return u;
 }
-// four int8 codes round_half_even(v * scale + offset), saturated to [-128, 127],
-// the first channel in the lowest byte.  cvt.rni saturates at the int32 range and
-// cvt.pack.sat (PTX ISA, sm_72+) clamps each value to the int8 range as it packs
-// two of them above the 16 bits taken from its third operand.
-__device__ __forceinline__ uint32_t quant4(float2 v01, float2 v23, float4 sc, float4 of) {
-  const int32_t a = __float2int_rn(fmaf(v01.x, sc.x, of.x));
-  const int32_t b = __float2int_rn(fmaf(v01.y, sc.y, of.y));
-  const int32_t c = __float2int_rn(fmaf(v23.x, sc.z, of.z));
-  const int32_t d = __float2int_rn(fmaf(v23.y, sc.w, of.w));
-  uint32_t hi, r;
-  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(d), "r"(c));
-  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
-  return r;
+// four quantised codes of v * scale + offset (one fp32 rounding), the first channel
+// in the lowest byte.  int8 (formula (3)): round half to even, saturated to
+// [-128, 127] -- cvt.rni saturates at the int32 range and cvt.pack.sat (PTX ISA,
+// sm_72+) clamps each value to the int8 range as it packs two of them above the
+// 16 bits taken from its third operand.  FP8: the hardware E4M3 / E5M2 conversion,
+// round to nearest even, saturated at the largest finite value.
+template <bool GEN>
+__device__ __forceinline__ uint32_t quant4(float2 v01, float2 v23, float4 sc, float4 of, int32_t qt) {
+  const float a = fmaf(v01.x, sc.x, of.x), b = fmaf(v01.y, sc.y, of.y);
+  const float c = fmaf(v23.x, sc.z, of.z), d = fmaf(v23.y, sc.w, of.w);
+  if (!GEN || qt == kQuantInt8) {
+    uint32_t hi, r;
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(__float2int_rn(d)), "r"(__float2int_rn(c)));
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(__float2int_rn(b)), "r"(__float2int_rn(a)), "r"(hi));
+    return r;
+  }
+  const __nv_fp8_interpretation_t k = qt == kQuantE4m3 ? __NV_E4M3 : __NV_E5M2;
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, k);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, k);
+  return lo | (hi << 16);
 }
 
 // Quantisation tables in shared memory, in units of 4 channels: scale[u] and
@@ -76,29 +97,32 @@ struct QuantTab {
   const float4* offset;
 };
 
-// 8 channels starting at `ch` (a multiple of 8) of a cache row: int8 or bf16
-__device__ __forceinline__ void store8(bool quant, void* row_base, int ch, const float2 (&v)[4],
+// 8 channels starting at `ch` (a multiple of 8) of a cache row: quantised (qt != 0,
+// one byte each) or in the input dtype
+template <bool F16, bool GEN>
+__device__ __forceinline__ void store8(int32_t qt, void* row_base, int ch, const float2 (&v)[4],
                                        QuantTab t) {
-  if (quant) {
+  if (qt != kQuantNone) {
     const int u = ch >> 2;
     uint2 w;
-    w.x = quant4(v[0], v[1], t.scale[u], t.offset[u]);
-    w.y = quant4(v[2], v[3], t.scale[u + 1], t.offset[u + 1]);
-    *reinterpret_cast<uint2*>(static_cast<int8_t*>(row_base) + ch) = w;
+    w.x = quant4<GEN>(v[0], v[1], t.scale[u], t.offset[u], qt);
+    w.y = quant4<GEN>(v[2], v[3], t.scale[u + 1], t.offset[u + 1], qt);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(row_base) + ch) = w;
   } else {
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(row_base) + ch) = pack8(v);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(row_base) + ch) = pack8<F16>(v);
   }
 }
 // 4 channels starting at `ch` (a multiple of 4)
-__device__ __forceinline__ void store4(bool quant, void* row_base, int ch, float2 v01, float2 v23,
+template <bool F16, bool GEN>
+__device__ __forceinline__ void store4(int32_t qt, void* row_base, int ch, float2 v01, float2 v23,
                                        QuantTab t) {
-  if (quant) {
-    *reinterpret_cast<uint32_t*>(static_cast<int8_t*>(row_base) + ch) =
-        quant4(v01, v23, t.scale[ch >> 2], t.offset[ch >> 2]);
+  if (qt != kQuantNone) {
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(row_base) + ch) =
+        quant4<GEN>(v01, v23, t.scale[ch >> 2], t.offset[ch >> 2], qt);
   } else {
     uint2 w;
-    w.x = pack_bf16x2(v01.x, v01.y);
-    w.y = pack_bf16x2(v23.x, v23.y);
+    w.x = from_f2<F16>(v01.x, v01.y);
+    w.y = from_f2<F16>(v23.x, v23.y);
     *reinterpret_cast<uint2*>(static_cast<uint16_t*>(row_base) + ch) = w;
   }
 }
@@ -107,7 +131,7 @@ __device__ __forceinline__ void store4(bool quant, void* row_base, int ch, float
 struct KvAux {
   float inv_rms;      // 1 / rms_size
   int32_t bs_shift;   // log2(block_size) when it is a power of two, else -1
-  int32_t qk, qv;     // int8 k / ckv caches
+  int32_t blocks_per_batch;  // PA_BLK_BNSD: ceil(S / block_size) index entries per batch
 };
 
 // What one lane needs from HBM for its row of a row group, as raw vectors, so
@@ -118,14 +142,15 @@ struct RowIn {
   uint4 xr;                // V1: chunk j of the raw RoPE part
   uint4 v[CPL];            // V2: chunks j + LPR*i of v_optional
   uint2 c1, c2, s1, s2;    // cos/sin of pairs 4j..4j+3, at j and R/2 + j
-  int64_t slot;
+  int64_t slot;            // the index entry (PA_BLK_BNSD: the start of the token's block)
   int32_t n;
+  int32_t aux;             // Norm: the batch b; PA_BLK_BNSD: s % block_size
 };
 
 // (b, n, s) of one row, advanced without division.
 struct Cursor {
-  int64_t row, tok;        // tok = b * S + s, the entry of `index`
-  int32_t n, s;
+  int64_t row, tok;        // tok = b * S + s
+  int32_t b, n, s;
   __device__ __forceinline__ void advance(int32_t step, int32_t N, int32_t S) {
     row += step;
     tok += step;
@@ -135,17 +160,16 @@ struct Cursor {
       tok -= S;
       if (++n == N) {
         n = 0;
+        ++b;
         tok += S;
       }
     }
   }
 };
 
-// Lane layout: a warp processes RPG = 32 / LPR rows at once; lane = j * RPG + g
-// works on row g of the group and owns its 16-byte chunks j + LPR * i, i < CPL
-// (the rows of a group are interleaved across lanes, so lanes that read the same
-// quantisation-table entry sit next to each other).
-template <int VARIANT, int LPR, int CPL>
+// GEN: the general kernel (Norm and PA_BLK_BNSD modes, S-broadcast cos/sin, FP8
+// caches); without it only PA / PA_BNSD with int8 or 16-bit caches is compiled in.
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
 struct KvRows {
   const KvLaunch& p;
   KvAux aux;
@@ -174,14 +198,24 @@ struct KvRows {
       }
     }
     if (valid && j < rope_lanes) {
-      const uint16_t* cs = p.cos + c.row * p.R;
-      const uint16_t* sn = p.sin + c.row * p.R;
+      // cos/sin row: (b, n, s), or (b, n, 0) when they are broadcast over S
+      const int64_t rrow = GEN && p.rope_bcast ? static_cast<int64_t>(c.b) * p.N + c.n : c.row;
+      const uint16_t* cs = p.cos + rrow * p.R;
+      const uint16_t* sn = p.sin + rrow * p.R;
       in.c1 = __ldcs(reinterpret_cast<const uint2*>(cs + 4 * j));
       in.c2 = __ldcs(reinterpret_cast<const uint2*>(cs + half + 4 * j));
       in.s1 = __ldcs(reinterpret_cast<const uint2*>(sn + 4 * j));
       in.s2 = __ldcs(reinterpret_cast<const uint2*>(sn + half + 4 * j));
     }
-    in.slot = valid ? __ldg(p.index + c.tok) : int64_t(-1);
+    // the index entry of this token (PA_BLK_BNSD: of its block of block_size tokens)
+    int64_t ipos = c.tok;
+    in.aux = GEN && p.mode == kModeNorm ? c.b : 0;
+    if (GEN && p.mode == kModePaBlkBnsd) {
+      const int32_t blk = aux.bs_shift >= 0 ? c.s >> aux.bs_shift : static_cast<int32_t>(c.s / p.block_size);
+      ipos = static_cast<int64_t>(c.b) * aux.blocks_per_batch + blk;
+      in.aux = c.s - static_cast<int32_t>(static_cast<int64_t>(blk) * p.block_size);
+    }
+    in.slot = valid ? __ldg(p.index + ipos) : int64_t(-1);
     in.n = c.n;
   }
 
@@ -192,7 +226,7 @@ struct KvRows {
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      unpack8(in.x[i], y[i]);
+      unpack8<F16>(in.x[i], y[i]);
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc = __ffma2_rn(y[i][k], y[i][k], acc);
     }
@@ -204,30 +238,36 @@ struct KvRows {
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       float2 g[4];
-      unpack8(gam[i], g);
+      unpack8<F16>(gam[i], g);
 #pragma unroll
       for (int k = 0; k < 4; ++k) y[i][k] = __fmul2_rn(__fmul2_rn(y[i][k], inv2), g[k]);
     }
     if (!valid) return;
 
-    // (4) slot of this token
-    const int64_t slot = in.slot;
+    // (4) slot of this token: the index entry, in PA_BLK_BNSD plus the token's place in its block
+    int64_t slot = in.slot;
+    if (GEN && p.mode == kModePaBlkBnsd && slot >= 0) slot += in.aux;
     const bool to_cache = slot >= 0 && slot < slots;
     if (!to_cache && slot != -1 && n == 0 && j == 0 && p.err_count != nullptr)
       atomicAdd(p.err_count, 1);  // once per token, not per head
-    int64_t blk = 0, off = 0;
+    int64_t cache_row = 0;
     if (to_cache) {
-      if (aux.bs_shift >= 0) {
-        blk = slot >> aux.bs_shift;
-        off = slot & (p.block_size - 1);
+      if (GEN && p.mode == kModeNorm) {  // [B, N, Scache, D]
+        cache_row = (static_cast<int64_t>(in.aux) * p.N + n) * p.cache_seq + slot;
       } else {
-        blk = slot / p.block_size;
-        off = slot - blk * p.block_size;
+        int64_t blk, off;
+        if (aux.bs_shift >= 0) {
+          blk = slot >> aux.bs_shift;
+          off = slot & (p.block_size - 1);
+        } else {
+          blk = slot / p.block_size;
+          off = slot - blk * p.block_size;
+        }
+        cache_row = p.mode == kModePa ? (blk * p.block_size + off) * p.N + n   // [bn, bs, N, D]
+                                      : (blk * p.N + n) * p.block_size + off;  // [bn, N, bs, D]
       }
     }
-    const int64_t cache_row = p.mode == 2 ? (blk * p.N + n) * p.block_size + off
-                                          : (blk * p.block_size + off) * p.N + n;
-    const bool qk = aux.qk != 0, qv = aux.qv != 0;
+    const int32_t qk = p.kq, qv = p.vq;
     void* k_row = static_cast<uint8_t*>(p.k_cache) + static_cast<size_t>(cache_row) * kw * (qk ? 1 : 2);
     void* c_row = static_cast<uint8_t*>(p.ckv_cache) + static_cast<size_t>(cache_row) * cw * (qv ? 1 : 2);
     const QuantTab kt{kt0.scale + (VARIANT == 2 ? n * (kw / 4) : 0), kt0.offset + (VARIANT == 2 ? n * (kw / 4) : 0)};
@@ -239,16 +279,16 @@ struct KvRows {
     if (j < rope_lanes) {
       float2 r[4];
       if (VARIANT == 1) {
-        unpack8(in.xr, r);
+        unpack8<F16>(in.xr, r);
       } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k) r[k] = y[0][k];
       }
       // r[m] = (x1, x2) of pair 4j + m
-      const float2 c1a = bf16x2_to_f2(in.c1.x), c1b = bf16x2_to_f2(in.c1.y);
-      const float2 c2a = bf16x2_to_f2(in.c2.x), c2b = bf16x2_to_f2(in.c2.y);
-      const float2 s1a = bf16x2_to_f2(in.s1.x), s1b = bf16x2_to_f2(in.s1.y);
-      const float2 s2a = bf16x2_to_f2(in.s2.x), s2b = bf16x2_to_f2(in.s2.y);
+      const float2 c1a = to_f2<F16>(in.c1.x), c1b = to_f2<F16>(in.c1.y);
+      const float2 c2a = to_f2<F16>(in.c2.x), c2b = to_f2<F16>(in.c2.y);
+      const float2 s1a = to_f2<F16>(in.s1.x), s1b = to_f2<F16>(in.s1.y);
+      const float2 s2a = to_f2<F16>(in.s2.x), s2b = to_f2<F16>(in.s2.y);
       const float2 x1a = make_float2(r[0].x, r[1].x), x1b = make_float2(r[2].x, r[3].x);
       const float2 x2a = make_float2(r[0].y, r[1].y), x2b = make_float2(r[2].y, r[3].y);
       // out_m = x1 cos_m - x2 sin_m ; out_{R/2+m} = x2 cos_{R/2+m} + x1 sin_{R/2+m}
@@ -257,12 +297,12 @@ struct KvRows {
       const float2 o2a = __ffma2_rn(x2a, c2a, __fmul2_rn(x1a, s2a));
       const float2 o2b = __ffma2_rn(x2b, c2b, __fmul2_rn(x1b, s2b));
       if (to_cache) {
-        store4(qk, k_row, 4 * j, o1a, o1b, kt);
-        store4(qk, k_row, half + 4 * j, o2a, o2b, kt);
+        store4<F16, GEN>(qk, k_row, 4 * j, o1a, o1b, kt);
+        store4<F16, GEN>(qk, k_row, half + 4 * j, o2a, o2b, kt);
       }
       if (kr_row != nullptr) {
-        store4(false, kr_row, 4 * j, o1a, o1b, kt);
-        store4(false, kr_row, half + 4 * j, o2a, o2b, kt);
+        store4<F16, GEN>(kQuantNone, kr_row, 4 * j, o1a, o1b, kt);
+        store4<F16, GEN>(kQuantNone, kr_row, half + 4 * j, o2a, o2b, kt);
       }
     }
 
@@ -272,8 +312,8 @@ struct KvRows {
       for (int i = 0; i < CPL; ++i) {
         const int ch = j + LPR * i;
         if (ch >= rope_lanes && ch < rms_chunks) {
-          if (to_cache) store8(qk, k_row, 8 * ch, y[i], kt);
-          if (kr_row != nullptr) store8(false, kr_row, 8 * ch, y[i], kt);
+          if (to_cache) store8<F16, GEN>(qk, k_row, 8 * ch, y[i], kt);
+          if (kr_row != nullptr) store8<F16, GEN>(kQuantNone, kr_row, 8 * ch, y[i], kt);
         }
       }
       // ckv <- v_optional
@@ -284,8 +324,8 @@ struct KvRows {
           if (to_cache) {
             if (qv) {
               float2 f[4];
-              unpack8(in.v[i], f);
-              store8(true, c_row, 8 * ch, f, vt);
+              unpack8<F16>(in.v[i], f);
+              store8<F16, GEN>(qv, c_row, 8 * ch, f, vt);
             } else {
               *reinterpret_cast<uint4*>(static_cast<uint16_t*>(c_row) + 8 * ch) = in.v[i];
             }
@@ -299,8 +339,8 @@ struct KvRows {
       for (int i = 0; i < CPL; ++i) {
         const int ch = j + LPR * i;
         if (ch < rms_chunks) {
-          if (to_cache) store8(qv, c_row, 8 * ch, y[i], vt);
-          if (ckv_row != nullptr) store8(false, ckv_row, 8 * ch, y[i], vt);
+          if (to_cache) store8<F16, GEN>(qv, c_row, 8 * ch, y[i], vt);
+          if (ckv_row != nullptr) store8<F16, GEN>(kQuantNone, ckv_row, 8 * ch, y[i], vt);
         }
       }
     }
@@ -317,7 +357,7 @@ size_t quant_table_bytes(const KvLaunch& L, bool qk, bool qv) {
 
 constexpr int kMinBlocks = 3;  // 12 warps per SM: up to 168 registers per thread
 
-template <int VARIANT, int LPR, int CPL>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     kv_rms_norm_rope_cache_kernel(const KvLaunch p, const KvAux aux) {
   extern __shared__ float4 tabs[];
@@ -345,13 +385,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     const int ch = j + LPR * i;
     gam[i] = ch * 8 < rms ? __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * ch)) : make_uint4(0, 0, 0, 0);
   }
-  const int ku = aux.qk ? heads * kw / 4 : 0, vu = aux.qv ? heads * cw / 4 : 0;
+  const int ku = p.kq ? heads * kw / 4 : 0, vu = p.vq ? heads * cw / 4 : 0;
   float4* ks = tabs;
   float4* ko = ks + ku;
   float4* vs = ko + ku;
   float4* vo = vs + vu;
-  const KvRows<VARIANT, LPR, CPL> w{p, aux, j, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
-                                    p.block_num * p.block_size, gam, QuantTab{ks, ko}, QuantTab{vs, vo}};
+  const int64_t slots = p.mode == kModeNorm ? p.cache_seq : p.block_num * p.block_size;
+  const KvRows<VARIANT, LPR, CPL, F16, GEN> w{p, aux, j, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
+                                         slots, gam, QuantTab{ks, ko}, QuantTab{vs, vo}};
 
   // the lane's load cursor: row r_begin + g, then RPG rows further each step
   Cursor cur;
@@ -361,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     const int64_t per_b = p.N * p.S;
     const int64_t b = start / per_b, rem = start - b * per_b;
     cur.row = start;
+    cur.b = static_cast<int32_t>(b);
     cur.n = static_cast<int32_t>(rem / p.S);
     cur.s = static_cast<int32_t>(rem - static_cast<int64_t>(cur.n) * p.S);
     cur.tok = b * p.S + cur.s;
@@ -416,10 +458,10 @@ unsigned persistent_grid(K kernel, int64_t rows, size_t smem) {
   return static_cast<unsigned>(want < cap ? want : cap);
 }
 
-template <int VARIANT, int LPR, int CPL>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
 cudaError_t launch_one(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
-  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL>;
-  const size_t smem = quant_table_bytes(L, aux.qk != 0, aux.qv != 0);
+  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL, F16, GEN>;
+  const size_t smem = quant_table_bytes(L, L.kq != 0, L.vq != 0);
   if (smem > 48 * 1024) {
     const cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -430,25 +472,31 @@ cudaError_t launch_one(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int VARIANT, int LPR>
-cudaError_t launch_cpl(const KvLaunch& L, const KvAux& aux, int cpl, cudaStream_t st) {
-  switch (cpl) {
-    case 1: return launch_one<VARIANT, LPR, 1>(L, aux, st);
-    case 2: return launch_one<VARIANT, LPR, 2>(L, aux, st);
-    case 3: return launch_one<VARIANT, LPR, 3>(L, aux, st);
-    case 4: return launch_one<VARIANT, LPR, 4>(L, aux, st);
-    default: return cudaErrorInvalidValue;
+// lane layouts built: 8 lanes per row with 1-4 chunks each, or 16 / 32 lanes with 4
+template <int VARIANT, bool F16, bool GEN>
+cudaError_t launch_layout(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st) {
+  if (lpr == 8) {
+    switch (cpl) {
+      case 1: return launch_one<VARIANT, 8, 1, F16, GEN>(L, aux, st);
+      case 2: return launch_one<VARIANT, 8, 2, F16, GEN>(L, aux, st);
+      case 3: return launch_one<VARIANT, 8, 3, F16, GEN>(L, aux, st);
+      case 4: return launch_one<VARIANT, 8, 4, F16, GEN>(L, aux, st);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  if (lpr == 16) return launch_one<VARIANT, 16, 4, F16, GEN>(L, aux, st);
+  if (lpr == 32) return launch_one<VARIANT, 32, 4, F16, GEN>(L, aux, st);
+  return cudaErrorInvalidValue;
 }
 
 template <int VARIANT>
 cudaError_t launch_variant(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st) {
-  switch (lpr) {
-    case 8: return launch_cpl<VARIANT, 8>(L, aux, cpl, st);
-    case 16: return launch_cpl<VARIANT, 16>(L, aux, cpl, st);
-    case 32: return launch_cpl<VARIANT, 32>(L, aux, cpl, st);
-    default: return cudaErrorInvalidValue;
-  }
+  const bool gen = (L.mode != kModePa && L.mode != kModePaBnsd) || L.rope_bcast ||
+                   L.kq == kQuantE4m3 || L.kq == kQuantE5m2 || L.vq == kQuantE4m3 || L.vq == kQuantE5m2;
+  if (L.f16) return gen ? launch_layout<VARIANT, true, true>(L, aux, lpr, cpl, st)
+                        : launch_layout<VARIANT, true, false>(L, aux, lpr, cpl, st);
+  return gen ? launch_layout<VARIANT, false, true>(L, aux, lpr, cpl, st)
+             : launch_layout<VARIANT, false, false>(L, aux, lpr, cpl, st);
 }
 
 }  // namespace
@@ -459,12 +507,13 @@ cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream
   if (L.variant == 2 && L.Dv / 8 > chunks) chunks = L.Dv / 8;  // v_optional rides the same lanes
   const int64_t rope_lanes = L.R / 8;
   // the fewest lanes per row that hold the RoPE pairs and at most 4 chunks each
+  // (8 lanes: as many chunks as needed; 16 or 32 lanes: 4)
   int lpr = 0, cpl = 0;
   for (int cand : {8, 16, 32}) {
     const int64_t c = (chunks + cand - 1) / cand;
     if (cand >= rope_lanes && c <= 4) {
       lpr = cand;
-      cpl = static_cast<int>(c);
+      cpl = cand == 8 ? static_cast<int>(c) : 4;
       break;
     }
   }
@@ -472,11 +521,13 @@ cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream
   KvAux aux{};
   aux.inv_rms = 1.0f / static_cast<float>(rms);
   aux.bs_shift = -1;
-  if ((L.block_size & (L.block_size - 1)) == 0)
-    for (aux.bs_shift = 0; (int64_t(1) << aux.bs_shift) < L.block_size; ++aux.bs_shift) {
-    }
-  aux.qk = L.k_scale != nullptr;
-  aux.qv = L.v_scale != nullptr;
+  aux.blocks_per_batch = 0;
+  if (L.mode != kModeNorm) {  // paged modes: block_size > 1 (checked by the caller)
+    if ((L.block_size & (L.block_size - 1)) == 0)
+      for (aux.bs_shift = 0; (int64_t(1) << aux.bs_shift) < L.block_size; ++aux.bs_shift) {
+      }
+    aux.blocks_per_batch = static_cast<int32_t>((L.S + L.block_size - 1) / L.block_size);
+  }
   return L.variant == 1 ? launch_variant<1>(L, aux, lpr, cpl, stream)
                         : launch_variant<2>(L, aux, lpr, cpl, stream);
 }

@@ -19,10 +19,11 @@ RA_OK = 0
 STATUS_NAMES = {0: "RA_OK", -1: "RA_ERR_INVALID_ARG", -2: "RA_ERR_UNSUPPORTED",
                 -3: "RA_ERR_ALIGNMENT", -4: "RA_ERR_WORKSPACE", -5: "RA_ERR_CUDA",
                 -6: "RA_ERR_TIMEOUT", -7: "RA_ERR_INDEX"}
-RA_BF16, RA_FP16, RA_INT8, RA_FP32 = 0, 1, 2, 3
+RA_BF16, RA_FP16, RA_INT8, RA_FP32, RA_FP8_E4M3, RA_FP8_E5M2 = 0, 1, 2, 3, 4, 5
 RA_NORM_NONE, RA_NORM_RMS_ACROSS_HEADS = 0, 1
 RA_LAYOUT_BSD, RA_LAYOUT_NBSD = 0, 1
-RA_CACHE_PA, RA_CACHE_PA_BNSD = 1, 2
+RA_CACHE_NORM, RA_CACHE_PA, RA_CACHE_PA_BNSD, RA_CACHE_PA_NZ, RA_CACHE_PA_BLK_BNSD, RA_CACHE_PA_BLK_NZ = \
+    0, 1, 2, 3, 4, 5
 
 EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns", "ra_test_stall_next_projection",
            "qkv_cte_mx_packed_weight_bytes", "qkv_cte_mx_pack_weight", "qkv_cte_mx_workspace_bytes",
@@ -51,7 +52,8 @@ class KvRmsNormRopeCacheParams(ctypes.Structure):
                 ("block_num", ctypes.c_int64), ("block_size", ctypes.c_int64),
                 ("kv_dtype", ctypes.c_int32), ("k_cache_dtype", ctypes.c_int32),
                 ("ckv_cache_dtype", ctypes.c_int32), ("epsilon", ctypes.c_float),
-                ("is_output_kv", ctypes.c_int32)]
+                ("is_output_kv", ctypes.c_int32), ("rope_s_broadcast", ctypes.c_int32),
+                ("cache_seq_len", ctypes.c_int64)]
 
 
 _LIB = None
@@ -118,10 +120,10 @@ def _stream(stream) -> int:
 
 
 def _bits16(t: torch.Tensor | None) -> torch.Tensor | None:
-    """bf16 tensors are passed as their 16-bit patterns."""
+    """bf16 / fp16 tensors are passed as their 16-bit patterns."""
     if t is None:
         return None
-    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+    return t.view(torch.int16) if t.dtype in (torch.bfloat16, torch.float16) else t
 
 
 def ra_abi_version() -> int:

@@ -11,13 +11,15 @@ import torch
 from . import native, synth
 
 
-def to_dev(x: np.ndarray | None, device: str = "cuda") -> torch.Tensor | None:
-    """numpy -> device tensor; uint16 arrays (bf16 bit patterns) become torch.bfloat16."""
+def to_dev(x: np.ndarray | None, device: str = "cuda", half: str = "bf16") -> torch.Tensor | None:
+    """numpy -> device tensor; uint16 arrays (16-bit float bit patterns) become
+    torch.bfloat16, or torch.float16 with half="fp16"."""
     if x is None:
         return None
     x = np.ascontiguousarray(x)
     if x.dtype == np.uint16:
-        return torch.from_numpy(x.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(x.view(np.int16)).to(device).view(
+            torch.float16 if half == "fp16" else torch.bfloat16)
     return torch.from_numpy(x).to(device)
 
 
@@ -76,33 +78,38 @@ class QkvRun:
 class KvRun:
     """Device buffers for one kv_rms_norm_rope_cache call of a synth.KVCase."""
 
+    QTYPES = {"int8": native.RA_INT8, "e4m3": native.RA_FP8_E4M3, "e5m2": native.RA_FP8_E5M2}
+
     def __init__(self, case: synth.KVCase, device: str = "cuda"):
         self.case = c = case
         qk, qv = c.k_scale is not None, c.v_scale is not None
+        half = native.RA_FP16 if c.dtype == "fp16" else native.RA_BF16
         self.params = native.KvRmsNormRopeCacheParams(
             B=c.B, N=c.N, S=c.S, Dkv=c.Dkv, Dv=c.Dv, rope_size=c.rope_size, variant=c.variant,
             cache_mode=synth.CACHE_MODES[c.cache_mode], block_num=c.block_num,
-            block_size=c.block_size, kv_dtype=native.RA_BF16,
-            k_cache_dtype=native.RA_INT8 if qk else native.RA_BF16,
-            ckv_cache_dtype=native.RA_INT8 if qv else native.RA_BF16,
-            epsilon=c.eps, is_output_kv=1 if c.is_output_kv else 0)
-        self.kv = to_dev(c.kv, device)
-        self.gamma = to_dev(c.gamma, device)
-        self.cos = to_dev(c.cos, device)
-        self.sin = to_dev(c.sin, device)
-        self.index = to_dev(c.index, device)
-        self.k_cache = to_dev(c.k_cache, device)
-        self.ckv_cache = to_dev(c.ckv_cache, device)
-        self.k_scale = to_dev(c.k_scale, device)
-        self.k_offset = to_dev(c.k_offset, device)
-        self.v_scale = to_dev(c.v_scale, device)
-        self.v_offset = to_dev(c.v_offset, device)
-        self.v = to_dev(c.v, device)
+            block_size=c.block_size, kv_dtype=half,
+            k_cache_dtype=self.QTYPES[c.k_qtype] if qk else half,
+            ckv_cache_dtype=self.QTYPES[c.v_qtype] if qv else half,
+            epsilon=c.eps, is_output_kv=1 if c.is_output_kv else 0,
+            rope_s_broadcast=1 if c.cos.shape[2] == 1 and c.S > 1 else 0, cache_seq_len=c.cache_seq)
+        dev = lambda x: to_dev(x, device, c.dtype)
+        self.kv = dev(c.kv)
+        self.gamma = dev(c.gamma)
+        self.cos = dev(c.cos)
+        self.sin = dev(c.sin)
+        self.index = dev(c.index)
+        self.k_cache = dev(c.k_cache)
+        self.ckv_cache = dev(c.ckv_cache)
+        self.k_scale = dev(c.k_scale)
+        self.k_offset = dev(c.k_offset)
+        self.v_scale = dev(c.v_scale)
+        self.v_offset = dev(c.v_offset)
+        self.v = dev(c.v)
         rows = (c.B, c.N, c.S)
-        self.k_rope = (torch.empty(rows + (c.k_width,), dtype=torch.bfloat16, device=device)
-                       if c.is_output_kv else None)
-        self.c_kv = (torch.empty(rows + (c.ckv_width,), dtype=torch.bfloat16, device=device)
-                     if c.is_output_kv else None)
+        self.outputs = c.is_output_kv and (c.cache_mode != "Norm" or (c.variant == 2 and (qk or qv)))
+        fdt = torch.float16 if c.dtype == "fp16" else torch.bfloat16
+        self.k_rope = torch.empty(rows + (c.k_width,), dtype=fdt, device=device) if self.outputs else None
+        self.c_kv = torch.empty(rows + (c.ckv_width,), dtype=fdt, device=device) if self.outputs else None
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
 
     def run(self, stream=None) -> None:

@@ -278,7 +278,7 @@ def sample_rows(T: int, seed: int, n_head: int = 128, n_tail: int = 256, n_rand:
 # ---------------------------------------------------------------------------
 # KvRmsNormRopeCache inputs
 # ---------------------------------------------------------------------------
-CACHE_MODES = {"PA": 1, "PA_BNSD": 2}
+CACHE_MODES = {"Norm": 0, "PA": 1, "PA_BNSD": 2, "PA_BLK_BNSD": 4}
 
 
 @dataclasses.dataclass

@@ -38,7 +38,7 @@ def test_exports_every_declared_function(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in the header but not exported"
     assert sorted(names) == sorted(native.EXPORTS)
-    assert native.ra_abi_version() == 2
+    assert native.ra_abi_version() == 3
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -178,8 +178,14 @@ def kv_call(L, p, **over):
     (dict(k_cache_dtype=2, ckv_cache_dtype=2, block_size=48), dict(ks=A16, vs=A16), -1),
     (dict(block_size=24), {}, -1),                              # bf16 caches need %16
     (dict(block_size=1), {}, -1),
-    (dict(cache_mode=0), {}, -2), (dict(cache_mode=3), {}, -2),  # Norm, PA_NZ not built
-    (dict(kv_dtype=1, k_cache_dtype=1, ckv_cache_dtype=1), {}, -2),  # fp16 not built
+    (dict(cache_mode=0), {}, -1),                               # Norm needs cache_seq_len >= S
+    (dict(cache_mode=0, cache_seq_len=64, k_cache_dtype=2), dict(ks=A16), -1),  # V1 Norm: no quant
+    (dict(cache_mode=3), {}, -2), (dict(cache_mode=5), {}, -2),  # FRACTAL_NZ modes not built
+    (dict(cache_mode=6), {}, -1),                               # unknown mode
+    (dict(kv_dtype=3, k_cache_dtype=3, ckv_cache_dtype=3), {}, -1),  # fp32 kv
+    (dict(k_cache_dtype=3), dict(ks=A16), -1),                  # fp32 is not a quantised cache type
+    (dict(k_cache_dtype=4, ckv_cache_dtype=5, block_size=48), dict(ks=A16, vs=A16), -1),  # 1-byte: %32
+    (dict(rope_s_broadcast=2), {}, -1),
     (dict(is_output_kv=1), {}, -1),                             # needs k_rope / c_kv
     (dict(epsilon=-1.0), {}, -1),
     ({}, dict(kv=A16 + 2), -3), ({}, dict(index=A16 + 4), -3), ({}, dict(kc=A16 + 8), -3),

@@ -69,6 +69,67 @@ def test_small(name, kw, skip):
     check_kv(case, run_case(case), name)
 
 
+VARIANTS = [
+    # Norm cache mode: [B, N, Scache, D], index [B, S] of per-batch offsets
+    ("norm_v2_int8", dict(variant=2, B=3, N=4, S=37, Dkv=192, Dv=128, cache_mode="Norm", cache_seq=50,
+                          quant_k=True, quant_v=True)),
+    ("norm_v2_bf16_no_outputs", dict(variant=2, B=2, N=2, S=20, Dkv=192, Dv=128, cache_mode="Norm",
+                                     cache_seq=24)),
+    ("norm_v1_bf16", dict(variant=1, B=3, N=1, S=21, Dkv=576, Dv=512, cache_mode="Norm", cache_seq=21)),
+    # PA_BLK_BNSD: one start slot per block of block_size tokens; partial last block
+    ("blk_v2_int8", dict(variant=2, B=2, N=2, S=70, Dkv=192, Dv=128, block_size=32,
+                         cache_mode="PA_BLK_BNSD", quant_k=True, quant_v=True)),
+    ("blk_v1_bf16_bs48", dict(variant=1, B=2, N=1, S=100, Dkv=576, Dv=512, block_size=48,
+                              cache_mode="PA_BLK_BNSD")),
+    # cos/sin [B, N, 1, R] broadcast over S
+    ("bcast_v2_int8", dict(variant=2, B=2, N=8, S=29, Dkv=192, Dv=128, block_size=32, block_num=4,
+                           quant_k=True, quant_v=True, rope_broadcast=True)),
+    ("bcast_norm_v1", dict(variant=1, B=2, N=1, S=33, Dkv=576, Dv=512, cache_mode="Norm",
+                           cache_seq=40, rope_broadcast=True)),
+    # fp16 inputs (and fp16 caches / outputs when not quantised)
+    ("fp16_v1", dict(variant=1, B=2, N=1, S=45, Dkv=576, Dv=512, block_size=16, block_num=8, dtype="fp16")),
+    ("fp16_v2_int8_k", dict(variant=2, B=2, N=4, S=30, Dkv=192, Dv=128, block_size=32, block_num=2,
+                            dtype="fp16", quant_k=True)),
+    ("fp16_v2_pa", dict(variant=2, B=3, N=2, S=21, Dkv=192, Dv=128, block_size=16, block_num=4,
+                        dtype="fp16", cache_mode="PA")),
+    # FP8 caches
+    ("fp8_v2_e4m3_e5m2", dict(variant=2, B=2, N=8, S=29, Dkv=192, Dv=128, block_size=32, block_num=4,
+                              quant_k=True, quant_v=True, k_qtype="e4m3", v_qtype="e5m2")),
+    ("fp8_v1_e5m2_sym", dict(variant=1, B=2, N=1, S=45, Dkv=576, Dv=512, block_size=32, block_num=4,
+                             quant_k=True, quant_v=True, k_qtype="e5m2", v_qtype="e4m3", offsets=False)),
+    ("fp8_fp16_norm_v2", dict(variant=2, B=2, N=2, S=40, Dkv=192, Dv=128, cache_mode="Norm", cache_seq=40,
+                              dtype="fp16", quant_k=True, quant_v=True, k_qtype="e4m3", v_qtype="int8")),
+]
+
+
+@pytest.mark.parametrize("name,kw", VARIANTS, ids=[s[0] for s in VARIANTS])
+@pytest.mark.parametrize("skip", [0.0, 0.2])
+def test_variants(name, kw, skip):
+    case = synth.make_kv(name, 400 + len(name), skip_frac=skip, **kw)
+    if "fp8" in name and case.k_scale is not None:
+        case.k_scale *= 8.0  # drive some codes into saturation
+    check_kv(case, run_case(case), name)
+
+
+def test_norm_mode_repeated_offsets_and_bad_values():
+    """Norm mode: the same offsets in different batches are legal; an offset outside
+    [-1, Scache) is counted once per token and not written."""
+    case = synth.make_kv("norm_bad", 9, variant=2, B=3, N=2, S=16, Dkv=192, Dv=128, cache_mode="Norm",
+                         cache_seq=20, quant_k=True, quant_v=True)
+    case.index[1] = case.index[0]
+    case.index[2, 3] = 20
+    case.index[0, 5] = -3
+    check_kv(case, run_case(case), "norm-bad")
+
+
+def test_blk_mode_skipped_and_bad_blocks():
+    case = synth.make_kv("blk_bad", 10, variant=2, B=2, N=2, S=50, Dkv=192, Dv=128, block_size=16,
+                         cache_mode="PA_BLK_BNSD")
+    case.index[1] = -1                                       # a whole block skipped
+    case.index[4] = case.block_num * case.block_size - 3     # block runs past the end of the cache
+    check_kv(case, run_case(case), "blk-bad")
+
+
 def test_out_of_range_index_counted_not_written():
     case = synth.make_kv("bad", 7, variant=2, B=2, N=2, S=16, Dkv=192, Dv=128, block_size=16,
                          block_num=4, skip_frac=0.1)
