@@ -68,6 +68,16 @@ def rms_norm_across_heads(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.nd
     return x * inv_rms[:, None] * np.asarray(gamma, dtype=np.float64)[None, :]
 
 
+def rms_norm_per_head(x: np.ndarray, gamma: np.ndarray, eps: float, head_dim: int) -> np.ndarray:
+    """The upstream (per-head) qk-norm (qkv_cte page, Design 1: each head's d_head
+    slice is normalised by its own RMS), with the per-head [d_head] gamma."""
+    T = x.shape[0]
+    xh = x.reshape(T, -1, head_dim)
+    inv_rms = 1.0 / np.sqrt(np.sum(xh * xh, axis=2) / head_dim + eps)
+    y = xh * inv_rms[:, :, None] * np.asarray(gamma, dtype=np.float64)[None, None, :]
+    return y.reshape(T, -1)
+
+
 def rope_rotate_half(y: np.ndarray, cos: np.ndarray, sin: np.ndarray, head_dim: int) -> np.ndarray:
     """Per head: out_lo = y_lo*cos_lo - y_hi*sin_lo; out_hi = y_hi*cos_hi + y_lo*sin_hi."""
     T = y.shape[0]
@@ -82,7 +92,7 @@ def rope_rotate_half(y: np.ndarray, cos: np.ndarray, sin: np.ndarray, head_dim: 
 
 
 def qkv_cte_mx(a, a_scale, w, w_block_exp, *, num_heads: int, num_kv_heads: int, head_dim: int,
-               weight_scales=None, bias=None, q_norm: bool = True, k_norm: bool = True,
+               weight_scales=None, bias=None, q_norm=True, k_norm=True,
                q_gamma=None, k_gamma=None, eps: float = 1e-6, fused_rope: bool = False,
                cos=None, sin=None) -> np.ndarray:
     """Full prologue for the given token rows.
@@ -92,6 +102,8 @@ def qkv_cte_mx(a, a_scale, w, w_block_exp, *, num_heads: int, num_kv_heads: int,
     None; q_gamma [n_q*d] / k_gamma [n_kv*d] fp32; cos/sin [T,d] fp32 (the rows
     of the tokens in ``a``).  Rows are independent, so any subset of a
     sequence's tokens may be passed.  Returns [T, I] float64.
+    q_norm / k_norm: False (none), True or "across" (RMS_NORM_ACROSS_HEADS,
+    gamma [n*d]) or "per_head" (the upstream per-head norm, gamma [d]).
     """
     o = project(a, a_scale, w, w_block_exp, weight_scales, bias)
     q_w = num_heads * head_dim
@@ -103,7 +115,9 @@ def qkv_cte_mx(a, a_scale, w, w_block_exp, *, num_heads: int, num_kv_heads: int,
         segments.append((q_w, q_w + k_w, k_norm, k_gamma))
     for lo, hi, norm, gamma in segments:
         y = o[:, lo:hi]
-        if norm:
+        if norm == "per_head":
+            y = rms_norm_per_head(y, gamma, eps, head_dim)
+        elif norm:
             y = rms_norm_across_heads(y, gamma, eps)
         if fused_rope:
             y = rope_rotate_half(y, cos, sin, head_dim)

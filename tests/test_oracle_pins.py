@@ -727,6 +727,41 @@ def test_kv_variants(check):
     check()
 
 
+def check_per_head_norm():
+    """Per-head qk-norm = torch's rms_norm over each head's d_head slice with the
+    [d_head] gamma; with one head it equals the across-heads norm."""
+    rng = np.random.default_rng(37)
+    T, n, d = 5, 3, 16
+    x = rng.normal(0, 2, (T, n * d))
+    g = rng.uniform(0.5, 1.5, d)
+    got = oq.rms_norm_per_head(x, g, 1e-6, d)
+    exp = F.rms_norm(torch.from_numpy(x.reshape(T, n, d)), (d,), torch.from_numpy(g), 1e-6).numpy().reshape(T, -1)
+    assert_close(got, exp, 1e-12, 1e-12)
+    one = oq.rms_norm_per_head(x[:, :d], g, 1e-6, d)
+    assert_close(one, oq.rms_norm_across_heads(x[:, :d], g, 1e-6), 1e-12, 1e-12)
+
+
+def check_qkv_per_head_segments():
+    """qkv_cte_mx with per-head norms: Q and K each per head, then RoPE; V untouched."""
+    c = synth.make_qkv("ph", 38, S=20, H=256, num_heads=2, num_kv_heads=2, head_dim=64)
+    qg, kg = c.q_gamma[:64], c.k_gamma[:64]
+    got = oq.qkv_cte_mx(c.a, c.a_scale, c.w, c.w_block_exp, num_heads=2, num_kv_heads=2, head_dim=64,
+                        bias=c.bias, q_norm="per_head", k_norm="per_head", q_gamma=qg, k_gamma=kg,
+                        eps=c.eps, fused_rope=True, cos=c.cos, sin=c.sin)
+    o = oq.project(c.a, c.a_scale, c.w, c.w_block_exp, bias=c.bias)
+    ref = o.copy()
+    for lo, g in ((0, qg), (128, kg)):
+        seg = o[:, lo:lo + 128].reshape(20, 2, 64)
+        y = F.rms_norm(torch.from_numpy(seg), (64,), torch.from_numpy(g.astype(np.float64)), c.eps).numpy()
+        ref[:, lo:lo + 128] = oq.rope_rotate_half(y.reshape(20, 128), c.cos, c.sin, 64)
+    assert_close(got, ref, 1e-12, 1e-12)
+
+
+@pytest.mark.parametrize("check", [check_per_head_norm, check_qkv_per_head_segments])
+def test_per_head(check):
+    check()
+
+
 # ---------------------------------------------------------------------------
 # planted mistakes: every mutant must be caught by at least one check
 # ---------------------------------------------------------------------------
@@ -739,7 +774,8 @@ ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_blo
               check_row_quant_hand, check_row_quant_zero_row, check_row_quant_roundtrip,
               check_row_quant_packed, check_nbsd_layout, check_fp8_encoders_vs_torch,
               check_kv_norm_mode, check_kv_norm_v1_no_outputs, check_kv_blk_mode,
-              check_kv_rope_broadcast, check_kv_fp16_inputs, check_kv_fp8_caches]
+              check_kv_rope_broadcast, check_kv_fp16_inputs, check_kv_fp8_caches,
+              check_per_head_norm, check_qkv_per_head_segments]
 
 
 def mutants():
@@ -836,7 +872,12 @@ def mutants():
         top = 448.0 if fmt == "e4m3" else 57344.0
         return np.where(np.abs(np.asarray(v, np.float64)) > top, (c & 0x80) | 0x7F, c).astype(np.uint8)
 
-    return [(okv, "token_slots", slots_blk_per_token), (okv, "cache_rows", rows_norm_ignores_batch),
+    orig_ph = oq.rms_norm_per_head
+
+    def ph_over_all_heads(x, g, eps, d):          # per-head norm taken over the whole segment
+        return oq.rms_norm_across_heads(x, np.tile(g, x.shape[1] // d), eps)
+
+    return [(oq, "rms_norm_per_head", ph_over_all_heads), (okv, "token_slots", slots_blk_per_token), (okv, "cache_rows", rows_norm_ignores_batch),
             (codes, "encode_fp8", fp8_no_saturation),
             (orq, "encode_e4m3_rne_sat", enc_half_away), (orq, "encode_e4m3_rne_sat", enc_no_saturation),
             (orq, "row_quantize", rq_fnuz_range),
