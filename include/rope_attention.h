@@ -75,8 +75,14 @@ int32_t ra_abi_version(void);
  * (a) qkv_cte_mx
  * ======================================================================== */
 
-/* Norm selector, after NormType in the page's "Interface" (qk_norm_pre_rope). */
-enum { RA_NORM_NONE = 0, RA_NORM_RMS_ACROSS_HEADS = 1 };
+/* Norm selector, after NormType in the page's "Interface" (qk_norm_pre_rope).
+ * RMS_ACROSS_HEADS: one RMS per token over the whole segment (Design 1), gamma
+ *   [n * head_dim]; applied by the second pass.
+ * RMS_PER_HEAD: the upstream qk-norm (Design 1: each head's slice by its own RMS),
+ *   gamma [head_dim] shared by the heads; a head fits in one projection tile, so
+ *   this norm and the segment's RoPE are applied in the projection epilogue and
+ *   the second pass leaves the segment alone.  Built for head_dim 64 and 128. */
+enum { RA_NORM_NONE = 0, RA_NORM_RMS_ACROSS_HEADS = 1, RA_NORM_RMS_PER_HEAD = 2 };
 /* Output layout, after QKVOutputLayout ("Interface", output_layout). */
 enum { RA_LAYOUT_BSD = 0, RA_LAYOUT_NBSD = 1 };
 
@@ -127,8 +133,9 @@ ra_status qkv_cte_mx_workspace_bytes(const qkv_cte_mx_params* p, size_t* bytes);
  *   bias          [I] bf16, or NULL.
  *   cos_cache, sin_cache  [B, S, head_dim] fp32 rotate-half tables (lanes j and
  *                 j + head_dim/2 pair up); required iff fused_rope.
- *   q_gamma       [num_heads*head_dim] fp32 segment-wide gamma; required iff q_norm.
- *   k_gamma       [num_kv_heads*head_dim] fp32; required iff k_norm.
+ *   q_gamma       [num_heads*head_dim] fp32 segment-wide gamma (RMS_ACROSS_HEADS) or
+ *                 [head_dim] (RMS_PER_HEAD); required iff q_norm.
+ *   k_gamma       likewise for the K segment; required iff k_norm.
  *   out           [T, I] bf16 (BSD), 16-byte aligned.  Q|K|V along the last dim.
  *   workspace     caller-owned, >= qkv_cte_mx_workspace_bytes, 16-byte aligned.
  * Errors: validation codes above; RA_ERR_CUDA on launch failure.  A device
@@ -150,11 +157,14 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
  * until qkv_cte_mx_norm_rope runs: fp16 of O * gamma * 2^-e with a power-of-two
  * e per (token, 128-column block) kept in the workspace, so the intermediate
  * carries 11 significant bits and the only bf16 rounding of Q and K is the
- * final one.  Arguments as for qkv_cte_mx. */
+ * final one.  Segments with the per-head norm are finished here: normed, rotated
+ * when fused_rope (cos_cache / sin_cache are then required; otherwise they may
+ * be NULL) and stored as bf16.  Arguments as for qkv_cte_mx. */
 ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
-                             const float* q_gamma, const float* k_gamma, uint16_t* out,
-                             void* workspace, size_t workspace_bytes, void* stream);
+                             const float* cos_cache, const float* sin_cache, const float* q_gamma,
+                             const float* k_gamma, uint16_t* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /* Second half on its own (Design 1b, Design 2): reduces the sums of squares
  * left in `workspace` by qkv_cte_mx_project for the same `out` into inv_rms per

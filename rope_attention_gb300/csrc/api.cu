@@ -61,11 +61,19 @@ struct QkvShape {
   int32_t q_end, k_end;
   int32_t n_part_tiles;
   int32_t s_begin, s_end;   // Q/K columns carried as scaled fp16 between the passes
+  int32_t ph_begin, ph_end; // Q/K columns finished in the projection (per-head norm)
   int32_t n_exp_blocks;     // 128-column blocks covering [0, s_end)
   int32_t part_stride, exp_stride;  // token-major row strides (16-byte multiples)
   size_t exps_offset;
   size_t workspace;
 };
+
+// which segments the norm/RoPE pass rewrites
+void second_pass_segments(const qkv_cte_mx_params* p, bool* do_q, bool* do_k) {
+  *do_q = p->q_norm == RA_NORM_RMS_ACROSS_HEADS || (p->q_norm == RA_NORM_NONE && p->fused_rope);
+  *do_k = p->num_kv_heads > 0 &&
+          (p->k_norm == RA_NORM_RMS_ACROSS_HEADS || (p->k_norm == RA_NORM_NONE && p->fused_rope));
+}
 
 ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   if (p == nullptr) return fail(RA_ERR_INVALID_ARG, "params is NULL");
@@ -77,10 +85,13 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   if (p->num_kv_heads < 0) return fail(RA_ERR_INVALID_ARG, "num_kv_heads must be >= 0");
   if (p->head_dim < 16 || p->head_dim % 16 != 0)
     return fail(RA_ERR_INVALID_ARG, "head_dim must be a positive multiple of 16");
-  if (p->q_norm != RA_NORM_NONE && p->q_norm != RA_NORM_RMS_ACROSS_HEADS)
-    return fail(RA_ERR_INVALID_ARG, "q_norm must be RA_NORM_NONE or RA_NORM_RMS_ACROSS_HEADS");
-  if (p->k_norm != RA_NORM_NONE && p->k_norm != RA_NORM_RMS_ACROSS_HEADS)
-    return fail(RA_ERR_INVALID_ARG, "k_norm must be RA_NORM_NONE or RA_NORM_RMS_ACROSS_HEADS");
+  if (p->q_norm != RA_NORM_NONE && p->q_norm != RA_NORM_RMS_ACROSS_HEADS && p->q_norm != RA_NORM_RMS_PER_HEAD)
+    return fail(RA_ERR_INVALID_ARG, "q_norm must be an RA_NORM_* value");
+  if (p->k_norm != RA_NORM_NONE && p->k_norm != RA_NORM_RMS_ACROSS_HEADS && p->k_norm != RA_NORM_RMS_PER_HEAD)
+    return fail(RA_ERR_INVALID_ARG, "k_norm must be an RA_NORM_* value");
+  if ((p->q_norm == RA_NORM_RMS_PER_HEAD || p->k_norm == RA_NORM_RMS_PER_HEAD) &&
+      p->head_dim != 64 && p->head_dim != 128)
+    return fail(RA_ERR_UNSUPPORTED, "the per-head norm is built for head_dim 64 and 128");
   if (p->k_norm != RA_NORM_NONE && p->num_kv_heads == 0)
     return fail(RA_ERR_INVALID_ARG, "k_norm needs a K segment (num_kv_heads == 0)");
   if (p->fused_rope != 0 && p->fused_rope != 1) return fail(RA_ERR_INVALID_ARG, "fused_rope must be 0 or 1");
@@ -99,15 +110,23 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   s->k_w = p->num_kv_heads * p->head_dim;
   s->q_end = s->q_w;
   s->k_end = s->q_w + s->k_w;
-  const bool any_norm = p->q_norm != RA_NORM_NONE || p->k_norm != RA_NORM_NONE;
-  const int32_t normed_end = p->k_norm != RA_NORM_NONE ? s->k_end : s->q_end;
-  s->n_part_tiles = any_norm ? (normed_end + ra::kPartCols - 1) / ra::kPartCols : 0;
-  // segments the second pass rewrites stay in fp32 between the passes
-  const bool do_q = p->q_norm != RA_NORM_NONE || p->fused_rope;
-  const bool do_k = p->num_kv_heads > 0 && (p->k_norm != RA_NORM_NONE || p->fused_rope);
+  const bool q_across = p->q_norm == RA_NORM_RMS_ACROSS_HEADS;
+  const bool k_across = p->k_norm == RA_NORM_RMS_ACROSS_HEADS;
+  const int32_t across_end = k_across ? s->k_end : (q_across ? s->q_end : 0);
+  s->n_part_tiles = (q_across || k_across) ? (across_end + ra::kPartCols - 1) / ra::kPartCols : 0;
+  // segments the second pass rewrites (across-heads norm, or RoPE without a norm) are
+  // carried as scaled fp16 between the passes; per-head segments are finished in the
+  // projection
+  bool do_q, do_k;
+  second_pass_segments(p, &do_q, &do_k);
   s->s_begin = do_q ? 0 : s->q_w;
-  s->s_end = do_k ? s->k_end : (do_q ? s->q_w : s->q_w);
+  s->s_end = do_k ? s->k_end : s->q_w;
   if (!do_q && !do_k) s->s_begin = s->s_end = 0;
+  const bool q_ph = p->q_norm == RA_NORM_RMS_PER_HEAD;
+  const bool k_ph = p->num_kv_heads > 0 && p->k_norm == RA_NORM_RMS_PER_HEAD;
+  s->ph_begin = q_ph ? 0 : s->q_w;
+  s->ph_end = k_ph ? s->k_end : s->q_w;
+  if (!q_ph && !k_ph) s->ph_begin = s->ph_end = 0;
   s->n_exp_blocks = (s->s_end + ra::kPartCols - 1) / ra::kPartCols;
   s->part_stride = (s->n_part_tiles + 1) / 2 * 2;
   s->exp_stride = (s->n_exp_blocks + 15) / 16 * 16;
@@ -120,8 +139,9 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
 
 ra_status check_project_args(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
                              const float* a_scale, const void* w_packed, const float* ws,
-                             const uint16_t* bias, const float* qg, const float* kg,
-                             const uint16_t* out, const void* workspace, size_t workspace_bytes) {
+                             const uint16_t* bias, const float* cos, const float* sin,
+                             const float* qg, const float* kg, const uint16_t* out,
+                             const void* workspace, size_t workspace_bytes) {
   if (!a || !a_scale || !w_packed || !out || !workspace)
     return fail(RA_ERR_INVALID_ARG, "a, a_scale, w_packed, out and workspace are required");
   if (!aligned16(a) || !aligned16(out) || !aligned16(w_packed) || !aligned16(workspace))
@@ -132,6 +152,10 @@ ra_status check_project_args(const qkv_cte_mx_params* p, const QkvShape& s, cons
   if (p->k_norm && !kg) return fail(RA_ERR_INVALID_ARG, "k_norm requires k_gamma");
   if ((qg && !aligned16(qg)) || (kg && !aligned16(kg)))
     return fail(RA_ERR_ALIGNMENT, "gammas must be 16-byte aligned");
+  if (s.ph_end > s.ph_begin && p->fused_rope) {
+    if (!cos || !sin) return fail(RA_ERR_INVALID_ARG, "the per-head norm with fused_rope needs cos/sin in the projection");
+    if (!aligned16(cos) || !aligned16(sin)) return fail(RA_ERR_ALIGNMENT, "cos/sin caches must be 16-byte aligned");
+  }
   if (workspace_bytes < s.workspace)
     return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
   return RA_OK;
@@ -154,8 +178,8 @@ ra_status check_norm_args(const qkv_cte_mx_params* p, const float* cos, const fl
 
 ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
                       const float* a_scale, const void* w_packed, const float* ws,
-                      const uint16_t* bias, const float* qg, const float* kg, uint16_t* out,
-                      void* workspace, cudaStream_t st) {
+                      const uint16_t* bias, const float* cos, const float* sin, const float* qg,
+                      const float* kg, uint16_t* out, void* workspace, cudaStream_t st) {
   ra::ProjLaunch L{};
   L.a = a;
   L.a_scale = a_scale;
@@ -178,8 +202,18 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
   L.exp_stride = s.exp_stride;
   L.s_begin = s.s_begin;
   L.s_end = s.s_end;
-  L.q_gamma = p->q_norm ? qg : nullptr;
-  L.k_gamma = p->k_norm ? kg : nullptr;
+  // the gamma the epilogue folds in: across-heads segments only (the per-head
+  // segments take theirs in the per-head norm)
+  L.q_gamma = p->q_norm == RA_NORM_RMS_ACROSS_HEADS ? qg : nullptr;
+  L.k_gamma = p->k_norm == RA_NORM_RMS_ACROSS_HEADS ? kg : nullptr;
+  L.ph_begin = s.ph_begin;
+  L.ph_end = s.ph_end;
+  L.ph_q_gamma = p->q_norm == RA_NORM_RMS_PER_HEAD ? qg : nullptr;
+  L.ph_k_gamma = p->k_norm == RA_NORM_RMS_PER_HEAD ? kg : nullptr;
+  L.ph_rope = p->fused_rope;
+  L.cos = cos;
+  L.sin = sin;
+  L.eps = p->norm_eps;
   L.wait_ns = g_wait_ns.load();
   L.stall_loads = g_stall_next.exchange(0);
   L.head_dim = p->head_dim;
@@ -192,8 +226,8 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
 
 ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const float* cos,
                         const float* sin, uint16_t* out, void* workspace, cudaStream_t st) {
-  const bool do_q = p->q_norm || p->fused_rope;
-  const bool do_k = p->num_kv_heads > 0 && (p->k_norm || p->fused_rope);
+  bool do_q, do_k;
+  second_pass_segments(p, &do_q, &do_k);
   if (!do_q && !do_k) return RA_OK;
   ra::NormRopeLaunch L{};
   L.out = out;
@@ -206,9 +240,11 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
   L.head_dim = p->head_dim;
   L.num_q_heads = p->num_heads;
   L.num_k_heads = p->num_kv_heads;
-  L.q_norm = p->q_norm != RA_NORM_NONE;
-  L.k_norm = p->k_norm != RA_NORM_NONE;
+  L.q_norm = p->q_norm == RA_NORM_RMS_ACROSS_HEADS;
+  L.k_norm = p->k_norm == RA_NORM_RMS_ACROSS_HEADS;
   L.rope = p->fused_rope;
+  L.do_q = do_q;
+  L.do_k = do_k;
   L.n_part_tiles = s.n_part_tiles;
   L.exps = reinterpret_cast<const int8_t*>(static_cast<const uint8_t*>(workspace) + s.exps_offset);
   L.part_stride = s.part_stride;
@@ -233,7 +269,7 @@ extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 3; }
+int32_t ra_abi_version(void) { return 4; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
@@ -273,16 +309,17 @@ ra_status qkv_cte_mx_workspace_bytes(const qkv_cte_mx_params* p, size_t* bytes) 
 
 ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
-                             const float* q_gamma, const float* k_gamma, uint16_t* out,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+                             const float* cos_cache, const float* sin_cache, const float* q_gamma,
+                             const float* k_gamma, uint16_t* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
   QkvShape s;
   ra_status st = check_params(p, &s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
-                          workspace, workspace_bytes);
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache,
+                          q_gamma, k_gamma, out, workspace, workspace_bytes);
   if (st != RA_OK) return st;
-  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out, workspace,
-                   static_cast<cudaStream_t>(stream));
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache, q_gamma,
+                   k_gamma, out, workspace, static_cast<cudaStream_t>(stream));
   return st == RA_OK ? ok() : st;
 }
 
@@ -306,14 +343,14 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
   QkvShape s;
   ra_status st = check_params(p, &s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
-                          workspace, workspace_bytes);
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache,
+                          q_gamma, k_gamma, out, workspace, workspace_bytes);
   if (st != RA_OK) return st;
   st = check_norm_args(p, cos_cache, sin_cache, out, workspace, workspace_bytes, s);
   if (st != RA_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out, workspace,
-                   cs);
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache, q_gamma,
+                   k_gamma, out, workspace, cs);
   if (st != RA_OK) return st;
   st = run_norm_rope(p, s, cos_cache, sin_cache, out, workspace, cs);
   return st == RA_OK ? ok() : st;

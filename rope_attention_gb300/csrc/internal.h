@@ -41,6 +41,14 @@ struct ProjLaunch {
   int32_t stall_loads;         // test hook: issue no TMA loads, so the pipeline waits run out
   int32_t head_dim;
   int32_t nbsd;                // out is [I / head_dim, T, head_dim] instead of [T, I]
+  // columns [ph_begin, ph_end) take the per-head norm (and RoPE) in the epilogue
+  int32_t ph_begin, ph_end;
+  const float* ph_q_gamma;     // [head_dim] per-head gamma of the Q / K segment, or null
+  const float* ph_k_gamma;
+  int32_t ph_rope;
+  const float* cos;            // [T, head_dim] fp32 rotate-half tables (per-head RoPE)
+  const float* sin;
+  float eps;
 };
 cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why);
 
@@ -63,6 +71,7 @@ struct NormRopeLaunch {
   int32_t n_exp_blocks, exp_stride;
   float eps;
   int32_t nbsd;                // out is [I / head_dim, T, head_dim] instead of [T, I]
+  int32_t do_q, do_k;          // segments this pass rewrites
 };
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);
 

@@ -63,8 +63,8 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
   const int ntok = static_cast<int>(p.T - t0 < kTok ? p.T - t0 : kTok);
   const int d = p.head_dim, half = d / 2;
   const int nq = p.num_q_heads, nk = p.num_k_heads;
-  const bool do_q = p.q_norm || p.rope;
-  const bool do_k = nk > 0 && (p.k_norm || p.rope);
+  const bool do_q = p.do_q != 0;
+  const bool do_k = nk > 0 && p.do_k != 0;
   const int h_begin = do_q ? 0 : nq;
   const int h_end = do_k ? nq + nk : nq;
   const int q_end = nq * d;

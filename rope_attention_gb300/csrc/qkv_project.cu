@@ -110,6 +110,12 @@ struct Params {
   uint64_t wait_ns;
   int32_t stall_loads;
   int32_t head_dim, nbsd;
+  int32_t ph_begin, ph_end, ph_rope;
+  const float* ph_q_gamma;
+  const float* ph_k_gamma;
+  const float* cos;
+  const float* sin;
+  float eps;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_tile) {
@@ -178,6 +184,64 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
+// One (lo, hi) pair of 16-column chunks of a head for the per-head norm (qkv_cte
+// page, Design 1: the upstream qk-norm, each head's slice by its own RMS, with a
+// [head_dim] gamma) and then the rotate-half RoPE (Design 2): columns j of the lo
+// chunk pair with j + D/2 of the hi chunk.  r holds v (after dequant and bias);
+// the pair is normed, rotated and stored as bf16.
+template <int D>
+__device__ __forceinline__ void per_head_pair(uint32_t (&r)[EPI_COLS], int lo_c, int hi_c, int jc, float inv,
+                                              const float* g, bool rope, int row, const Params& p,
+                                              uint16_t* dst_lo, uint16_t* dst_hi) {
+  const float2 inv2 = make_float2(inv, inv);
+  // two halves of 8 columns each, so that few values are live beside the accumulator
+#pragma unroll
+  for (int half8 = 0; half8 < 2; ++half8) {
+    asm volatile("" ::: "memory");  // keep this half's side loads from being hoisted
+    const int j = jc + 8 * half8;
+    float2 y_lo[4], y_hi[4];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float4 gl = __ldg(reinterpret_cast<const float4*>(g + j) + q);
+      const float4 gh = __ldg(reinterpret_cast<const float4*>(g + j + D / 2) + q);
+      const int k = 8 * half8 + 4 * q;
+      y_lo[2 * q] = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(r[lo_c * 16 + k]), __uint_as_float(r[lo_c * 16 + k + 1])), inv2), make_float2(gl.x, gl.y));
+      y_lo[2 * q + 1] = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(r[lo_c * 16 + k + 2]), __uint_as_float(r[lo_c * 16 + k + 3])), inv2), make_float2(gl.z, gl.w));
+      y_hi[2 * q] = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(r[hi_c * 16 + k]), __uint_as_float(r[hi_c * 16 + k + 1])), inv2), make_float2(gh.x, gh.y));
+      y_hi[2 * q + 1] = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(r[hi_c * 16 + k + 2]), __uint_as_float(r[hi_c * 16 + k + 3])), inv2), make_float2(gh.z, gh.w));
+    }
+    if (rope) {
+      // lo' = lo cos_j - hi sin_j ; hi' = hi cos_{j+D/2} + lo sin_{j+D/2}
+      const float4* cs = reinterpret_cast<const float4*>(p.cos + static_cast<size_t>(row) * D + j);
+      const float4* sn = reinterpret_cast<const float4*>(p.sin + static_cast<size_t>(row) * D + j);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float4 cl = __ldg(cs + q), ch = __ldg(cs + D / 8 + q);
+        const float4 sl = __ldg(sn + q), sh = __ldg(sn + D / 8 + q);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float2 c_lo = h ? make_float2(cl.z, cl.w) : make_float2(cl.x, cl.y);
+          const float2 c_hi = h ? make_float2(ch.z, ch.w) : make_float2(ch.x, ch.y);
+          const float2 s_lo = h ? make_float2(-sl.z, -sl.w) : make_float2(-sl.x, -sl.y);
+          const float2 s_hi = h ? make_float2(sh.z, sh.w) : make_float2(sh.x, sh.y);
+          const float2 lo = y_lo[2 * q + h], hi = y_hi[2 * q + h];
+          y_lo[2 * q + h] = __ffma2_rn(lo, c_lo, __fmul2_rn(hi, s_lo));
+          y_hi[2 * q + h] = __ffma2_rn(hi, c_hi, __fmul2_rn(lo, s_hi));
+        }
+      }
+    }
+    reinterpret_cast<uint4*>(dst_lo)[half8] =
+        make_uint4(pack_bf16x2(y_lo[0].x, y_lo[0].y), pack_bf16x2(y_lo[1].x, y_lo[1].y),
+                   pack_bf16x2(y_lo[2].x, y_lo[2].y), pack_bf16x2(y_lo[3].x, y_lo[3].y));
+    reinterpret_cast<uint4*>(dst_hi)[half8] =
+        make_uint4(pack_bf16x2(y_hi[0].x, y_hi[0].y), pack_bf16x2(y_hi[1].x, y_hi[1].y),
+                   pack_bf16x2(y_hi[2].x, y_hi[2].y), pack_bf16x2(y_hi[3].x, y_hi[3].y));
+  }
+}
+
+// PHD: head_dim of the per-head norm path built into the epilogue, 0 for none (a
+// separate instantiation, so the across-heads kernel keeps its register allocation)
+template <int PHD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     qkv_project_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -358,6 +422,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const size_t orow = static_cast<size_t>(row_ok ? row : 0);
       uint16_t* out_row = p.out + orow * p.I;
       const int col_base = nt * BN + chalf * EPI_COLS;
+      float ph_ss[PHD > 0 ? EPI_COLS / PHD : 1];  // per-head sums of v^2 (per-head norm)
+#pragma unroll
+      for (int h = 0; h < (PHD > 0 ? EPI_COLS / PHD : 1); ++h) ph_ss[h] = 0.f;
       // pass 1: dequant, channel scale and bias in place (packed fp32x2 arithmetic);
       // sums of squares of v, before gamma
       const float2 as2 = make_float2(as, as);
@@ -403,9 +470,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             sq2 = __ffma2_rn(v, v, sq2);
           }
         }
+        if constexpr (PHD > 0) ph_ss[c / (PHD / 16)] += sq2.x + sq2.y;
         if (col0 < p.q_end) ssq += sq2.x + sq2.y;
         else if (col0 < p.k_end) ssk += sq2.x + sq2.y;
       }
+      // segments with the per-head norm are finished here
       // the segment-wide gamma of the normed segments, on the columns the second
       // pass rewrites (inv_rms is one scalar per token and segment, and RoPE is
       // linear, so scaling by gamma here is exact: rot(v * inv * gamma) = inv * rot(v * gamma)),
@@ -444,6 +513,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int col0 = col_base + c * 16;
         if (col0 >= p.I) break;
         if (!row_ok) continue;
+        // BSD: [T, I]; NBSd: [I / head_dim, T, head_dim] (a 16-column chunk never crosses a head)
+        auto out_at = [&](int col) {
+          return p.nbsd ? p.out + (static_cast<size_t>(col / p.head_dim) * p.T + orow) * p.head_dim + col % p.head_dim
+                        : out_row + col;
+        };
+        if constexpr (PHD > 0) {
+          // per-head segments: each (lo, hi) chunk pair of a head is normed, rotated and
+          // stored when its lo chunk comes up
+          const int hh = c / (PHD / 16), cin = c % (PHD / 16);
+          const int h0 = col_base + hh * PHD;
+          if (h0 >= p.ph_begin && h0 < p.ph_end) {
+            if (cin < PHD / 32) {
+              const float inv = rsqrtf(ph_ss[hh] * (1.f / PHD) + p.eps);
+              const float* g = h0 < p.q_end ? p.ph_q_gamma : p.ph_k_gamma;
+              per_head_pair<PHD>(r, c, c + PHD / 32, cin * 16, inv, g, p.ph_rope != 0, row, p, out_at(col0),
+                                 out_at(col0 + PHD / 2));
+            }
+            continue;
+          }
+        }
         uint32_t o[8];
         if (col0 >= p.s_begin && col0 < p.s_end) {
 #pragma unroll
@@ -456,10 +545,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < 8; ++k)
             o[k] = pack_bf16x2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
         }
-        // BSD: [T, I]; NBSd: [I / head_dim, T, head_dim] (a 16-column chunk never crosses a head)
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.nbsd ? p.out + (static_cast<size_t>(col0 / p.head_dim) * p.T + orow) * p.head_dim + col0 % p.head_dim
-                   : out_row + col0);
+        uint4* dst = reinterpret_cast<uint4*>(out_at(col0));
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
       }
@@ -614,12 +700,21 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.stall_loads = L.stall_loads;
   p.head_dim = L.head_dim;
   p.nbsd = L.nbsd;
+  p.ph_begin = L.ph_begin;
+  p.ph_end = L.ph_end;
+  p.ph_rope = L.ph_rope;
+  p.ph_q_gamma = L.ph_q_gamma;
+  p.ph_k_gamma = L.ph_k_gamma;
+  p.cos = L.cos;
+  p.sin = L.sin;
+  p.eps = L.eps;
 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(qkv_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SMEM_ALLOC);
+    for (auto k : {qkv_project_kernel<0>, qkv_project_kernel<64>, qkv_project_kernel<128>})
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   });
   if (attr_err != cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -627,7 +722,12 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   }
   const int num_tiles = p.num_m * p.num_n;
   const int pairs = std::max(1, std::min(num_tiles, device_sm_count() / 2));
-  qkv_project_kernel<<<2 * pairs, NUM_THREADS, SMEM_ALLOC, stream>>>(p);
+  if (p.ph_end <= p.ph_begin)
+    qkv_project_kernel<0><<<2 * pairs, NUM_THREADS, SMEM_ALLOC, stream>>>(p);
+  else if (p.head_dim == 128)
+    qkv_project_kernel<128><<<2 * pairs, NUM_THREADS, SMEM_ALLOC, stream>>>(p);
+  else
+    qkv_project_kernel<64><<<2 * pairs, NUM_THREADS, SMEM_ALLOC, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -37,8 +37,7 @@ class QkvRun:
         self.params = native.QkvCteMxParams(
             B=c.B, S=c.S, H=c.H, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
             head_dim=c.head_dim,
-            q_norm=native.RA_NORM_RMS_ACROSS_HEADS if c.q_norm else native.RA_NORM_NONE,
-            k_norm=native.RA_NORM_RMS_ACROSS_HEADS if c.k_norm else native.RA_NORM_NONE,
+            q_norm=self.norm_code(c.q_norm), k_norm=self.norm_code(c.k_norm),
             fused_rope=1 if c.fused_rope else 0, norm_eps=c.eps, output_layout=layout)
         self.a = to_dev(c.a, device)
         self.a_scale = to_dev(c.a_scale, device)
@@ -58,6 +57,12 @@ class QkvRun:
         nws = native.qkv_cte_mx_workspace_bytes(self.params)
         self.workspace = torch.zeros(nws, dtype=torch.uint8, device=device)
 
+    @staticmethod
+    def norm_code(norm) -> int:
+        if norm == "per_head":
+            return native.RA_NORM_RMS_PER_HEAD
+        return native.RA_NORM_RMS_ACROSS_HEADS if norm else native.RA_NORM_NONE
+
     def run(self, stream=None) -> None:
         native.qkv_cte_mx(self.params, self.a, self.a_scale, self.w_packed, self.weight_scales,
                           self.bias, self.cos, self.sin, self.q_gamma, self.k_gamma, self.out,
@@ -65,8 +70,8 @@ class QkvRun:
 
     def project(self, stream=None) -> None:
         native.qkv_cte_mx_project(self.params, self.a, self.a_scale, self.w_packed,
-                                  self.weight_scales, self.bias, self.q_gamma, self.k_gamma,
-                                  self.out, self.workspace, stream)
+                                  self.weight_scales, self.bias, self.cos, self.sin, self.q_gamma,
+                                  self.k_gamma, self.out, self.workspace, stream)
 
     def norm_rope(self, stream=None) -> None:
         native.qkv_cte_mx_norm_rope(self.params, self.cos, self.sin, self.out, self.workspace, stream)

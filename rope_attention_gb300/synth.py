@@ -158,13 +158,13 @@ class QKVCase:
     w_block_exp: np.ndarray  # [H/32, I] uint8 ue8m0
     weight_scales: np.ndarray | None  # [I] fp32 or None
     bias: np.ndarray | None  # [I] uint16 (bf16 bits) or None
-    q_norm: bool
-    k_norm: bool
+    q_norm: bool | str      # False, True (across heads) or "per_head"
+    k_norm: bool | str
     fused_rope: bool
     cos: np.ndarray | None   # [T, d] fp32
     sin: np.ndarray | None
-    q_gamma: np.ndarray | None  # [num_heads*d] fp32
-    k_gamma: np.ndarray | None  # [num_kv_heads*d] fp32
+    q_gamma: np.ndarray | None  # [num_heads*d] fp32 ([d] for the per-head norm)
+    k_gamma: np.ndarray | None  # [num_kv_heads*d] fp32 ([d] for the per-head norm)
     eps: float
 
     @property
@@ -182,7 +182,7 @@ class QKVCase:
 
 def make_qkv(name: str, seed: int, S: int, H: int, num_heads: int, num_kv_heads: int,
              head_dim: int, *, B: int = 1, rope: str | None = "1d", grid=None,
-             q_norm: bool = True, k_norm: bool = True, bias: bool = True,
+             q_norm: bool | str = True, k_norm: bool | str = True, bias: bool = True,
              weight_scales: bool = False, eps: float = 1e-6,
              a_std: float = 1.0, w_std: float = 0.02) -> QKVCase:
     T = B * S
@@ -195,8 +195,10 @@ def make_qkv(name: str, seed: int, S: int, H: int, num_heads: int, num_kv_heads:
     del w32
     b = encode_bf16(stream(seed, 2).normal(0.0, 0.01, I).astype(np.float32)) if bias else None
     ws = stream(seed, 3).uniform(0.5, 2.0, I).astype(np.float32) if weight_scales else None
-    qg = stream(seed, 4).uniform(0.5, 1.5, num_heads * head_dim).astype(np.float32) if q_norm else None
-    kg = (stream(seed, 5).uniform(0.5, 1.5, num_kv_heads * head_dim).astype(np.float32)
+    qn = head_dim if q_norm == "per_head" else num_heads * head_dim
+    kn = head_dim if k_norm == "per_head" else num_kv_heads * head_dim
+    qg = stream(seed, 4).uniform(0.5, 1.5, qn).astype(np.float32) if q_norm else None
+    kg = (stream(seed, 5).uniform(0.5, 1.5, kn).astype(np.float32)
           if (k_norm and num_kv_heads > 0) else None)
     cos = sin = None
     if rope == "1d":
@@ -207,7 +209,7 @@ def make_qkv(name: str, seed: int, S: int, H: int, num_heads: int, num_kv_heads:
         c1, s1 = rope_rotate_half_3d(grid, head_dim)
         cos, sin = np.tile(c1, (B, 1)), np.tile(s1, (B, 1))
     return QKVCase(name, B, S, H, num_heads, num_kv_heads, head_dim, a, a_scale, w, w_exp,
-                   ws, b, q_norm, k_norm and num_kv_heads > 0, rope is not None, cos, sin,
+                   ws, b, q_norm, k_norm if num_kv_heads > 0 else False, rope is not None, cos, sin,
                    qg, kg, eps)
 
 

@@ -87,6 +87,38 @@ def test_nbsd_layout(name, kw, split):
     check_qkv(case, as_f64(torch.from_numpy(back).view(torch.bfloat16)), qkv_reference(case), name)
 
 
+PER_HEAD = [
+    ("ph128_rope", dict(S=260, H=512, num_heads=4, num_kv_heads=4, head_dim=128, q_norm="per_head",
+                        k_norm="per_head")),
+    ("ph64_odd_heads", dict(S=333, H=384, num_heads=3, num_kv_heads=1, head_dim=64, q_norm="per_head",
+                            k_norm="per_head")),
+    ("ph_q_across_k", dict(S=200, H=256, num_heads=3, num_kv_heads=2, head_dim=64, q_norm="per_head")),
+    ("across_q_ph_k", dict(S=129, H=256, num_heads=2, num_kv_heads=2, head_dim=128, k_norm="per_head")),
+    ("ph_no_rope", dict(S=150, H=256, num_heads=2, num_kv_heads=2, head_dim=128, q_norm="per_head",
+                        k_norm="per_head", rope=None)),
+    ("ph_q_only_segment", dict(S=100, H=256, num_heads=4, num_kv_heads=0, head_dim=64, q_norm="per_head")),
+]
+
+
+@pytest.mark.parametrize("name,kw", PER_HEAD, ids=[s[0] for s in PER_HEAD])
+def test_per_head_norm(name, kw):
+    """The upstream per-head qk-norm (+ RoPE), finished in the projection epilogue."""
+    case = synth.make_qkv(name, 500 + len(name), **kw)
+    r = run_full(case)
+    check_qkv(case, as_f64(r.out), qkv_reference(case), name)
+    s = run_full(case, split=True)
+    assert torch.equal(r.out.view(torch.int16), s.out.view(torch.int16)), "split != fused"
+
+
+def test_per_head_norm_nbsd():
+    case = synth.make_qkv("ph_nbsd", 77, B=2, S=90, H=256, num_heads=2, num_kv_heads=2, head_dim=128,
+                          q_norm="per_head", k_norm="per_head")
+    r = run_full(case, layout=native.RA_LAYOUT_NBSD)
+    g = r.out.view(torch.int16).cpu().numpy()
+    back = g.transpose(1, 0, 2).reshape(case.T, case.I)
+    check_qkv(case, as_f64(torch.from_numpy(back).view(torch.bfloat16)), qkv_reference(case), "ph_nbsd")
+
+
 def test_split_entry_points_match_fused():
     case = synth.make_qkv("split", 5, S=250, H=256, num_heads=3, num_kv_heads=3, head_dim=64)
     a = run_full(case)
