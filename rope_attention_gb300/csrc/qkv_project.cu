@@ -410,10 +410,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < EPI_COLS / 16; ++c) tmem_ld16(t_base + c * 16, r + c * 16);
       tmem_ld_wait();
-      // the accumulator is in registers: hand TMEM back to the MMA issuer now
+      // the accumulator is in registers: hand TMEM back to the MMA issuer now.  The
+      // TMEM reads have completed (tcgen05.wait::ld), which is all the issuer needs
+      // before it overwrites the accumulator, so the arrive is relaxed: a release
+      // would first wait for this warp's stores of the previous tile to become
+      // visible to the cluster and hold the tensor pipe idle meanwhile (3-5 %).
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acce_leader);
+      if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader);
 
       const int row = mb * PAIR_M + static_cast<int>(rank) * BM + row_in_cta;
       const bool row_ok = row < p.T;
