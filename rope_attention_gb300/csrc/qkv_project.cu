@@ -110,6 +110,7 @@ struct Params {
   uint64_t wait_ns;
   int32_t stall_loads;
   int32_t head_dim, nbsd;
+  int32_t out32;  // out is 32-byte aligned, so every 16-column chunk is (I and head_dim are multiples of 16)
   int32_t ph_begin, ph_end, ph_rope;
   const float* ph_q_gamma;
   const float* ph_k_gamma;
@@ -549,9 +550,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < 8; ++k)
             o[k] = pack_bf16x2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
         }
-        uint4* dst = reinterpret_cast<uint4*>(out_at(col0));
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        uint16_t* dst = out_at(col0);
+        if (p.out32) {  // one 32-byte store (sm_100+): half the store instructions and transactions
+          asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(o[0]), "r"(o[1]),
+                       "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                       : "memory");
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
       }
       const int blk = nt * 2 + chalf;
       if (blk < p.n_exp && row_ok)
@@ -704,6 +711,7 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.stall_loads = L.stall_loads;
   p.head_dim = L.head_dim;
   p.nbsd = L.nbsd;
+  p.out32 = (reinterpret_cast<uintptr_t>(L.out) & 31u) == 0;
   p.ph_begin = L.ph_begin;
   p.ph_end = L.ph_end;
   p.ph_rope = L.ph_rope;

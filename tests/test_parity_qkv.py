@@ -119,6 +119,21 @@ def test_per_head_norm_nbsd():
     check_qkv(case, as_f64(torch.from_numpy(back).view(torch.bfloat16)), qkv_reference(case), "ph_nbsd")
 
 
+def test_output_only_16_byte_aligned():
+    """The epilogue writes 32-byte pieces when `out` is 32-byte aligned and 16-byte
+    pieces otherwise: an `out` that starts 16 bytes into a buffer takes the second
+    path and must give the same bits."""
+    case = synth.make_qkv("align16", 12, S=200, H=256, num_heads=2, num_kv_heads=2, head_dim=64)
+    a = run_full(case)
+    b = runner.QkvRun(case)
+    buf = torch.empty(case.T * case.I + 64, dtype=torch.bfloat16, device="cuda")
+    b.out = buf[8:8 + case.T * case.I].view(case.T, case.I)  # 16 bytes past a 32-byte boundary
+    assert b.out.data_ptr() % 32 == 16
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
 def test_split_entry_points_match_fused():
     case = synth.make_qkv("split", 5, S=250, H=256, num_heads=3, num_kv_heads=3, head_dim=64)
     a = run_full(case)
