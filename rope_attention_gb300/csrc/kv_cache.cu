@@ -24,6 +24,9 @@
 //  * two row groups in registers per lane: one is processed while the next loads;
 //  * the per-channel quantisation scales and offsets (per head in V2) are
 //    staged once per block in shared memory;
+//  * the two common row shapes (V1 576 = 512 + 64, V2 192 / 128 with RoPE on 64)
+//    are compiled in for the paged int8 / 16-bit calls, so that addressing and the
+//    per-chunk tests fold to constants; other shapes read theirs at run time;
 //  * packed fp32x2 arithmetic; int8 codes are rounded with cvt.rni and packed
 //    with saturation by cvt.pack.sat;
 //  * lane j < rope_size/8 of a row owns interleaved pairs 4j..4j+3, whose outputs
@@ -127,6 +130,21 @@ __device__ __forceinline__ void store4(int32_t qt, void* row_base, int ch, float
   }
 }
 
+// Row shapes compiled in for the common calls, so that the per-row addressing and
+// the chunk tests fold to constants (0: every size read at run time).
+template <int SHAPE>
+struct RowShape {
+  static constexpr int dkv = 0, dv = 0, r = 0;
+};
+template <>
+struct RowShape<1> {  // V1, the MLA combined kv: 512 normed + 64 RoPE channels
+  static constexpr int dkv = 576, dv = 512, r = 64;
+};
+template <>
+struct RowShape<2> {  // V2: kv of 192 channels (RoPE on the first 64), v of 128
+  static constexpr int dkv = 192, dv = 128, r = 64;
+};
+
 // Launch constants computed on the host.
 struct KvAux {
   float inv_rms;      // 1 / rms_size
@@ -169,11 +187,12 @@ struct Cursor {
 
 // GEN: the general kernel (Norm and PA_BLK_BNSD modes, S-broadcast cos/sin, FP8
 // caches); without it only PA / PA_BNSD with int8 or 16-bit caches is compiled in.
-template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE>
 struct KvRows {
   const KvLaunch& p;
   KvAux aux;
   int j;
+  int dkv, dv, r;
   int rms, rms_chunks, v_chunks, rope_lanes, half, kw, cw;
   int64_t slots;
   const uint4 (&gam)[CPL];
@@ -181,7 +200,7 @@ struct KvRows {
 
   __device__ __forceinline__ void load(const Cursor& c, bool valid, RowIn<CPL>& in) const {
     const uint4 z = make_uint4(0, 0, 0, 0);
-    const uint16_t* x = p.kv + c.row * p.Dkv;
+    const uint16_t* x = p.kv + c.row * dkv;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int ch = j + LPR * i;
@@ -190,7 +209,7 @@ struct KvRows {
     if (VARIANT == 1)
       in.xr = valid && j < rope_lanes ? __ldcs(reinterpret_cast<const uint4*>(x + rms + 8 * j)) : z;
     if (VARIANT == 2) {
-      const uint16_t* vrow = p.v + c.row * p.Dv;
+      const uint16_t* vrow = p.v + c.row * dv;
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int ch = j + LPR * i;
@@ -200,8 +219,8 @@ struct KvRows {
     if (valid && j < rope_lanes) {
       // cos/sin row: (b, n, s), or (b, n, 0) when they are broadcast over S
       const int64_t rrow = GEN && p.rope_bcast ? static_cast<int64_t>(c.b) * p.N + c.n : c.row;
-      const uint16_t* cs = p.cos + rrow * p.R;
-      const uint16_t* sn = p.sin + rrow * p.R;
+      const uint16_t* cs = p.cos + rrow * r;
+      const uint16_t* sn = p.sin + rrow * r;
       in.c1 = __ldcs(reinterpret_cast<const uint2*>(cs + 4 * j));
       in.c2 = __ldcs(reinterpret_cast<const uint2*>(cs + half + 4 * j));
       in.s1 = __ldcs(reinterpret_cast<const uint2*>(sn + 4 * j));
@@ -357,7 +376,7 @@ size_t quant_table_bytes(const KvLaunch& L, bool qk, bool qv) {
 
 constexpr int kMinBlocks = 3;  // 12 warps per SM: up to 168 registers per thread
 
-template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     kv_rms_norm_rope_cache_kernel(const KvLaunch p, const KvAux aux) {
   extern __shared__ float4 tabs[];
@@ -366,10 +385,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   const int lane = threadIdx.x & 31;
   const int g = lane % RPG, j = lane / RPG;
   const int64_t rows = p.B * p.N * p.S;
-  const int R = p.R;
-  const int rms = VARIANT == 1 ? static_cast<int>(p.Dkv) - R : static_cast<int>(p.Dkv);
-  const int kw = VARIANT == 1 ? R : static_cast<int>(p.Dkv);
-  const int cw = VARIANT == 1 ? rms : static_cast<int>(p.Dv);
+  using Sh = RowShape<SHAPE>;
+  const int R = Sh::r ? Sh::r : p.R;
+  const int dkv = Sh::dkv ? Sh::dkv : static_cast<int>(p.Dkv);
+  const int dv = Sh::dv ? Sh::dv : static_cast<int>(p.Dv);
+  const int rms = VARIANT == 1 ? dkv - R : dkv;
+  const int kw = VARIANT == 1 ? R : dkv;
+  const int cw = VARIANT == 1 ? rms : dv;
   const int heads = VARIANT == 2 ? static_cast<int>(p.N) : 1;
   const int32_t N = static_cast<int32_t>(p.N), S = static_cast<int32_t>(p.S);
 
@@ -391,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   float4* vs = ko + ku;
   float4* vo = vs + vu;
   const int64_t slots = p.mode == kModeNorm ? p.cache_seq : p.block_num * p.block_size;
-  const KvRows<VARIANT, LPR, CPL, F16, GEN> w{p, aux, j, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
+  const KvRows<VARIANT, LPR, CPL, F16, GEN, SHAPE> w{p, aux, j, dkv, dv, R, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
                                          slots, gam, QuantTab{ks, ko}, QuantTab{vs, vo}};
 
   // the lane's load cursor: row r_begin + g, then RPG rows further each step
@@ -458,9 +480,9 @@ unsigned persistent_grid(K kernel, int64_t rows, size_t smem) {
   return static_cast<unsigned>(want < cap ? want : cap);
 }
 
-template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE>
 cudaError_t launch_one(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
-  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL, F16, GEN>;
+  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL, F16, GEN, SHAPE>;
   const size_t smem = quant_table_bytes(L, L.kq != 0, L.vq != 0);
   if (smem > 48 * 1024) {
     const cudaError_t e =
@@ -477,22 +499,41 @@ template <int VARIANT, bool F16, bool GEN>
 cudaError_t launch_layout(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st) {
   if (lpr == 8) {
     switch (cpl) {
-      case 1: return launch_one<VARIANT, 8, 1, F16, GEN>(L, aux, st);
-      case 2: return launch_one<VARIANT, 8, 2, F16, GEN>(L, aux, st);
-      case 3: return launch_one<VARIANT, 8, 3, F16, GEN>(L, aux, st);
-      case 4: return launch_one<VARIANT, 8, 4, F16, GEN>(L, aux, st);
+      case 1: return launch_one<VARIANT, 8, 1, F16, GEN, 0>(L, aux, st);
+      case 2: return launch_one<VARIANT, 8, 2, F16, GEN, 0>(L, aux, st);
+      case 3: return launch_one<VARIANT, 8, 3, F16, GEN, 0>(L, aux, st);
+      case 4: return launch_one<VARIANT, 8, 4, F16, GEN, 0>(L, aux, st);
       default: return cudaErrorInvalidValue;
     }
   }
-  if (lpr == 16) return launch_one<VARIANT, 16, 4, F16, GEN>(L, aux, st);
-  if (lpr == 32) return launch_one<VARIANT, 32, 4, F16, GEN>(L, aux, st);
+  if (lpr == 16) return launch_one<VARIANT, 16, 4, F16, GEN, 0>(L, aux, st);
+  if (lpr == 32) return launch_one<VARIANT, 32, 4, F16, GEN, 0>(L, aux, st);
   return cudaErrorInvalidValue;
+}
+
+// the lean kernel with a fixed row shape, when the call has one of them
+template <int VARIANT, bool F16>
+bool launch_fixed(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st, cudaError_t* err) {
+  if (VARIANT == 1 && L.Dkv == RowShape<1>::dkv && L.R == RowShape<1>::r && lpr == 16 && cpl == 4) {
+    *err = launch_one<VARIANT, 16, 4, F16, false, 1>(L, aux, st);
+    return true;
+  }
+  if (VARIANT == 2 && L.Dkv == RowShape<2>::dkv && L.Dv == RowShape<2>::dv && L.R == RowShape<2>::r &&
+      lpr == 8 && cpl == 3) {
+    *err = launch_one<VARIANT, 8, 3, F16, false, 2>(L, aux, st);
+    return true;
+  }
+  return false;
 }
 
 template <int VARIANT>
 cudaError_t launch_variant(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st) {
   const bool gen = (L.mode != kModePa && L.mode != kModePaBnsd) || L.rope_bcast ||
                    L.kq == kQuantE4m3 || L.kq == kQuantE5m2 || L.vq == kQuantE4m3 || L.vq == kQuantE5m2;
+  cudaError_t err = cudaSuccess;
+  if (!gen && (L.f16 ? launch_fixed<VARIANT, true>(L, aux, lpr, cpl, st, &err)
+                     : launch_fixed<VARIANT, false>(L, aux, lpr, cpl, st, &err)))
+    return err;
   if (L.f16) return gen ? launch_layout<VARIANT, true, true>(L, aux, lpr, cpl, st)
                         : launch_layout<VARIANT, true, false>(L, aux, lpr, cpl, st);
   return gen ? launch_layout<VARIANT, false, true>(L, aux, lpr, cpl, st)
