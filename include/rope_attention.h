@@ -35,7 +35,8 @@
  *    means a CUDA runtime call failed (message carries cudaGetErrorString).
  *  - Device-side conditions (a pipeline wait that ran out of time, an index
  *    out of range) never trap: they are recorded in device memory that the
- *    caller reads after synchronising (qkv_cte_mx_status, dev_error_count).
+ *    caller reads after synchronising (qkv_cte_mx_status,
+ *    kv_rms_norm_rope_cache_status, dev_error_count).
  *  - bf16 values are passed as their 16-bit patterns (uint16_t).
  */
 #ifndef ROPE_ATTENTION_H_
@@ -205,7 +206,8 @@ ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_t* a, const
                              const float* k_gamma, uint16_t* out, void* stream);
 
 /* Test hook: time limit, in nanoseconds, of each device pipeline wait in the
- * projection kernel (default 2e9).  Values < 1000 are raised to 1000. */
+ * projection kernel and the staged KV cache kernel (default 2e9).  Values < 1000
+ * are raised to 1000. */
 void ra_set_wait_timeout_ns(int64_t ns);
 
 /* Test hook for failure detection.  The next projection launch (qkv_cte_mx or
@@ -305,7 +307,13 @@ typedef struct {
  *               slot lies outside the cache (any negative index other than -1, or
  *               beyond block_num*block_size / cache_seq_len); such tokens are not written.
  * V1 in NORM mode takes no quantisation parameters.
- * All row pointers 16-byte aligned; Dkv, Dv and rope_size multiples of 8. */
+ * All row pointers 16-byte aligned; Dkv, Dv and rope_size multiples of 8.
+ * Calls of the two common row shapes (V1 Dkv 576 with rope_size 64; V2 Dkv 192,
+ * Dv 128, rope_size 64) in PA / PA_BNSD mode with int8 or 16-bit caches and
+ * per-token cos/sin run a pipelined kernel whose waits have a time limit; a
+ * wait that runs out is reported by kv_rms_norm_rope_cache_status.  The first
+ * call on each device looks up that status word (cudaGetSymbolAddress); make
+ * it before any stream capture. */
 ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const uint16_t* kv,
                                  const uint16_t* gamma, const uint16_t* cos, const uint16_t* sin,
                                  const int64_t* index, void* k_cache, void* ckv_cache,
@@ -313,6 +321,21 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
                                  const float* k_rope_offset, const float* c_kv_offset,
                                  const uint16_t* v_optional, uint16_t* k_rope, uint16_t* c_kv,
                                  int32_t* dev_error_count, void* stream);
+
+/* Synchronises `stream`, reads this library's KV status word on the current
+ * device, clears it, and stores it in *device_status (0 = fine).  Returns
+ * RA_ERR_TIMEOUT if a pipeline wait of kv_rms_norm_rope_cache gave up since the
+ * last read (that call's caches and outputs are then undefined), else RA_OK.
+ * The word is shared by every call on the device. */
+ra_status kv_rms_norm_rope_cache_status(void* stream, int32_t* device_status);
+
+/* Test hook for failure detection.  The next kv_rms_norm_rope_cache call that
+ * runs the pipelined kernel (see above) issues none of its copies, so its waits
+ * run out after the time limit of ra_set_wait_timeout_ns; every block records
+ * the timeout in the status word and exits, and kv_rms_norm_rope_cache_status
+ * reports RA_ERR_TIMEOUT.  Nothing is in flight when the waits give up.  The
+ * caches of that call are undefined.  Applies to one call, then clears itself. */
+void ra_test_stall_next_kv_cache(void);
 
 #ifdef __cplusplus
 }

@@ -32,6 +32,7 @@ namespace {
 thread_local std::string g_last_error;
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_stall_next{0};  // ra_test_stall_next_projection
+std::atomic<int> g_stall_next_kv{0};  // ra_test_stall_next_kv_cache
 
 ra_status fail(ra_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ra_status fail(ra_status code, const char* fmt, ...) {
@@ -269,11 +270,13 @@ extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 4; }
+int32_t ra_abi_version(void) { return 5; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
 void ra_test_stall_next_projection(void) { g_stall_next.store(1); }
+
+void ra_test_stall_next_kv_cache(void) { g_stall_next_kv.store(1); }
 
 ra_status qkv_cte_mx_packed_weight_bytes(int64_t H, int64_t I, size_t* bytes) {
   if (!bytes) return fail(RA_ERR_INVALID_ARG, "bytes is NULL");
@@ -511,8 +514,27 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
   L.vq = vq;
   L.rope_bcast = p->rope_s_broadcast;
   L.cache_seq = mode == RA_CACHE_NORM ? p->cache_seq_len : 0;
+  L.wait_ns = g_wait_ns.load();
+  L.stall_loads = g_stall_next_kv.exchange(0);
+  L.status = ra::kv_status_word();
   cudaError_t e = ra::launch_kv_rms_norm_rope_cache(L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_rms_norm_rope_cache launch");
+  return ok();
+}
+
+ra_status kv_rms_norm_rope_cache_status(void* stream, int32_t* device_status) {
+  if (!device_status) return fail(RA_ERR_INVALID_ARG, "device_status is required");
+  int32_t* word = ra::kv_status_word();
+  if (!word) return fail(RA_ERR_CUDA, "the KV status word cannot be found on this device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(word, 0, sizeof(v), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "KV status read");
+  *device_status = v;
+  if (v != 0) return fail(RA_ERR_TIMEOUT, "a KV cache pipeline wait ran out of time (status %d)", v);
   return ok();
 }
 

@@ -34,6 +34,8 @@
 //    Cache rows are contiguous, so each scattered slot is written with whole vectors.
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "kv_cache.h"
 #include "ptx.cuh"
@@ -187,7 +189,8 @@ struct Cursor {
 
 // GEN: the general kernel (Norm and PA_BLK_BNSD modes, S-broadcast cos/sin, FP8
 // caches); without it only PA / PA_BNSD with int8 or 16-bit caches is compiled in.
-template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE>
+// JLO: lane = g * LPR + j (a row's lanes adjacent), else lane = j * (32 / LPR) + g.
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE, bool JLO = false>
 struct KvRows {
   const KvLaunch& p;
   KvAux aux;
@@ -250,8 +253,13 @@ struct KvRows {
       for (int k = 0; k < 4; ++k) acc = __ffma2_rn(y[i][k], y[i][k], acc);
     }
     float ss = acc.x + acc.y;
+    if constexpr (JLO) {
 #pragma unroll
-    for (int o = 16; o >= 32 / LPR; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    } else {
+#pragma unroll
+      for (int o = 16; o >= 32 / LPR; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    }
     const float inv = rsqrtf(fmaf(ss, aux.inv_rms, p.eps));
     const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
@@ -468,6 +476,243 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   }
 }
 
+// ---------------------------------------------------------------- staged kernel
+// For the two common row shapes on the paged int8 / 16-bit path.  A tile of
+// kTileRows consecutive (b, n, s) rows is one contiguous span in each of kv, v,
+// cos and sin, so one lane of a producer warp moves it into shared memory with
+// four bulk copies (cp.async.bulk, completion counted by the stage's mbarrier),
+// kStages - 1 tiles ahead of four consumer warps.  The producer warp also looks up
+// each row's head and cache slot.  The consumers run the same row arithmetic as
+// the kernel above on operands read from shared memory, with a row's lanes
+// adjacent so that those reads are free of bank conflicts.  Every wait has a time
+// limit: when one runs out the block records it in the status word and leaves,
+// the producer first waiting (with a limit) for the copies it issued.
+constexpr int kTileRows = 16;
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kStagedThreads = (kConsumerWarps + 1) * 32;
+static_assert(kTileRows <= 32, "one producer lane per tile row");
+
+__device__ int32_t g_kv_status;
+
+// Shared-memory plan of the staged kernel, in bytes from the dynamic base.
+struct StagedPlan {
+  uint32_t tables, stage_bytes, stages, slots, heads, bars, flag, total;
+};
+__host__ __device__ inline StagedPlan staged_plan(uint32_t table_bytes, uint32_t stage_bytes) {
+  StagedPlan pl;
+  pl.tables = 0;
+  pl.stage_bytes = stage_bytes;
+  pl.stages = (table_bytes + 127u) & ~127u;
+  pl.slots = pl.stages + kStages * stage_bytes;
+  pl.heads = pl.slots + kStages * kTileRows * 8;
+  pl.bars = pl.heads + kStages * kTileRows * 4;
+  pl.flag = pl.bars + 2 * kStages * 8;
+  pl.total = pl.flag + 16;
+  return pl;
+}
+
+template <int VARIANT>
+struct StagedShape {
+  using Sh = RowShape<VARIANT>;
+  static constexpr int R = Sh::r, DKV = Sh::dkv, DV = VARIANT == 2 ? Sh::dv : 0;
+  static constexpr int RMS = VARIANT == 1 ? DKV - R : DKV;
+  static constexpr int KW = VARIANT == 1 ? R : DKV, CW = VARIANT == 1 ? RMS : Sh::dv;
+  static constexpr int LPR = VARIANT == 1 ? 16 : 8, CPL = VARIANT == 1 ? 4 : 3, RPG = 32 / LPR;
+  static constexpr uint32_t KV_B = kTileRows * DKV * 2, V_B = kTileRows * DV * 2, CS_B = kTileRows * R * 2;
+  static constexpr uint32_t STAGE_B = KV_B + V_B + 2 * CS_B;
+  static constexpr uint32_t ROW_B = STAGE_B / kTileRows;
+  static constexpr int STEPS = kTileRows / (kConsumerWarps * RPG);  // row groups per consumer warp and tile
+  static_assert(STEPS * kConsumerWarps * RPG == kTileRows, "tile rows split evenly over the consumer warps");
+  static_assert(RMS / 8 <= LPR * CPL && Sh::dv / 8 <= LPR * CPL && R / 8 <= LPR, "lane layout holds the row");
+};
+
+// warp-collective bounded wait: every lane returns the same answer
+__device__ bool kv_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit, volatile int* abort_flag) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((i & 31u) == 31u) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0) {
+        const uint64_t t = globaltimer_ns();
+        if (t0 == 0) t0 = t;
+        else if (*abort_flag || t - t0 > limit) give_up = 1;
+      }
+      give_up = __shfl_sync(0xffffffffu, give_up, 0);
+      if (give_up) {
+        if ((threadIdx.x & 31) == 0) *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <int VARIANT, bool F16>
+__global__ void __launch_bounds__(kStagedThreads, 3)
+    kv_staged_kernel(const KvLaunch p, const KvAux aux, const uint32_t tiles) {
+  using T = StagedShape<VARIANT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rows = static_cast<uint32_t>(p.B * p.N * p.S);
+  const uint32_t S = static_cast<uint32_t>(p.S), N = static_cast<uint32_t>(p.N);
+  const int heads = VARIANT == 2 ? static_cast<int>(p.N) : 1;
+  const int ku = p.kq ? heads * T::KW / 4 : 0, vu = p.vq ? heads * T::CW / 4 : 0;
+  const StagedPlan pl = staged_plan(static_cast<uint32_t>(2 * (ku + vu) * 16), T::STAGE_B);
+  float4* ks = reinterpret_cast<float4*>(smem);
+  float4* ko = ks + ku;
+  float4* vs = ko + ku;
+  float4* vo = vs + vu;
+  int64_t* slot_s = reinterpret_cast<int64_t*>(smem + pl.slots);
+  int32_t* head_s = reinterpret_cast<int32_t*>(smem + pl.heads);
+  const uint32_t bars = smem_u32(smem + pl.bars);  // full[kStages], then empty[kStages]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pl.flag);
+  const uint32_t stage0 = smem_u32(smem + pl.stages);
+  const uint64_t limit = static_cast<uint64_t>(p.wait_ns);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bars + 8 * s, 32);                           // every producer lane arrives
+      mbar_init(bars + 8 * (kStages + s), kConsumerWarps);   // one arrive per consumer warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = threadIdx.x; u < ku; u += kStagedThreads) {
+    ks[u] = __ldg(reinterpret_cast<const float4*>(p.k_scale) + u);
+    ko[u] = p.k_offset ? __ldg(reinterpret_cast<const float4*>(p.k_offset) + u) : zero4;
+  }
+  for (int u = threadIdx.x; u < vu; u += kStagedThreads) {
+    vs[u] = __ldg(reinterpret_cast<const float4*>(p.v_scale) + u);
+    vo[u] = p.v_offset ? __ldg(reinterpret_cast<const float4*>(p.v_offset) + u) : zero4;
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // producer: tile k of this block goes to stage k % kStages
+    uint32_t k = 0;
+    bool live = true;
+    for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++k) {
+      const uint32_t s = k % kStages, use = k / kStages;
+      if (k >= kStages && !kv_wait_warp(bars + 8 * (kStages + s), (use & 1u) ^ 1u, limit, abort_flag)) {
+        live = false;
+        break;
+      }
+      const uint32_t r0 = tile * kTileRows;
+      const uint32_t nr = rows - r0 < static_cast<uint32_t>(kTileRows) ? rows - r0 : kTileRows;
+      const uint32_t full = bars + 8 * s;
+      if (lane == 0) {  // the copies first, so that the slot lookups below overlap them
+        mbar_expect_tx(full, nr * T::ROW_B);
+        if (!p.stall_loads) {
+          const uint32_t dst = stage0 + s * T::STAGE_B;
+          bulk_load(dst, p.kv + static_cast<size_t>(r0) * T::DKV, nr * T::DKV * 2, full);
+          if (VARIANT == 2) bulk_load(dst + T::KV_B, p.v + static_cast<size_t>(r0) * T::DV, nr * T::DV * 2, full);
+          bulk_load(dst + T::KV_B + T::V_B, p.cos + static_cast<size_t>(r0) * T::R, nr * T::R * 2, full);
+          bulk_load(dst + T::KV_B + T::V_B + T::CS_B, p.sin + static_cast<size_t>(r0) * T::R, nr * T::R * 2, full);
+        }
+      }
+      if (lane < static_cast<int>(nr)) {  // row r0 + lane: its head and its token's cache slot
+        const uint32_t r = r0 + lane;
+        const uint32_t bn = r / S, sq = r - bn * S;
+        const uint32_t b = bn / N;
+        slot_s[s * kTileRows + lane] = __ldg(p.index + static_cast<int64_t>(b) * S + sq);
+        head_s[s * kTileRows + lane] = static_cast<int32_t>(bn - b * N);
+      }
+      mbar_arrive(full);  // each lane releases its own writes above
+    }
+    if (!live && lane == 0) atomicExch(p.status, 1);
+    // leave only when no copy into this block's shared memory can still be in flight
+    if (lane == 0) {
+      for (uint32_t u = k > static_cast<uint32_t>(kStages) ? k - kStages : 0; u < k; ++u) {
+        const uint32_t bar = bars + 8 * (u % kStages), parity = (u / kStages) & 1u;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity)) {
+          if (globaltimer_ns() - t0 > limit) {
+            atomicExch(p.status, 1);
+            break;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // consumers
+  const int g = lane / T::LPR, j = lane % T::LPR;
+  uint4 gam[T::CPL];
+#pragma unroll
+  for (int i = 0; i < T::CPL; ++i) gam[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * (j + T::LPR * i)));
+  const int64_t slots = p.block_num * p.block_size;
+  const KvRows<VARIANT, T::LPR, T::CPL, F16, false, VARIANT, true> w{
+      p, aux, j, T::DKV, T::DV, T::R, T::RMS, T::RMS / 8, VARIANT == 2 ? T::CW / 8 : 0, T::R / 8, T::R / 2,
+      T::KW, T::CW, slots, gam, QuantTab{ks, ko}, QuantTab{vs, vo}};
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  uint32_t k = 0;
+  for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++k) {
+    const uint32_t s = k % kStages, use = k / kStages;
+    if (!kv_wait_warp(bars + 8 * s, use & 1u, limit, abort_flag)) {
+      if (lane == 0) atomicExch(p.status, 1);
+      return;
+    }
+    const uint8_t* st = smem + pl.stages + s * T::STAGE_B;
+    const uint32_t r0 = tile * kTileRows;
+#pragma unroll
+    for (int step = 0; step < T::STEPS; ++step) {
+      const int lr = (warp * T::STEPS + step) * T::RPG + g;  // row within the tile
+      RowIn<T::CPL> in;
+      const uint8_t* x = st + lr * T::DKV * 2;
+#pragma unroll
+      for (int i = 0; i < T::CPL; ++i) in.x[i] = *reinterpret_cast<const uint4*>(x + 16 * (j + T::LPR * i));
+      if (VARIANT == 1) in.xr = j < T::R / 8 ? *reinterpret_cast<const uint4*>(x + 2 * T::RMS + 16 * j) : z;
+      if (VARIANT == 2) {
+        const uint8_t* v = st + T::KV_B + lr * T::DV * 2;
+#pragma unroll
+        for (int i = 0; i < T::CPL; ++i) {
+          const int ch = j + T::LPR * i;
+          in.v[i] = ch < T::DV / 8 ? *reinterpret_cast<const uint4*>(v + 16 * ch) : z;
+        }
+      }
+      if (j < T::R / 8) {
+        const uint8_t* cs = st + T::KV_B + T::V_B + lr * T::R * 2;
+        const uint8_t* sn = cs + T::CS_B;
+        in.c1 = *reinterpret_cast<const uint2*>(cs + 8 * j);
+        in.c2 = *reinterpret_cast<const uint2*>(cs + T::R + 8 * j);
+        in.s1 = *reinterpret_cast<const uint2*>(sn + 8 * j);
+        in.s2 = *reinterpret_cast<const uint2*>(sn + T::R + 8 * j);
+      }
+      in.slot = slot_s[s * kTileRows + lr];
+      in.n = head_s[s * kTileRows + lr];
+      in.aux = 0;
+      const uint32_t row = r0 + lr;
+      w.process(in, row, row < rows);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kStages + s));
+  }
+}
+
+template <int VARIANT, bool F16>
+cudaError_t launch_staged(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
+  using T = StagedShape<VARIANT>;
+  auto kernel = kv_staged_kernel<VARIANT, F16>;
+  const StagedPlan pl = staged_plan(static_cast<uint32_t>(quant_table_bytes(L, L.kq != 0, L.vq != 0)), T::STAGE_B);
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.total));
+  if (e != cudaSuccess) return e;
+  const int64_t rows = L.B * L.N * L.S;
+  const uint32_t tiles = static_cast<uint32_t>((rows + kTileRows - 1) / kTileRows);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStagedThreads, pl.total) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t cap = static_cast<int64_t>(per_sm) * device_sm_count();
+  const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
+  kernel<<<grid, kStagedThreads, pl.total, st>>>(L, aux, tiles);
+  return cudaGetLastError();
+}
+
 // persistent grid: as many blocks as fit on the GPU at once, capped by the row count
 template <typename K>
 unsigned persistent_grid(K kernel, int64_t rows, size_t smem) {
@@ -514,16 +759,17 @@ cudaError_t launch_layout(const KvLaunch& L, const KvAux& aux, int lpr, int cpl,
 // the lean kernel with a fixed row shape, when the call has one of them
 template <int VARIANT, bool F16>
 bool launch_fixed(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st, cudaError_t* err) {
-  if (VARIANT == 1 && L.Dkv == RowShape<1>::dkv && L.R == RowShape<1>::r && lpr == 16 && cpl == 4) {
-    *err = launch_one<VARIANT, 16, 4, F16, false, 1>(L, aux, st);
+  const bool shape = VARIANT == 1 ? L.Dkv == RowShape<1>::dkv && L.R == RowShape<1>::r && lpr == 16 && cpl == 4
+                                   : L.Dkv == RowShape<2>::dkv && L.Dv == RowShape<2>::dv && L.R == RowShape<2>::r &&
+                                         lpr == 8 && cpl == 3;
+  if (!shape) return false;
+  if (L.status != nullptr && L.B * L.N * L.S < (int64_t(1) << 31) - kTileRows) {
+    *err = launch_staged<VARIANT, F16>(L, aux, st);
     return true;
   }
-  if (VARIANT == 2 && L.Dkv == RowShape<2>::dkv && L.Dv == RowShape<2>::dv && L.R == RowShape<2>::r &&
-      lpr == 8 && cpl == 3) {
-    *err = launch_one<VARIANT, 8, 3, F16, false, 2>(L, aux, st);
-    return true;
-  }
-  return false;
+  *err = VARIANT == 1 ? launch_one<VARIANT, 16, 4, F16, false, 1>(L, aux, st)
+                      : launch_one<VARIANT, 8, 3, F16, false, 2>(L, aux, st);
+  return true;
 }
 
 template <int VARIANT>
@@ -541,6 +787,19 @@ cudaError_t launch_variant(const KvLaunch& L, const KvAux& aux, int lpr, int cpl
 }
 
 }  // namespace
+
+int32_t* kv_status_word() {
+  static std::atomic<int32_t*> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+  if (dev < 64) {
+    if (int32_t* q = cache[dev].load()) return q;
+  }
+  void* q = nullptr;
+  if (cudaGetSymbolAddress(&q, g_kv_status) != cudaSuccess) return nullptr;
+  if (dev < 64) cache[dev].store(static_cast<int32_t*>(q));
+  return static_cast<int32_t*>(q);
+}
 
 cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream) {
   const int64_t rms = L.variant == 1 ? L.Dkv - L.R : L.Dkv;

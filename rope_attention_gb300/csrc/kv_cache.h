@@ -27,6 +27,7 @@ struct KvLaunch {
   uint16_t* k_rope;
   uint16_t* c_kv;
   int32_t* err_count;
+  int32_t* status;             // kv_status_word(); the staged kernel runs only when it is known
   int64_t B, N, S, Dkv, Dv;
   int32_t R;                   // rope size
   int32_t variant;             // 1 or 2
@@ -38,7 +39,12 @@ struct KvLaunch {
   int32_t f16;                 // inputs (and unquantised caches, outputs) are fp16
   int32_t kq, vq;              // KvQuant of the k / ckv cache
   int32_t rope_bcast;          // cos/sin are [B, N, 1, R]
+  int64_t wait_ns;             // time limit of each pipeline wait (staged kernel)
+  int32_t stall_loads;         // test hook: the staged kernel issues no copies, so its waits run out
 };
+// Device address of this library's KV status word on the current device (0 = fine,
+// 1 = a pipeline wait of the staged kernel gave up); nullptr if it cannot be found.
+int32_t* kv_status_word();
 cudaError_t launch_kv_rms_norm_rope_cache(const KvLaunch& L, cudaStream_t stream);
 
 }  // namespace ra

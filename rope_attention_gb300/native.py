@@ -28,7 +28,8 @@ RA_CACHE_NORM, RA_CACHE_PA, RA_CACHE_PA_BNSD, RA_CACHE_PA_NZ, RA_CACHE_PA_BLK_BN
 EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns", "ra_test_stall_next_projection",
            "qkv_cte_mx_packed_weight_bytes", "qkv_cte_mx_pack_weight", "qkv_cte_mx_workspace_bytes",
            "qkv_cte_mx", "qkv_cte_mx_project", "qkv_cte_mx_norm_rope", "qkv_cte_mx_status",
-           "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache", "row_quantize_e4m3", "row_quantize_e4m3_packed"]
+           "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache", "kv_rms_norm_rope_cache_status",
+           "ra_test_stall_next_kv_cache", "row_quantize_e4m3", "row_quantize_e4m3_packed"]
 
 
 class RAError(RuntimeError):
@@ -85,6 +86,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qkv_cte_mx_noalloc": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, P, P]),
         "kv_rms_norm_rope_cache": (i32, [ctypes.POINTER(KvRmsNormRopeCacheParams), P, P, P, P, P,
                                          P, P, P, P, P, P, P, P, P, P, P]),
+        "kv_rms_norm_rope_cache_status": (i32, [P, ctypes.POINTER(i32)]),
+        "ra_test_stall_next_kv_cache": (None, []),
         "row_quantize_e4m3": (i32, [P, i64, i64, P, P, P]),
         "row_quantize_e4m3_packed": (i32, [P, i64, i64, P, P]),
     }
@@ -137,6 +140,11 @@ def ra_set_wait_timeout_ns(ns: int) -> None:
 def ra_test_stall_next_projection() -> None:
     """Test hook: the next projection launch issues no loads, so its waits time out."""
     load().ra_test_stall_next_projection()
+
+
+def ra_test_stall_next_kv_cache() -> None:
+    """Test hook: the next pipelined KV cache launch issues no copies, so its waits time out."""
+    load().ra_test_stall_next_kv_cache()
 
 
 # ---------------------------------------------------------------- qkv_cte_mx
@@ -215,6 +223,15 @@ def qkv_cte_mx_status(workspace: torch.Tensor, stream=None) -> int:
 
 
 # ---------------------------------------------------------------- kv_rms_norm_rope_cache
+def kv_rms_norm_rope_cache_status(stream=None) -> int:
+    """Synchronises the stream; returns the KV status word (0 = fine) and clears it."""
+    v = ctypes.c_int32()
+    st = load().kv_rms_norm_rope_cache_status(_stream(stream), ctypes.byref(v))
+    if st not in (RA_OK, -6):
+        _check(st)
+    return v.value
+
+
 def kv_rms_norm_rope_cache(params, kv, gamma, cos, sin, index, k_cache, ckv_cache, k_rope_scale=None,
                            c_kv_scale=None, k_rope_offset=None, c_kv_offset=None, v_optional=None,
                            k_rope=None, c_kv=None, dev_error_count=None, stream=None) -> None:

@@ -38,7 +38,7 @@ def test_exports_every_declared_function(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in the header but not exported"
     assert sorted(names) == sorted(native.EXPORTS)
-    assert native.ra_abi_version() == 4
+    assert native.ra_abi_version() == 5
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -137,6 +137,7 @@ def test_project_and_norm_rejections(L):
     assert st == -1                                          # fused_rope needs cos/sin
     v = ctypes.c_int32()
     assert L.qkv_cte_mx_status(None, None, ctypes.byref(v)) == -1
+    assert L.kv_rms_norm_rope_cache_status(None, None) == -1    # device_status is required
 
 
 def test_pack_weight_rejections(L):
