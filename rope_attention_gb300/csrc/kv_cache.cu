@@ -23,7 +23,7 @@
 //    lookup, addressing, the RMS shuffle tree) are shared;
 //  * two row groups in registers per lane: one is processed while the next loads;
 //  * the per-channel quantisation scales and offsets (per head in V2) are
-//    staged once per block in shared memory;
+//    staged once per block in shared memory, laid out for conflict-free reads;
 //  * the two common row shapes (V1 576 = 512 + 64, V2 192 / 128 with RoPE on 64)
 //    are compiled in for the paged int8 / 16-bit calls, so that addressing and the
 //    per-chunk tests fold to constants; other shapes read theirs at run time;
@@ -95,12 +95,40 @@ __device__ __forceinline__ uint32_t quant4(float2 v01, float2 v23, float4 sc, fl
   return lo | (hi << 16);
 }
 
-// Quantisation tables in shared memory, in units of 4 channels: scale[u] and
-// offset[u] (float4) for channels 4u..4u+3, heads one after another.
+// Quantisation tables in shared memory, in units of 4 channels (a float4 of
+// scales, and one of offsets, for channels 4u..4u+3), heads one after another
+// `stride` apart.  Within a head, group u sits at (u odd ? odd : 0) + (u / 2) * step.
+//  * split layout (step 1, odd = 4 mod 8): a lane that quantises the 8 channels of
+//    chunk c reads positions c and odd + c, one that quantises 4 reads u / 2 or
+//    odd + u / 2, so with the lanes of a quarter warp on consecutive chunks (or
+//    groups) their 16-byte reads land in distinct banks;
+//  * plain layout (step 2, odd 1): group u at u; chunk c reads 2c and 2c + 1, two
+//    lanes of a quarter warp per bank.
+struct TabLayout {
+  int odd, step, stride;  // float4 units
+};
+__host__ __device__ inline TabLayout tab_layout(int width, bool split) {  // width % 8 == 0
+  if (!split) return TabLayout{1, 2, width / 4};
+  const int half = width / 8;  // groups of each parity
+  const int odd = half + (12 - half % 8) % 8;
+  return TabLayout{odd, 1, odd + half};
+}
 struct QuantTab {
   const float4* scale;
   const float4* offset;
+  int odd, step, stride;
 };
+// Fills one table (every head) from the per-channel scale / offset arrays.
+__device__ __forceinline__ void fill_table(float4* ts, float4* to, const float* scale, const float* offset,
+                                           int heads, int width, TabLayout l) {
+  const int groups = width / 4, n = heads * groups;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int hd = e / groups, u = e - hd * groups;
+    const int pos = hd * l.stride + ((u & 1) ? l.odd : 0) + (u >> 1) * l.step;
+    ts[pos] = __ldg(reinterpret_cast<const float4*>(scale) + e);
+    to[pos] = offset ? __ldg(reinterpret_cast<const float4*>(offset) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
 
 // 8 channels starting at `ch` (a multiple of 8) of a cache row: quantised (qt != 0,
 // one byte each) or in the input dtype
@@ -108,10 +136,11 @@ template <bool F16, bool GEN>
 __device__ __forceinline__ void store8(int32_t qt, void* row_base, int ch, const float2 (&v)[4],
                                        QuantTab t) {
   if (qt != kQuantNone) {
-    const int u = ch >> 2;
+    const int c = ch >> 3;
     uint2 w;
-    w.x = quant4<GEN>(v[0], v[1], t.scale[u], t.offset[u], qt);
-    w.y = quant4<GEN>(v[2], v[3], t.scale[u + 1], t.offset[u + 1], qt);
+    const int e = c * t.step;
+    w.x = quant4<GEN>(v[0], v[1], t.scale[e], t.offset[e], qt);
+    w.y = quant4<GEN>(v[2], v[3], t.scale[t.odd + e], t.offset[t.odd + e], qt);
     *reinterpret_cast<uint2*>(static_cast<uint8_t*>(row_base) + ch) = w;
   } else {
     *reinterpret_cast<uint4*>(static_cast<uint16_t*>(row_base) + ch) = pack8<F16>(v);
@@ -122,8 +151,9 @@ template <bool F16, bool GEN>
 __device__ __forceinline__ void store4(int32_t qt, void* row_base, int ch, float2 v01, float2 v23,
                                        QuantTab t) {
   if (qt != kQuantNone) {
+    const int u = ch >> 2, pos = ((u & 1) ? t.odd : 0) + (u >> 1) * t.step;
     *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(row_base) + ch) =
-        quant4<GEN>(v01, v23, t.scale[ch >> 2], t.offset[ch >> 2], qt);
+        quant4<GEN>(v01, v23, t.scale[pos], t.offset[pos], qt);
   } else {
     uint2 w;
     w.x = from_f2<F16>(v01.x, v01.y);
@@ -297,8 +327,9 @@ struct KvRows {
     const int32_t qk = p.kq, qv = p.vq;
     void* k_row = static_cast<uint8_t*>(p.k_cache) + static_cast<size_t>(cache_row) * kw * (qk ? 1 : 2);
     void* c_row = static_cast<uint8_t*>(p.ckv_cache) + static_cast<size_t>(cache_row) * cw * (qv ? 1 : 2);
-    const QuantTab kt{kt0.scale + (VARIANT == 2 ? n * (kw / 4) : 0), kt0.offset + (VARIANT == 2 ? n * (kw / 4) : 0)};
-    const QuantTab vt{vt0.scale + (VARIANT == 2 ? n * (cw / 4) : 0), vt0.offset + (VARIANT == 2 ? n * (cw / 4) : 0)};
+    const int kh = VARIANT == 2 ? n * kt0.stride : 0, vh = VARIANT == 2 ? n * vt0.stride : 0;
+    const QuantTab kt{kt0.scale + kh, kt0.offset + kh, kt0.odd, kt0.step, kt0.stride};
+    const QuantTab vt{vt0.scale + vh, vt0.offset + vh, vt0.odd, vt0.step, vt0.stride};
     uint16_t* kr_row = p.out_kv ? p.k_rope + row * kw : nullptr;
     uint16_t* ckv_row = p.out_kv ? p.c_kv + row * cw : nullptr;
 
@@ -375,11 +406,12 @@ struct KvRows {
 };
 
 // Shared-memory bytes of the quantisation tables (scale and offset, per head in V2).
-size_t quant_table_bytes(const KvLaunch& L, bool qk, bool qv) {
+size_t quant_table_bytes(const KvLaunch& L, bool qk, bool qv, bool split) {
   const int64_t heads = L.variant == 2 ? L.N : 1;
-  const int64_t kw = L.variant == 1 ? L.R : L.Dkv;
-  const int64_t cw = L.variant == 1 ? L.Dkv - L.R : L.Dv;
-  return static_cast<size_t>(heads) * ((qk ? kw : 0) + (qv ? cw : 0)) * 2 * sizeof(float);
+  const int kw = static_cast<int>(L.variant == 1 ? L.R : L.Dkv);
+  const int cw = static_cast<int>(L.variant == 1 ? L.Dkv - L.R : L.Dv);
+  const int64_t units = (qk ? tab_layout(kw, split).stride : 0) + (qv ? tab_layout(cw, split).stride : 0);
+  return static_cast<size_t>(heads * units) * 2 * sizeof(float4);
 }
 
 constexpr int kMinBlocks = 3;  // 12 warps per SM: up to 168 registers per thread
@@ -415,14 +447,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     const int ch = j + LPR * i;
     gam[i] = ch * 8 < rms ? __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * ch)) : make_uint4(0, 0, 0, 0);
   }
-  const int ku = p.kq ? heads * kw / 4 : 0, vu = p.vq ? heads * cw / 4 : 0;
+  const TabLayout kl = tab_layout(kw, true), vl = tab_layout(cw, true);
+  const int ku = p.kq ? heads * kl.stride : 0, vu = p.vq ? heads * vl.stride : 0;
   float4* ks = tabs;
   float4* ko = ks + ku;
   float4* vs = ko + ku;
   float4* vo = vs + vu;
   const int64_t slots = p.mode == kModeNorm ? p.cache_seq : p.block_num * p.block_size;
   const KvRows<VARIANT, LPR, CPL, F16, GEN, SHAPE> w{p, aux, j, dkv, dv, R, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
-                                         slots, gam, QuantTab{ks, ko}, QuantTab{vs, vo}};
+                                         slots, gam, QuantTab{ks, ko, kl.odd, kl.step, kl.stride},
+                                         QuantTab{vs, vo, vl.odd, vl.step, vl.stride}};
 
   // the lane's load cursor: row r_begin + g, then RPG rows further each step
   Cursor cur;
@@ -449,15 +483,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
       next += RPG;
     }
   }
-  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int u = threadIdx.x; u < ku; u += kThreads) {
-    ks[u] = __ldg(reinterpret_cast<const float4*>(p.k_scale) + u);
-    ko[u] = p.k_offset ? __ldg(reinterpret_cast<const float4*>(p.k_offset) + u) : zero4;
-  }
-  for (int u = threadIdx.x; u < vu; u += kThreads) {
-    vs[u] = __ldg(reinterpret_cast<const float4*>(p.v_scale) + u);
-    vo[u] = p.v_offset ? __ldg(reinterpret_cast<const float4*>(p.v_offset) + u) : zero4;
-  }
+  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, kw, kl);
+  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, cw, vl);
   __syncthreads();
 
   for (int64_t base = r_begin; base < r_end; base += DEPTH * RPG) {
@@ -523,6 +550,10 @@ struct StagedShape {
   static constexpr uint32_t STAGE_B = KV_B + V_B + 2 * CS_B;
   static constexpr uint32_t ROW_B = STAGE_B / kTileRows;
   static constexpr int STEPS = kTileRows / (kConsumerWarps * RPG);  // row groups per consumer warp and tile
+  // V1 keeps the plain table layout: its step (a DRAM-bound mix of reads and
+  // row-contiguous output writes) measured faster with it (74 vs 77 us), though
+  // the split layout has fewer bank conflicts.
+  static constexpr bool SPLIT = VARIANT == 2;
   static_assert(STEPS * kConsumerWarps * RPG == kTileRows, "tile rows split evenly over the consumer warps");
   static_assert(RMS / 8 <= LPR * CPL && Sh::dv / 8 <= LPR * CPL && R / 8 <= LPR, "lane layout holds the row");
 };
@@ -558,7 +589,8 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   const uint32_t rows = static_cast<uint32_t>(p.B * p.N * p.S);
   const uint32_t S = static_cast<uint32_t>(p.S), N = static_cast<uint32_t>(p.N);
   const int heads = VARIANT == 2 ? static_cast<int>(p.N) : 1;
-  const int ku = p.kq ? heads * T::KW / 4 : 0, vu = p.vq ? heads * T::CW / 4 : 0;
+  const TabLayout kl = tab_layout(T::KW, T::SPLIT), vl = tab_layout(T::CW, T::SPLIT);
+  const int ku = p.kq ? heads * kl.stride : 0, vu = p.vq ? heads * vl.stride : 0;
   const StagedPlan pl = staged_plan(static_cast<uint32_t>(2 * (ku + vu) * 16), T::STAGE_B);
   float4* ks = reinterpret_cast<float4*>(smem);
   float4* ko = ks + ku;
@@ -579,15 +611,8 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int u = threadIdx.x; u < ku; u += kStagedThreads) {
-    ks[u] = __ldg(reinterpret_cast<const float4*>(p.k_scale) + u);
-    ko[u] = p.k_offset ? __ldg(reinterpret_cast<const float4*>(p.k_offset) + u) : zero4;
-  }
-  for (int u = threadIdx.x; u < vu; u += kStagedThreads) {
-    vs[u] = __ldg(reinterpret_cast<const float4*>(p.v_scale) + u);
-    vo[u] = p.v_offset ? __ldg(reinterpret_cast<const float4*>(p.v_offset) + u) : zero4;
-  }
+  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, T::KW, kl);
+  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, T::CW, vl);
   __syncthreads();
 
   if (warp == kConsumerWarps) {
@@ -647,7 +672,8 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   const int64_t slots = p.block_num * p.block_size;
   const KvRows<VARIANT, T::LPR, T::CPL, F16, false, VARIANT, true> w{
       p, aux, j, T::DKV, T::DV, T::R, T::RMS, T::RMS / 8, VARIANT == 2 ? T::CW / 8 : 0, T::R / 8, T::R / 2,
-      T::KW, T::CW, slots, gam, QuantTab{ks, ko}, QuantTab{vs, vo}};
+      T::KW, T::CW, slots, gam, QuantTab{ks, ko, kl.odd, kl.step, kl.stride},
+      QuantTab{vs, vo, vl.odd, vl.step, vl.stride}};
   const uint4 z = make_uint4(0, 0, 0, 0);
   uint32_t k = 0;
   for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++k) {
@@ -697,7 +723,8 @@ template <int VARIANT, bool F16>
 cudaError_t launch_staged(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
   using T = StagedShape<VARIANT>;
   auto kernel = kv_staged_kernel<VARIANT, F16>;
-  const StagedPlan pl = staged_plan(static_cast<uint32_t>(quant_table_bytes(L, L.kq != 0, L.vq != 0)), T::STAGE_B);
+  const StagedPlan pl =
+      staged_plan(static_cast<uint32_t>(quant_table_bytes(L, L.kq != 0, L.vq != 0, T::SPLIT)), T::STAGE_B);
   const cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.total));
   if (e != cudaSuccess) return e;
@@ -728,7 +755,7 @@ unsigned persistent_grid(K kernel, int64_t rows, size_t smem) {
 template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE>
 cudaError_t launch_one(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
   auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL, F16, GEN, SHAPE>;
-  const size_t smem = quant_table_bytes(L, L.kq != 0, L.vq != 0);
+  const size_t smem = quant_table_bytes(L, L.kq != 0, L.vq != 0, true);
   if (smem > 48 * 1024) {
     const cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
