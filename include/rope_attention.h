@@ -178,8 +178,9 @@ ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cach
                                size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, reads the workspace status word, clears it, and
- * stores it in *device_status (0 = fine).  Returns RA_ERR_TIMEOUT if a
- * projection wait gave up since the last read, else RA_OK. */
+ * stores it in *device_status (0 = fine).  Returns RA_ERR_TIMEOUT if a wait of
+ * the projection or of the pipelined norm/RoPE pass gave up since the last
+ * read, else RA_OK. */
 ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_status);
 
 /* qkv_cte_mx for callers that cannot allocate device memory.  The pages have
@@ -206,8 +207,8 @@ ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_t* a, const
                              const float* k_gamma, uint16_t* out, void* stream);
 
 /* Test hook: time limit, in nanoseconds, of each device pipeline wait in the
- * projection kernel and the staged KV cache kernel (default 2e9).  Values < 1000
- * are raised to 1000. */
+ * projection kernel, the pipelined norm/RoPE pass and the pipelined KV cache
+ * kernel (default 2e9).  Values < 1000 are raised to 1000. */
 void ra_set_wait_timeout_ns(int64_t ns);
 
 /* Test hook for failure detection.  The next projection launch (qkv_cte_mx or
@@ -218,6 +219,16 @@ void ra_set_wait_timeout_ns(int64_t ns);
  * waits give up, so the CUDA context stays usable.  The output of that launch
  * is undefined.  Applies to one launch, then clears itself. */
 void ra_test_stall_next_projection(void);
+
+/* Test hook for failure detection.  The next norm/RoPE pass (qkv_cte_mx or
+ * qkv_cte_mx_norm_rope) that runs the pipelined kernel -- BSD output, head_dim
+ * 64 or 128, at most 24 KB of rewritten Q/K columns per token -- issues none of
+ * its copies, so its waits run out after the time limit above; every block
+ * records the timeout in the workspace status word and exits, and
+ * qkv_cte_mx_status reports RA_ERR_TIMEOUT.  Nothing is in flight when the
+ * waits give up.  The output of that call is undefined.  Applies to one call,
+ * then clears itself. */
+void ra_test_stall_next_norm_rope(void);
 
 /* ========================================================================
  * Row FP8 quantisation of the activation (the step before qkv_cte_mx)

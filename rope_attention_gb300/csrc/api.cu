@@ -33,6 +33,7 @@ thread_local std::string g_last_error;
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_stall_next{0};  // ra_test_stall_next_projection
 std::atomic<int> g_stall_next_kv{0};  // ra_test_stall_next_kv_cache
+std::atomic<int> g_stall_next_norm{0};  // ra_test_stall_next_norm_rope
 
 ra_status fail(ra_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ra_status fail(ra_status code, const char* fmt, ...) {
@@ -253,6 +254,9 @@ ra_status run_norm_rope(const qkv_cte_mx_params* p, const QkvShape& s, const flo
   L.exp_stride = s.exp_stride;
   L.eps = p->norm_eps;
   L.nbsd = p->output_layout == RA_LAYOUT_NBSD;
+  L.status = static_cast<int32_t*>(workspace);
+  L.wait_ns = g_wait_ns.load();
+  L.stall_loads = g_stall_next_norm.exchange(0);
   cudaError_t e = ra::launch_qk_norm_rope(L, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm/rope launch");
   return RA_OK;
@@ -270,13 +274,15 @@ extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 5; }
+int32_t ra_abi_version(void) { return 6; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
 void ra_test_stall_next_projection(void) { g_stall_next.store(1); }
 
 void ra_test_stall_next_kv_cache(void) { g_stall_next_kv.store(1); }
+
+void ra_test_stall_next_norm_rope(void) { g_stall_next_norm.store(1); }
 
 ra_status qkv_cte_mx_packed_weight_bytes(int64_t H, int64_t I, size_t* bytes) {
   if (!bytes) return fail(RA_ERR_INVALID_ARG, "bytes is NULL");

@@ -72,6 +72,9 @@ struct NormRopeLaunch {
   float eps;
   int32_t nbsd;                // out is [I / head_dim, T, head_dim] instead of [T, I]
   int32_t do_q, do_k;          // segments this pass rewrites
+  int32_t* status;             // workspace status word (pipelined kernel: a wait ran out)
+  int64_t wait_ns;             // time limit of each pipeline wait
+  int32_t stall_loads;         // test hook: the pipelined kernel issues no copies
 };
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);
 

@@ -558,28 +558,6 @@ struct StagedShape {
   static_assert(RMS / 8 <= LPR * CPL && Sh::dv / 8 <= LPR * CPL && R / 8 <= LPR, "lane layout holds the row");
 };
 
-// warp-collective bounded wait: every lane returns the same answer
-__device__ bool kv_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit, volatile int* abort_flag) {
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    const bool ok = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, ok)) return true;
-    if ((i & 31u) == 31u) {
-      int give_up = 0;
-      if ((threadIdx.x & 31) == 0) {
-        const uint64_t t = globaltimer_ns();
-        if (t0 == 0) t0 = t;
-        else if (*abort_flag || t - t0 > limit) give_up = 1;
-      }
-      give_up = __shfl_sync(0xffffffffu, give_up, 0);
-      if (give_up) {
-        if ((threadIdx.x & 31) == 0) *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
 template <int VARIANT, bool F16>
 __global__ void __launch_bounds__(kStagedThreads, 3)
     kv_staged_kernel(const KvLaunch p, const KvAux aux, const uint32_t tiles) {
@@ -621,7 +599,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
     bool live = true;
     for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++k) {
       const uint32_t s = k % kStages, use = k / kStages;
-      if (k >= kStages && !kv_wait_warp(bars + 8 * (kStages + s), (use & 1u) ^ 1u, limit, abort_flag)) {
+      if (k >= kStages && !bounded_wait_warp(bars + 8 * (kStages + s), (use & 1u) ^ 1u, limit, abort_flag)) {
         live = false;
         break;
       }
@@ -651,14 +629,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
     // leave only when no copy into this block's shared memory can still be in flight
     if (lane == 0) {
       for (uint32_t u = k > static_cast<uint32_t>(kStages) ? k - kStages : 0; u < k; ++u) {
-        const uint32_t bar = bars + 8 * (u % kStages), parity = (u / kStages) & 1u;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar, parity)) {
-          if (globaltimer_ns() - t0 > limit) {
-            atomicExch(p.status, 1);
-            break;
-          }
-        }
+        if (!bounded_drain(bars + 8 * (u % kStages), (u / kStages) & 1u, limit)) atomicExch(p.status, 1);
       }
     }
     return;
@@ -678,7 +649,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   uint32_t k = 0;
   for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++k) {
     const uint32_t s = k % kStages, use = k / kStages;
-    if (!kv_wait_warp(bars + 8 * s, use & 1u, limit, abort_flag)) {
+    if (!bounded_wait_warp(bars + 8 * s, use & 1u, limit, abort_flag)) {
       if (lane == 0) atomicExch(p.status, 1);
       return;
     }

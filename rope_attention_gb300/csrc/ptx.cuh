@@ -53,6 +53,54 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Bounded mbarrier waits (limit in ns of %globaltimer).  A wait gives up when
+// the limit passes or when *abort_flag is set, and then sets *abort_flag.
+// single thread:
+__device__ inline bool bounded_wait_one(uint32_t bar, uint32_t parity, uint64_t limit,
+                                        volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*abort_flag || globaltimer_ns() - t0 > limit) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+// whole warp (every lane returns the same answer):
+__device__ inline bool bounded_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit,
+                                         volatile int* abort_flag) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((i & 31u) == 31u) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0) {
+        const uint64_t t = globaltimer_ns();
+        if (t0 == 0) t0 = t;
+        else if (*abort_flag || t - t0 > limit) give_up = 1;
+      }
+      give_up = __shfl_sync(0xffffffffu, give_up, 0);
+      if (give_up) {
+        if ((threadIdx.x & 31) == 0) *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+// used while leaving: wait for the phase, at most `limit` ns; false if it did not complete
+__device__ inline bool bounded_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit) return false;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA / bulk copies
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -75,6 +123,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// plain bulk copy shared -> global, tracked by the issuing thread's bulk groups;
+// both addresses 16-byte aligned, bytes % 16 == 0
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's bulk groups still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until every bulk group of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

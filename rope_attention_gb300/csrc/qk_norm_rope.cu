@@ -33,6 +33,12 @@ constexpr int kThreads = 128;
 constexpr int kTok = 8;        // tokens per block
 constexpr int kUnroll = 2;     // tokens whose loads are in flight together per item
 
+__device__ __forceinline__ void lds8f(const float* p, float2 (&f)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = make_float2(a.x, a.y); f[1] = make_float2(a.z, a.w);
+  f[2] = make_float2(b.x, b.y); f[3] = make_float2(b.z, b.w);
+}
 __device__ __forceinline__ void ldg8f(const float* p, float2 (&f)[4]) {
   const float4 a = __ldg(reinterpret_cast<const float4*>(p));
   const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
@@ -151,9 +157,226 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeLa
   }
 }
 
+// ---------------------------------------------------------------- pipelined kernel
+// For the BSD layout with head_dim 64 or 128.  A token's Q/K columns are one
+// contiguous span of `out` (20 KB for 80 heads of 128), and its partial sums,
+// exponents and cos/sin rows are contiguous rows of their own, so one lane of a
+// producer warp moves a token into a shared-memory stage with a handful of bulk
+// copies (cp.async.bulk, completion counted by the stage's mbarrier), up to
+// kSt - 1 tokens ahead.  Eight consumer warps rewrite the stage in place; when
+// all eight have arrived on the stage's done barrier, one thread writes the
+// span back with a bulk store and releases the stage once that store has read
+// it.  Each consumer thread keeps the same 8-column offset within a head for
+// every item (256 is a multiple of the items per head), so it reads its cos/sin
+// once per token.  Every wait is bounded; a wait that runs out records 1 in the
+// status word and the block leaves, each thread first waiting (with a limit)
+// for the copies it issued.
+constexpr int kSt = 4;                    // stages
+constexpr int kStWarps = 8;               // consumer warps
+constexpr int kStThreads = (kStWarps + 1) * 32;
+constexpr int kStMaxSpan = 24 * 1024;     // Q/K bytes per token the stage holds
+
+struct StagePlan {                        // byte offsets within a stage
+  uint32_t span, part, exps, cos, sin, bytes, tx;
+  uint32_t span_bytes, part_bytes;
+};
+
+StagePlan stage_plan(const NormRopeLaunch& L) {
+  const int h_begin = L.do_q ? 0 : L.num_q_heads;
+  const int h_end = (L.num_k_heads > 0 && L.do_k) ? L.num_q_heads + L.num_k_heads : L.num_q_heads;
+  StagePlan pl{};
+  pl.span_bytes = static_cast<uint32_t>((h_end - h_begin) * L.head_dim * 2);
+  pl.part_bytes = L.n_part_tiles > 0 ? static_cast<uint32_t>(L.part_stride) * 8u : 0u;
+  pl.span = 0;
+  pl.part = pl.span_bytes;
+  pl.exps = pl.part + pl.part_bytes;
+  pl.cos = pl.exps + static_cast<uint32_t>(L.exp_stride);
+  const uint32_t cs = L.rope ? static_cast<uint32_t>(L.head_dim) * 4u : 0u;
+  pl.sin = pl.cos + cs;
+  pl.tx = pl.sin + cs;
+  pl.bytes = (pl.tx + 127u) & ~127u;
+  return pl;
+}
+
+template <int D, bool ROT>
+__global__ void __launch_bounds__(kStThreads, 2)
+    qk_norm_rope_staged_kernel(const NormRopeLaunch p, const StagePlan pl) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int HALF = D / 2;
+  constexpr int PER_HEAD = ROT ? D / 16 : D / 8;  // 8-column items per head
+  static_assert((kStWarps * 32) % PER_HEAD == 0, "a thread keeps its offset within the head");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = p.num_q_heads, nk = p.num_k_heads;
+  const int h_begin = p.do_q ? 0 : nq;
+  const int h_end = (nk > 0 && p.do_k) ? nq + nk : nq;
+  const int64_t span_col = static_cast<int64_t>(h_begin) * D;
+  const uint32_t bars = smem_u32(smem + kSt * pl.bytes);  // full[kSt], empty[kSt], done[kSt]
+  auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
+  auto empty_bar = [&](uint32_t s) { return bars + 8u * (kSt + s); };
+  auto done_bar = [&](uint32_t s) { return bars + 8u * (2 * kSt + s); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSt * pl.bytes + 3 * kSt * 8);
+  const uint32_t stage0 = smem_u32(smem);
+  const uint64_t limit = static_cast<uint64_t>(p.wait_ns);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSt; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(done_bar(s), kStWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kStWarps) {
+    // producer: token k of this block goes to stage k % kSt
+    if (lane == 0) {
+      uint32_t k = 0;
+      bool live = true;
+      for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++k) {
+        const uint32_t s = k % kSt, use = k / kSt;
+        if (k >= kSt && !bounded_wait_one(empty_bar(s), (use & 1u) ^ 1u, limit, abort_flag)) {
+          live = false;
+          break;
+        }
+        const uint32_t full = full_bar(s), dst = stage0 + s * pl.bytes;
+        mbar_arrive_expect_tx(full, pl.tx);
+        if (!p.stall_loads) {
+          bulk_load(dst + pl.span, p.out + t * p.I + span_col, pl.span_bytes, full);
+          if (pl.part_bytes) bulk_load(dst + pl.part, p.partials + t * p.part_stride, pl.part_bytes, full);
+          bulk_load(dst + pl.exps, p.exps + t * p.exp_stride, static_cast<uint32_t>(p.exp_stride), full);
+          if (ROT) {
+            bulk_load(dst + pl.cos, p.cos + t * D, D * 4, full);
+            bulk_load(dst + pl.sin, p.sin + t * D, D * 4, full);
+          }
+        }
+      }
+      if (!live) atomicExch(p.status, 1);
+      // leave only when no copy into this block's shared memory can still be in flight
+      for (uint32_t u = k > static_cast<uint32_t>(kSt) ? k - kSt : 0; u < k; ++u)
+        if (!bounded_drain(full_bar(u % kSt), (u / kSt) & 1u, limit)) atomicExch(p.status, 1);
+    }
+    return;
+  }
+
+  // consumers
+  const int ct = threadIdx.x;                 // 0 .. 255
+  const int u = ct % PER_HEAD;                // this thread's 8-column offset within a head
+  const int items = (h_end - h_begin) * PER_HEAD;
+  const int q_end = nq * D;
+  const bool storer = threadIdx.x == 0;
+  const float wq = static_cast<float>(nq * D), wk = static_cast<float>(nk * D);
+  uint32_t k = 0;
+  bool ok = true;
+  for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++k) {
+    const uint32_t s = k % kSt, use = k / kSt;
+    if (!bounded_wait_warp(full_bar(s), use & 1u, limit, abort_flag)) {
+      ok = false;
+      break;
+    }
+    uint8_t* st = smem + s * pl.bytes;
+    // 1b: inv_rms of the token, its partials summed lane-strided then by an xor tree
+    float sq = 0.f, sk = 0.f;
+    const float2* part = reinterpret_cast<const float2*>(st + pl.part);
+    for (int j = lane; j < p.n_part_tiles; j += 32) {
+      const float2 v = part[j];
+      sq += v.x;
+      sk += v.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    const float inv_q = p.q_norm ? rsqrtf(sq / wq + p.eps) : 1.f;
+    const float inv_k = p.k_norm ? rsqrtf(sk / wk + p.eps) : 1.f;
+    const int8_t* ex = reinterpret_cast<const int8_t*>(st + pl.exps);
+    float2 c_lo[4], c_hi[4], s_lo[4], s_hi[4];
+    if (ROT) {
+      const float* cs = reinterpret_cast<const float*>(st + pl.cos) + 8 * u;
+      const float* sn = reinterpret_cast<const float*>(st + pl.sin) + 8 * u;
+      lds8f(cs, c_lo);
+      lds8f(cs + HALF, c_hi);
+      lds8f(sn, s_lo);
+      lds8f(sn + HALF, s_hi);
+    }
+    for (int it = ct; it < items; it += kStWarps * 32) {
+      const int rel = (it / PER_HEAD) * D + 8 * u;  // column within the span
+      const int col = static_cast<int>(span_col) + rel;
+      const float inv = col < q_end ? inv_q : inv_k;
+      uint4* lo = reinterpret_cast<uint4*>(st + pl.span + 2 * rel);
+      float2 y_lo[4];
+      decode8(*lo, inv * exp2_int(ex[col / kPartCols]), y_lo);
+      if (ROT) {
+        uint4* hi = reinterpret_cast<uint4*>(st + pl.span + 2 * (rel + HALF));
+        float2 y_hi[4];
+        decode8(*hi, inv * exp2_int(ex[(col + HALF) / kPartCols]), y_hi);
+        float2 o_lo[4], o_hi[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          o_lo[m] = __ffma2_rn(y_lo[m], c_lo[m], __fmul2_rn(y_hi[m], make_float2(-s_lo[m].x, -s_lo[m].y)));
+          o_hi[m] = __ffma2_rn(y_hi[m], c_hi[m], __fmul2_rn(y_lo[m], s_hi[m]));
+        }
+        *lo = pack8(o_lo);
+        *hi = pack8(o_hi);
+      } else {
+        *lo = pack8(y_lo);
+      }
+    }
+    // the rewritten span is read next by the bulk store (async proxy)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done_bar(s));
+    if (warp == 0) {
+      int go = 1;
+      if (storer) {
+        go = bounded_wait_one(done_bar(s), use & 1u, limit, abort_flag) ? 1 : 0;
+        if (go) {
+          bulk_store(p.out + t * p.I + span_col, stage0 + s * pl.bytes + pl.span, pl.span_bytes);
+          bulk_commit();
+          bulk_wait_read<1>();  // the previous token's store has read its stage
+          if (k > 0) mbar_arrive(empty_bar((k - 1) % kSt));
+        }
+      }
+      go = __shfl_sync(0xffffffffu, go, 0);
+      if (!go) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  if (!ok && lane == 0) atomicExch(p.status, 1);
+  if (storer) bulk_wait_all();  // this thread's stores are complete before the block ends
+}
+
+template <int D, bool ROT>
+cudaError_t launch_staged(const NormRopeLaunch& L, const StagePlan& pl, cudaStream_t st) {
+  auto kernel = qk_norm_rope_staged_kernel<D, ROT>;
+  const size_t smem = static_cast<size_t>(kSt) * pl.bytes + 3 * kSt * 8 + 16;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStThreads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int64_t cap = static_cast<int64_t>(per_sm) * device_sm_count();
+  const unsigned grid = static_cast<unsigned>(L.T < cap ? L.T : cap);
+  kernel<<<grid, kStThreads, smem, st>>>(L, pl);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream) {
+  const StagePlan pl = stage_plan(L);
+  const bool staged = !L.nbsd && L.status != nullptr && (L.head_dim == 64 || L.head_dim == 128) &&
+                      pl.span_bytes > 0 && pl.span_bytes <= static_cast<uint32_t>(kStMaxSpan) &&
+                      L.exp_stride > 0 && L.exp_stride % 16 == 0 && L.part_stride % 2 == 0 &&
+                      L.I % 8 == 0 && L.T < (int64_t(1) << 31);
+  if (staged) {
+    if (L.head_dim == 128) return L.rope ? launch_staged<128, true>(L, pl, stream) : launch_staged<128, false>(L, pl, stream);
+    return L.rope ? launch_staged<64, true>(L, pl, stream) : launch_staged<64, false>(L, pl, stream);
+  }
   const int64_t blocks = (L.T + kTok - 1) / kTok;
   qk_norm_rope_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(L);
   return cudaGetLastError();

@@ -29,7 +29,8 @@ EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns", "ra_test
            "qkv_cte_mx_packed_weight_bytes", "qkv_cte_mx_pack_weight", "qkv_cte_mx_workspace_bytes",
            "qkv_cte_mx", "qkv_cte_mx_project", "qkv_cte_mx_norm_rope", "qkv_cte_mx_status",
            "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache", "kv_rms_norm_rope_cache_status",
-           "ra_test_stall_next_kv_cache", "row_quantize_e4m3", "row_quantize_e4m3_packed"]
+           "ra_test_stall_next_kv_cache", "ra_test_stall_next_norm_rope", "row_quantize_e4m3",
+           "row_quantize_e4m3_packed"]
 
 
 class RAError(RuntimeError):
@@ -88,6 +89,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                          P, P, P, P, P, P, P, P, P, P, P]),
         "kv_rms_norm_rope_cache_status": (i32, [P, ctypes.POINTER(i32)]),
         "ra_test_stall_next_kv_cache": (None, []),
+        "ra_test_stall_next_norm_rope": (None, []),
         "row_quantize_e4m3": (i32, [P, i64, i64, P, P, P]),
         "row_quantize_e4m3_packed": (i32, [P, i64, i64, P, P]),
     }
@@ -140,6 +142,11 @@ def ra_set_wait_timeout_ns(ns: int) -> None:
 def ra_test_stall_next_projection() -> None:
     """Test hook: the next projection launch issues no loads, so its waits time out."""
     load().ra_test_stall_next_projection()
+
+
+def ra_test_stall_next_norm_rope() -> None:
+    """Test hook: the next pipelined norm/RoPE launch issues no copies, so its waits time out."""
+    load().ra_test_stall_next_norm_rope()
 
 
 def ra_test_stall_next_kv_cache() -> None:

@@ -38,7 +38,7 @@ def test_exports_every_declared_function(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in the header but not exported"
     assert sorted(names) == sorted(native.EXPORTS)
-    assert native.ra_abi_version() == 5
+    assert native.ra_abi_version() == 6
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -7,8 +7,10 @@ none of its loads, so its waits run out with nothing in flight.  The kernel must
 record the timeout in the workspace status word (read on the host through
 qkv_cte_mx_status, which also clears it), release its tensor memory and exit;
 the CUDA context must stay usable, and the next call, with the hook cleared,
-must give the correct result.  The pipelined KV cache kernel is held to the same
-rules through ra_test_stall_next_kv_cache and kv_rms_norm_rope_cache_status.
+must give the correct result.  The pipelined norm/RoPE pass (through
+ra_test_stall_next_norm_rope and the same status word) and the pipelined KV
+cache kernel (through ra_test_stall_next_kv_cache and
+kv_rms_norm_rope_cache_status) are held to the same rules.
 """
 import ctypes
 
@@ -43,6 +45,29 @@ def test_stalled_pipeline_reports_timeout_and_context_survives():
     finally:
         native.ra_set_wait_timeout_ns(DEFAULT_WAIT_NS)
     check_qkv(case, as_f64(run.out), qkv_reference(case), "call after a timed-out launch")
+
+
+def test_stalled_norm_rope_pipeline_reports_timeout_and_context_survives():
+    case = synth.qkv_tiny()
+    run = runner.QkvRun(case)
+    native.ra_set_wait_timeout_ns(2_000_000)  # 2 ms per wait
+    try:
+        run.project()
+        torch.cuda.synchronize()
+        assert run.status() == 0
+        native.ra_test_stall_next_norm_rope()
+        run.norm_rope()
+        v = ctypes.c_int32()
+        st = native.load().qkv_cte_mx_status(ctypes.c_void_p(run.workspace.data_ptr()), None,
+                                             ctypes.byref(v))
+        assert st == -6 and v.value == 1, (st, v.value)
+        # cleared by the read; the hook applied to one launch only
+        run.run()
+        torch.cuda.synchronize()
+        assert run.status() == 0
+    finally:
+        native.ra_set_wait_timeout_ns(DEFAULT_WAIT_NS)
+    check_qkv(case, as_f64(run.out), qkv_reference(case), "call after a timed-out norm/RoPE pass")
 
 
 def test_stalled_kv_pipeline_reports_timeout_and_context_survives():
