@@ -229,7 +229,8 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = measure_e2e(q, k, qcase, kcase, args, ws)
     # rows measured outside the step come last, so their buffers cannot disturb it
-    nxt = {} if args.no_next else {"row_quantize_e4m3": time_row_quantize(qcase, args, hbm)}
+    nxt = {} if args.no_next else {"row_quantize_e4m3": time_row_quantize(qcase, args, hbm),
+                                   "qkv_cte_mx_per_head": time_per_head(q, args, fp8_peak)}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
@@ -294,6 +295,42 @@ def time_row_quantize(qcase, args, hbm_gbs):
     return {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4),
             "input": f"bf16 hidden state [{T}, {H}] (N(0,1), row factors 2^U(-3,3), 1% outlier channels x8)",
             "note": "measured alone, not part of the step"}
+
+
+def time_per_head(q, args, fp8_peak):
+    """The per-head qk-norm variant (each head normed by its own RMS, gamma [head_dim],
+    then the rotate-half RoPE) on the workload's projection: the step's inputs and
+    weights with q_norm = k_norm = RMS_PER_HEAD, projection + RoPE pass timed alone
+    (CUDA events over K calls after W warm-ups)."""
+    import torch
+    from rope_attention_gb300 import native, runner, synth
+    c = q.case
+    pp = native.QkvCteMxParams.from_buffer_copy(q.params)
+    pp.q_norm = pp.k_norm = native.RA_NORM_RMS_PER_HEAD
+    qg = runner.to_dev(synth.stream(97, 0).uniform(0.5, 1.5, c.head_dim).astype("float32"))
+    kg = runner.to_dev(synth.stream(97, 1).uniform(0.5, 1.5, c.head_dim).astype("float32"))
+    ws = torch.zeros(native.qkv_cte_mx_workspace_bytes(pp), dtype=torch.uint8, device="cuda")
+
+    def call():
+        native.qkv_cte_mx_project(pp, q.a, q.a_scale, q.w_packed, q.weight_scales, q.bias, qg, kg, q.out, ws)
+        native.qkv_cte_mx_norm_rope(pp, q.cos, q.sin, q.out, ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        call()
+    end.record()
+    torch.cuda.synchronize()
+    assert native.qkv_cte_mx_status(ws) == 0, "per-head call reported a wait timeout"
+    ms = start.elapsed_time(end) / args.steps
+    tf = c.flops / (ms * 1e-3) / 1e12
+    del ws
+    return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4),
+            "note": f"q_norm = k_norm = RMS_PER_HEAD (gamma [{c.head_dim}]) on the step's projection, "
+                    "projection + RoPE pass, measured alone, not part of the step"}
 
 
 def measure_e2e(q, k, qcase, kcase, args, ws):

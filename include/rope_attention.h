@@ -158,20 +158,22 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
  * until qkv_cte_mx_norm_rope runs: fp16 of O * gamma * 2^-e with a power-of-two
  * e per (token, 128-column block) kept in the workspace, so the intermediate
  * carries 11 significant bits and the only bf16 rounding of Q and K is the
- * final one.  Segments with the per-head norm are finished here: normed, rotated
- * when fused_rope (cos_cache / sin_cache are then required; otherwise they may
- * be NULL) and stored as bf16.  Arguments as for qkv_cte_mx. */
+ * final one.  Segments with the per-head norm are normed here, each head by
+ * its own RMS and the [head_dim] gamma: without fused_rope they are finished
+ * (bf16); with it they are held in the same encoding and qkv_cte_mx_norm_rope
+ * rotates them.  Arguments as for qkv_cte_mx (no cos/sin: every rotation is
+ * applied by the second pass). */
 ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
-                             const float* cos_cache, const float* sin_cache, const float* q_gamma,
-                             const float* k_gamma, uint16_t* out, void* workspace,
+                             const float* q_gamma, const float* k_gamma, uint16_t* out, void* workspace,
                              size_t workspace_bytes, void* stream);
 
 /* Second half on its own (Design 1b, Design 2): reduces the sums of squares
  * left in `workspace` by qkv_cte_mx_project for the same `out` into inv_rms per
- * token and segment, applies it and the rotate-half RoPE (cos/sin required iff
- * fused_rope) to the encoded Q and K columns and writes them back into `out` as
- * bf16.  V is not touched.  This is the seam where a tensor-parallel
+ * token and across-heads segment, applies it (per-head segments are already
+ * normed) and the rotate-half RoPE (cos/sin required iff fused_rope) to the
+ * encoded Q and K columns and writes them back into `out` as bf16.  V is not
+ * touched.  This is the seam where a tensor-parallel
  * all-reduce of the sums would go. */
 ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cache,
                                const float* sin_cache, uint16_t* out, void* workspace,

@@ -71,10 +71,11 @@ struct QkvShape {
 };
 
 // which segments the norm/RoPE pass rewrites
+// (across-heads norm, and RoPE whatever the norm: a per-head segment is normed in
+// the projection and rotated here)
 void second_pass_segments(const qkv_cte_mx_params* p, bool* do_q, bool* do_k) {
-  *do_q = p->q_norm == RA_NORM_RMS_ACROSS_HEADS || (p->q_norm == RA_NORM_NONE && p->fused_rope);
-  *do_k = p->num_kv_heads > 0 &&
-          (p->k_norm == RA_NORM_RMS_ACROSS_HEADS || (p->k_norm == RA_NORM_NONE && p->fused_rope));
+  *do_q = p->q_norm == RA_NORM_RMS_ACROSS_HEADS || p->fused_rope;
+  *do_k = p->num_kv_heads > 0 && (p->k_norm == RA_NORM_RMS_ACROSS_HEADS || p->fused_rope);
 }
 
 ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
@@ -141,9 +142,8 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
 
 ra_status check_project_args(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
                              const float* a_scale, const void* w_packed, const float* ws,
-                             const uint16_t* bias, const float* cos, const float* sin,
-                             const float* qg, const float* kg, const uint16_t* out,
-                             const void* workspace, size_t workspace_bytes) {
+                             const uint16_t* bias, const float* qg, const float* kg,
+                             const uint16_t* out, const void* workspace, size_t workspace_bytes) {
   if (!a || !a_scale || !w_packed || !out || !workspace)
     return fail(RA_ERR_INVALID_ARG, "a, a_scale, w_packed, out and workspace are required");
   if (!aligned16(a) || !aligned16(out) || !aligned16(w_packed) || !aligned16(workspace))
@@ -154,10 +154,6 @@ ra_status check_project_args(const qkv_cte_mx_params* p, const QkvShape& s, cons
   if (p->k_norm && !kg) return fail(RA_ERR_INVALID_ARG, "k_norm requires k_gamma");
   if ((qg && !aligned16(qg)) || (kg && !aligned16(kg)))
     return fail(RA_ERR_ALIGNMENT, "gammas must be 16-byte aligned");
-  if (s.ph_end > s.ph_begin && p->fused_rope) {
-    if (!cos || !sin) return fail(RA_ERR_INVALID_ARG, "the per-head norm with fused_rope needs cos/sin in the projection");
-    if (!aligned16(cos) || !aligned16(sin)) return fail(RA_ERR_ALIGNMENT, "cos/sin caches must be 16-byte aligned");
-  }
   if (workspace_bytes < s.workspace)
     return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
   return RA_OK;
@@ -180,8 +176,8 @@ ra_status check_norm_args(const qkv_cte_mx_params* p, const float* cos, const fl
 
 ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
                       const float* a_scale, const void* w_packed, const float* ws,
-                      const uint16_t* bias, const float* cos, const float* sin, const float* qg,
-                      const float* kg, uint16_t* out, void* workspace, cudaStream_t st) {
+                      const uint16_t* bias, const float* qg, const float* kg, uint16_t* out,
+                      void* workspace, cudaStream_t st) {
   ra::ProjLaunch L{};
   L.a = a;
   L.a_scale = a_scale;
@@ -212,9 +208,7 @@ ra_status run_project(const qkv_cte_mx_params* p, const QkvShape& s, const uint8
   L.ph_end = s.ph_end;
   L.ph_q_gamma = p->q_norm == RA_NORM_RMS_PER_HEAD ? qg : nullptr;
   L.ph_k_gamma = p->k_norm == RA_NORM_RMS_PER_HEAD ? kg : nullptr;
-  L.ph_rope = p->fused_rope;
-  L.cos = cos;
-  L.sin = sin;
+  L.ph_carry = p->fused_rope;
   L.eps = p->norm_eps;
   L.wait_ns = g_wait_ns.load();
   L.stall_loads = g_stall_next.exchange(0);
@@ -274,7 +268,7 @@ extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 6; }
+int32_t ra_abi_version(void) { return 7; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
@@ -318,16 +312,15 @@ ra_status qkv_cte_mx_workspace_bytes(const qkv_cte_mx_params* p, size_t* bytes) 
 
 ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
-                             const float* cos_cache, const float* sin_cache, const float* q_gamma,
-                             const float* k_gamma, uint16_t* out, void* workspace,
+                             const float* q_gamma, const float* k_gamma, uint16_t* out, void* workspace,
                              size_t workspace_bytes, void* stream) {
   QkvShape s;
   ra_status st = check_params(p, &s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache,
-                          q_gamma, k_gamma, out, workspace, workspace_bytes);
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
+                          workspace, workspace_bytes);
   if (st != RA_OK) return st;
-  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache, q_gamma,
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma,
                    k_gamma, out, workspace, static_cast<cudaStream_t>(stream));
   return st == RA_OK ? ok() : st;
 }
@@ -352,13 +345,13 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
   QkvShape s;
   ra_status st = check_params(p, &s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache,
-                          q_gamma, k_gamma, out, workspace, workspace_bytes);
+  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
+                          workspace, workspace_bytes);
   if (st != RA_OK) return st;
   st = check_norm_args(p, cos_cache, sin_cache, out, workspace, workspace_bytes, s);
   if (st != RA_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache, q_gamma,
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma,
                    k_gamma, out, workspace, cs);
   if (st != RA_OK) return st;
   st = run_norm_rope(p, s, cos_cache, sin_cache, out, workspace, cs);

@@ -41,13 +41,12 @@ struct ProjLaunch {
   int32_t stall_loads;         // test hook: issue no TMA loads, so the pipeline waits run out
   int32_t head_dim;
   int32_t nbsd;                // out is [I / head_dim, T, head_dim] instead of [T, I]
-  // columns [ph_begin, ph_end) take the per-head norm (and RoPE) in the epilogue
+  // columns [ph_begin, ph_end) take the per-head norm in the epilogue: finished
+  // there (bf16) without RoPE, or normed and carried to the RoPE pass (ph_carry)
   int32_t ph_begin, ph_end;
   const float* ph_q_gamma;     // [head_dim] per-head gamma of the Q / K segment, or null
   const float* ph_k_gamma;
-  int32_t ph_rope;
-  const float* cos;            // [T, head_dim] fp32 rotate-half tables (per-head RoPE)
-  const float* sin;
+  int32_t ph_carry;
   float eps;
 };
 cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const char** why);

@@ -111,11 +111,9 @@ struct Params {
   int32_t stall_loads;
   int32_t head_dim, nbsd;
   int32_t out32;  // out is 32-byte aligned, so every 16-column chunk is (I and head_dim are multiples of 16)
-  int32_t ph_begin, ph_end, ph_rope;
+  int32_t ph_begin, ph_end, ph_carry;
   const float* ph_q_gamma;
   const float* ph_k_gamma;
-  const float* cos;
-  const float* sin;
   float eps;
 };
 
@@ -187,13 +185,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
 
 // One (lo, hi) pair of 16-column chunks of a head for the per-head norm (qkv_cte
 // page, Design 1: the upstream qk-norm, each head's slice by its own RMS, with a
-// [head_dim] gamma) and then the rotate-half RoPE (Design 2): columns j of the lo
-// chunk pair with j + D/2 of the hi chunk.  r holds v (after dequant and bias);
-// the pair is normed, rotated and stored as bf16.
+// [head_dim] gamma) when the call has no RoPE: r holds v (after dequant and bias);
+// the pair is normed and stored as bf16.  (With RoPE a per-head segment is normed
+// in the pass-1 loop below and carried to the RoPE pass instead.)
 template <int D>
 __device__ __forceinline__ void per_head_pair(uint32_t (&r)[EPI_COLS], int lo_c, int hi_c, int jc, float inv,
-                                              const float* g, bool rope, int row, const Params& p,
-                                              uint16_t* dst_lo, uint16_t* dst_hi) {
+                                              const float* g, uint16_t* dst_lo, uint16_t* dst_hi) {
   const float2 inv2 = make_float2(inv, inv);
   // two halves of 8 columns each, so that few values are live beside the accumulator
 #pragma unroll
@@ -210,26 +207,6 @@ __device__ __forceinline__ void per_head_pair(uint32_t (&r)[EPI_COLS], int lo_c,
       y_lo[2 * q + 1] = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(r[lo_c * 16 + k + 2]), __uint_as_float(r[lo_c * 16 + k + 3])), inv2), make_float2(gl.z, gl.w));
       y_hi[2 * q] = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(r[hi_c * 16 + k]), __uint_as_float(r[hi_c * 16 + k + 1])), inv2), make_float2(gh.x, gh.y));
       y_hi[2 * q + 1] = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(r[hi_c * 16 + k + 2]), __uint_as_float(r[hi_c * 16 + k + 3])), inv2), make_float2(gh.z, gh.w));
-    }
-    if (rope) {
-      // lo' = lo cos_j - hi sin_j ; hi' = hi cos_{j+D/2} + lo sin_{j+D/2}
-      const float4* cs = reinterpret_cast<const float4*>(p.cos + static_cast<size_t>(row) * D + j);
-      const float4* sn = reinterpret_cast<const float4*>(p.sin + static_cast<size_t>(row) * D + j);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float4 cl = __ldg(cs + q), ch = __ldg(cs + D / 8 + q);
-        const float4 sl = __ldg(sn + q), sh = __ldg(sn + D / 8 + q);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float2 c_lo = h ? make_float2(cl.z, cl.w) : make_float2(cl.x, cl.y);
-          const float2 c_hi = h ? make_float2(ch.z, ch.w) : make_float2(ch.x, ch.y);
-          const float2 s_lo = h ? make_float2(-sl.z, -sl.w) : make_float2(-sl.x, -sl.y);
-          const float2 s_hi = h ? make_float2(sh.z, sh.w) : make_float2(sh.x, sh.y);
-          const float2 lo = y_lo[2 * q + h], hi = y_hi[2 * q + h];
-          y_lo[2 * q + h] = __ffma2_rn(lo, c_lo, __fmul2_rn(hi, s_lo));
-          y_hi[2 * q + h] = __ffma2_rn(hi, c_hi, __fmul2_rn(lo, s_hi));
-        }
-      }
     }
     reinterpret_cast<uint4*>(dst_lo)[half8] =
         make_uint4(pack_bf16x2(y_lo[0].x, y_lo[0].y), pack_bf16x2(y_lo[1].x, y_lo[1].y),
@@ -490,6 +467,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int col0 = col_base + c * 16;
         if (col0 >= p.I) break;
         if (col0 < p.s_begin || col0 >= p.s_end) continue;
+        if constexpr (PHD > 0) {
+          // a per-head segment carried to the RoPE pass: its norm (inv_rms of the head,
+          // then the per-head gamma) is applied here, before the encoding
+          if (p.ph_carry && col0 >= p.ph_begin && col0 < p.ph_end) {
+            const float inv = rsqrtf(ph_ss[c / (PHD / 16)] * (1.f / PHD) + p.eps);
+            const float2 inv2 = make_float2(inv, inv);
+            const float4* g4 = reinterpret_cast<const float4*>((col0 < p.q_end ? p.ph_q_gamma : p.ph_k_gamma) + col0 % PHD);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const float4 t = __ldg(g4 + k4);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int k = 2 * k4 + h;
+                const float2 v = make_float2(__uint_as_float(r[c * 16 + 2 * k]), __uint_as_float(r[c * 16 + 2 * k + 1]));
+                const float2 z = __fmul2_rn(__fmul2_rn(v, inv2), h ? make_float2(t.z, t.w) : make_float2(t.x, t.y));
+                r[c * 16 + 2 * k] = __float_as_uint(z.x);
+                r[c * 16 + 2 * k + 1] = __float_as_uint(z.y);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(__uint_as_float(r[c * 16 + j])));
+            continue;
+          }
+        }
         const float* g = col0 < p.q_end ? p.q_gamma : p.k_gamma;
         if (g != nullptr) {
           const float4* g4 = reinterpret_cast<const float4*>(g + (col0 < p.q_end ? col0 : col0 - p.q_end));
@@ -528,12 +529,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           // stored when its lo chunk comes up
           const int hh = c / (PHD / 16), cin = c % (PHD / 16);
           const int h0 = col_base + hh * PHD;
-          if (h0 >= p.ph_begin && h0 < p.ph_end) {
+          if (!p.ph_carry && h0 >= p.ph_begin && h0 < p.ph_end) {
             if (cin < PHD / 32) {
               const float inv = rsqrtf(ph_ss[hh] * (1.f / PHD) + p.eps);
               const float* g = h0 < p.q_end ? p.ph_q_gamma : p.ph_k_gamma;
-              per_head_pair<PHD>(r, c, c + PHD / 32, cin * 16, inv, g, p.ph_rope != 0, row, p, out_at(col0),
-                                 out_at(col0 + PHD / 2));
+              per_head_pair<PHD>(r, c, c + PHD / 32, cin * 16, inv, g, out_at(col0), out_at(col0 + PHD / 2));
             }
             continue;
           }
@@ -714,11 +714,9 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   p.out32 = (reinterpret_cast<uintptr_t>(L.out) & 31u) == 0;
   p.ph_begin = L.ph_begin;
   p.ph_end = L.ph_end;
-  p.ph_rope = L.ph_rope;
+  p.ph_carry = L.ph_carry;
   p.ph_q_gamma = L.ph_q_gamma;
   p.ph_k_gamma = L.ph_k_gamma;
-  p.cos = L.cos;
-  p.sin = L.sin;
   p.eps = L.eps;
 
   static std::once_flag attr_once;

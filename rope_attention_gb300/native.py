@@ -81,7 +81,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qkv_cte_mx_pack_weight": (i32, [P, P, i64, i64, P, sz, P]),
         "qkv_cte_mx_workspace_bytes": (i32, [ctypes.POINTER(QkvCteMxParams), ctypes.POINTER(sz)]),
         "qkv_cte_mx": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, P, P, sz, P]),
-        "qkv_cte_mx_project": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, P, P, sz, P]),
+        "qkv_cte_mx_project": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, sz, P]),
         "qkv_cte_mx_norm_rope": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, sz, P]),
         "qkv_cte_mx_status": (i32, [P, P, ctypes.POINTER(i32)]),
         "qkv_cte_mx_noalloc": (i32, [ctypes.POINTER(QkvCteMxParams), P, P, P, P, P, P, P, P, P, P, P]),
@@ -191,13 +191,12 @@ def qkv_cte_mx(params, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
 
 
-def qkv_cte_mx_project(params, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache, q_gamma,
-                       k_gamma, out, workspace, stream=None) -> None:
+def qkv_cte_mx_project(params, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out, workspace,
+                       stream=None) -> None:
     _check(load().qkv_cte_mx_project(
         ctypes.byref(params), _ptr(a, torch.uint8, "a"), _ptr(a_scale, torch.float32, "a_scale"),
         _ptr(w_packed, torch.uint8, "w_packed"), _ptr(weight_scales, torch.float32, "weight_scales"),
-        _ptr(_bits16(bias), None, "bias"), _ptr(cos_cache, torch.float32, "cos_cache"),
-        _ptr(sin_cache, torch.float32, "sin_cache"), _ptr(q_gamma, torch.float32, "q_gamma"),
+        _ptr(_bits16(bias), None, "bias"), _ptr(q_gamma, torch.float32, "q_gamma"),
         _ptr(k_gamma, torch.float32, "k_gamma"), _ptr(_bits16(out), None, "out"),
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
 

@@ -70,8 +70,8 @@ class QkvRun:
 
     def project(self, stream=None) -> None:
         native.qkv_cte_mx_project(self.params, self.a, self.a_scale, self.w_packed,
-                                  self.weight_scales, self.bias, self.cos, self.sin, self.q_gamma,
-                                  self.k_gamma, self.out, self.workspace, stream)
+                                  self.weight_scales, self.bias, self.q_gamma, self.k_gamma, self.out,
+                                  self.workspace, stream)
 
     def norm_rope(self, stream=None) -> None:
         native.qkv_cte_mx_norm_rope(self.params, self.cos, self.sin, self.out, self.workspace, stream)

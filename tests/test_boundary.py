@@ -38,7 +38,7 @@ def test_exports_every_declared_function(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in the header but not exported"
     assert sorted(names) == sorted(native.EXPORTS)
-    assert native.ra_abi_version() == 6
+    assert native.ra_abi_version() == 7
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -123,16 +123,15 @@ def test_qkv_call_rejected(L, over, code):
 def test_project_and_norm_rejections(L):
     p = qp()
     assert ws_bytes(L, p) > 8   # the 8-byte workspace below is always refused
-    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, None, None, A16, A16, A16, A16,
-                              8, None)
+    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, A16, A16, A16, A16, 8, None)
     assert st == -4
-    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, None, None, None, A16, A16, A16,
+    st = L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, None, A16, A16, A16,
                               ws_bytes(L, p), None)
     assert st == -1                                          # q_norm needs q_gamma
     ph = qp(q_norm=2, k_norm=2, head_dim=64)
-    st = L.qkv_cte_mx_project(ctypes.byref(ph), A16, A16, A16, None, None, None, None, A16, A16, A16, A16,
+    st = L.qkv_cte_mx_project(ctypes.byref(ph), A16, A16, A16, None, None, A16, None, A16, A16,
                               ws_bytes(L, ph), None)
-    assert st == -1 and b"cos/sin" in L.ra_last_error()   # per-head norm + RoPE needs cos/sin here
+    assert st == -1 and b"k_gamma" in L.ra_last_error()     # the per-head K norm needs its gamma
     st = L.qkv_cte_mx_norm_rope(ctypes.byref(p), None, A16, A16, A16, ws_bytes(L, p), None)
     assert st == -1                                          # fused_rope needs cos/sin
     v = ctypes.c_int32()
