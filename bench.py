@@ -54,7 +54,7 @@ def load_peaks():
 # changes the figure no longer describes it and the bench reports null.
 K1_SOURCES = ("rope_attention_gb300/csrc/qkv_project.cu", "rope_attention_gb300/csrc/ptx.cuh",
               "rope_attention_gb300/csrc/internal.h")
-K1_DRAM_BYTES = {("wan720", "98cc85e37c5109d7"): 2002325248 + 2354397440}
+K1_DRAM_BYTES = {("wan720", "7c2b34efc3b18a80"): 2148415232 + 2360175104}
 
 
 def k1_source_digest() -> str:
