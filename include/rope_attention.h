@@ -296,6 +296,9 @@ typedef struct {
                            * with quantisation, per the page's combination table)    */
   int32_t rope_s_broadcast;  /* 1 = cos/sin are [B, N, 1, rope_size], broadcast over S */
   int64_t cache_seq_len;  /* NORM mode: Scache (>= S); ignored otherwise             */
+  int32_t k_quant_scalar; /* V1: 1 = k_rope_scale / k_rope_offset are [1] (one value for
+                           * every channel) instead of [k_w]; must be 0 in V2         */
+  int32_t c_kv_quant_scalar; /* V1: likewise for c_kv_scale / c_kv_offset             */
 } kv_rms_norm_rope_cache_params;
 
 /* One call of KvRmsNormRopeCache.
@@ -307,8 +310,10 @@ typedef struct {
  *               (PA modes: block starts / block_size) must be unique.
  *   k_cache     paged cache of width k_w = rope_size (V1) or Dkv (V2), updated in place.
  *   ckv_cache   paged cache of width c_w = rms_size (V1) or Dv (V2), updated in place.
- *   k_rope_scale / k_rope_offset  fp32 per channel: [k_w] (V1) or [N, k_w] (V2); NULL = absent.
- *   c_kv_scale   / c_kv_offset    fp32 per channel: [c_w] (V1) or [N, c_w] (V2); NULL = absent.
+ *   k_rope_scale / k_rope_offset  fp32 per channel: [k_w] (V1; [1] with k_quant_scalar)
+ *               or [N, k_w] (V2); NULL = absent.
+ *   c_kv_scale   / c_kv_offset    fp32 per channel: [c_w] (V1; [1] with c_kv_quant_scalar)
+ *               or [N, c_w] (V2); NULL = absent.
  *               An offset without its scale is rejected.
  *   v_optional  [B, N, S, Dv] bf16; required in V2, must be NULL in V1.
  *   k_rope      [B, N, S, k_w] and c_kv [B, N, S, c_w], kv_dtype: written iff outputs

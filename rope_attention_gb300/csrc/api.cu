@@ -268,7 +268,7 @@ extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 7; }
+int32_t ra_abi_version(void) { return 8; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
@@ -462,6 +462,12 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
     if ((!qk || !qv) && p->block_size % 16 != 0)
       return fail(RA_ERR_INVALID_ARG, "2-byte caches need block_size %% 16 == 0");
   }
+  if ((p->k_quant_scalar != 0 && p->k_quant_scalar != 1) || (p->c_kv_quant_scalar != 0 && p->c_kv_quant_scalar != 1))
+    return fail(RA_ERR_INVALID_ARG, "k_quant_scalar and c_kv_quant_scalar must be 0 or 1");
+  if (p->variant == 2 && (p->k_quant_scalar || p->c_kv_quant_scalar))
+    return fail(RA_ERR_INVALID_ARG, "V2 quantisation parameters are [N, D]; the [1] form is V1 only");
+  if ((p->k_quant_scalar && !qk) || (p->c_kv_quant_scalar && !qv))
+    return fail(RA_ERR_INVALID_ARG, "a [1] quantisation parameter flag needs its scale");
   if (p->rope_s_broadcast != 0 && p->rope_s_broadcast != 1)
     return fail(RA_ERR_INVALID_ARG, "rope_s_broadcast must be 0 or 1");
   if (!(p->epsilon >= 0.f) || !std::isfinite(p->epsilon))
@@ -512,6 +518,8 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
   L.kq = kq;
   L.vq = vq;
   L.rope_bcast = p->rope_s_broadcast;
+  L.k_scalar = p->k_quant_scalar;
+  L.v_scalar = p->c_kv_quant_scalar;
   L.cache_seq = mode == RA_CACHE_NORM ? p->cache_seq_len : 0;
   L.wait_ns = g_wait_ns.load();
   L.stall_loads = g_stall_next_kv.exchange(0);

@@ -118,15 +118,22 @@ struct QuantTab {
   const float4* offset;
   int odd, step, stride;
 };
-// Fills one table (every head) from the per-channel scale / offset arrays.
+// Fills one table (every head) from the per-channel scale / offset arrays, or
+// from their one value when they are [1] (`scalar`).
 __device__ __forceinline__ void fill_table(float4* ts, float4* to, const float* scale, const float* offset,
-                                           int heads, int width, TabLayout l) {
+                                           int heads, int width, TabLayout l, bool scalar) {
   const int groups = width / 4, n = heads * groups;
   for (int e = threadIdx.x; e < n; e += blockDim.x) {
     const int hd = e / groups, u = e - hd * groups;
     const int pos = hd * l.stride + ((u & 1) ? l.odd : 0) + (u >> 1) * l.step;
-    ts[pos] = __ldg(reinterpret_cast<const float4*>(scale) + e);
-    to[pos] = offset ? __ldg(reinterpret_cast<const float4*>(offset) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (scalar) {
+      const float s0 = __ldg(scale), o0 = offset ? __ldg(offset) : 0.f;
+      ts[pos] = make_float4(s0, s0, s0, s0);
+      to[pos] = make_float4(o0, o0, o0, o0);
+    } else {
+      ts[pos] = __ldg(reinterpret_cast<const float4*>(scale) + e);
+      to[pos] = offset ? __ldg(reinterpret_cast<const float4*>(offset) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -483,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
       next += RPG;
     }
   }
-  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, kw, kl);
-  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, cw, vl);
+  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, kw, kl, p.k_scalar != 0);
+  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, cw, vl, p.v_scalar != 0);
   __syncthreads();
 
   for (int64_t base = r_begin; base < r_end; base += DEPTH * RPG) {
@@ -589,8 +596,8 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, T::KW, kl);
-  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, T::CW, vl);
+  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, T::KW, kl, p.k_scalar != 0);
+  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, T::CW, vl, p.v_scalar != 0);
   __syncthreads();
 
   if (warp == kConsumerWarps) {

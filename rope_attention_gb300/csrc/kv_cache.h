@@ -38,6 +38,7 @@ struct KvLaunch {
   int32_t out_kv;              // write k_rope / c_kv
   int32_t f16;                 // inputs (and unquantised caches, outputs) are fp16
   int32_t kq, vq;              // KvQuant of the k / ckv cache
+  int32_t k_scalar, v_scalar;  // V1: the component's scale / offset are one value [1]
   int32_t rope_bcast;          // cos/sin are [B, N, 1, R]
   int64_t wait_ns;             // time limit of each pipeline wait (staged kernel)
   int32_t stall_loads;         // test hook: the staged kernel issues no copies, so its waits run out

@@ -55,7 +55,8 @@ class KvRmsNormRopeCacheParams(ctypes.Structure):
                 ("kv_dtype", ctypes.c_int32), ("k_cache_dtype", ctypes.c_int32),
                 ("ckv_cache_dtype", ctypes.c_int32), ("epsilon", ctypes.c_float),
                 ("is_output_kv", ctypes.c_int32), ("rope_s_broadcast", ctypes.c_int32),
-                ("cache_seq_len", ctypes.c_int64)]
+                ("cache_seq_len", ctypes.c_int64), ("k_quant_scalar", ctypes.c_int32),
+                ("c_kv_quant_scalar", ctypes.c_int32)]
 
 
 _LIB = None

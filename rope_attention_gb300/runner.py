@@ -96,7 +96,9 @@ class KvRun:
             k_cache_dtype=self.QTYPES[c.k_qtype] if qk else half,
             ckv_cache_dtype=self.QTYPES[c.v_qtype] if qv else half,
             epsilon=c.eps, is_output_kv=1 if c.is_output_kv else 0,
-            rope_s_broadcast=1 if c.cos.shape[2] == 1 and c.S > 1 else 0, cache_seq_len=c.cache_seq)
+            rope_s_broadcast=1 if c.cos.shape[2] == 1 and c.S > 1 else 0, cache_seq_len=c.cache_seq,
+            k_quant_scalar=1 if qk and c.k_scale.shape == (1,) else 0,
+            c_kv_quant_scalar=1 if qv and c.v_scale.shape == (1,) else 0)
         dev = lambda x: to_dev(x, device, c.dtype)
         self.kv = dev(c.kv)
         self.gamma = dev(c.gamma)

@@ -366,7 +366,7 @@ def make_kv(name: str, seed: int, *, variant: int, B: int, N: int, S: int, Dkv: 
             offsets: bool = True, with_v: bool | None = None, eps: float = 1e-5,
             is_output_kv: bool = True, skip_frac: float = 0.0, dtype: str = "bf16",
             k_qtype: str = "int8", v_qtype: str = "int8", rope_broadcast: bool = False,
-            cache_seq: int | None = None) -> KVCase:
+            cache_seq: int | None = None, k_scalar: bool = False, v_scalar: bool = False) -> KVCase:
     """Synthetic KvRmsNormRopeCache call.
 
     kv, v ~ N(0,1); gamma ~ U(0.5,1.5); cos/sin from position s with ladder
@@ -380,8 +380,10 @@ def make_kv(name: str, seed: int, *, variant: int, B: int, N: int, S: int, Dkv: 
       PA_BLK_BNSD: per block of block_size tokens, the start slot of a distinct
         random cache block (block id * block_size), shape [B * ceil(S / block_size)];
     a fraction ``skip_frac`` of the entries replaced by -1.  Quant scales
-    ~ U(10,40), offsets ~ U(-2,2); a quantised cache is int8 or FP8 (``k_qtype``,
-    ``v_qtype``).  Caches start filled with a sentinel the op never writes.
+    ~ U(10,40), offsets ~ U(-2,2), per channel ([D] in V1, [N, D] in V2) or, with
+    ``k_scalar`` / ``v_scalar`` (V1), one value [1] for the whole component; a
+    quantised cache is int8 or FP8 (``k_qtype``, ``v_qtype``).  Caches start
+    filled with a sentinel the op never writes.
     """
     enc = {"bf16": encode_bf16, "fp16": encode_fp16}[dtype]
     rms = Dkv - rope_size if variant == 1 else Dkv
@@ -414,8 +416,8 @@ def make_kv(name: str, seed: int, *, variant: int, B: int, N: int, S: int, Dkv: 
     v = None
     if with_v if with_v is not None else (variant == 2):
         v = enc(stream(seed, 4).standard_normal((B, N, S, Dv), dtype=np.float32))
-    qshape_k = (kw,) if variant == 1 else (N, kw)
-    qshape_v = (cw,) if variant == 1 else (N, cw)
+    qshape_k = ((1,) if k_scalar else (kw,)) if variant == 1 else (N, kw)
+    qshape_v = ((1,) if v_scalar else (cw,)) if variant == 1 else (N, cw)
     ks = stream(seed, 5).uniform(10, 40, qshape_k).astype(np.float32) if quant_k else None
     ko = stream(seed, 6).uniform(-2, 2, qshape_k).astype(np.float32) if (quant_k and offsets) else None
     vs = stream(seed, 7).uniform(10, 40, qshape_v).astype(np.float32) if quant_v else None

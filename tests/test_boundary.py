@@ -38,7 +38,7 @@ def test_exports_every_declared_function(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in the header but not exported"
     assert sorted(names) == sorted(native.EXPORTS)
-    assert native.ra_abi_version() == 7
+    assert native.ra_abi_version() == 8
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -192,6 +192,10 @@ def kv_call(L, p, **over):
     (dict(k_cache_dtype=3), dict(ks=A16), -1),                  # fp32 is not a quantised cache type
     (dict(k_cache_dtype=4, ckv_cache_dtype=5, block_size=48), dict(ks=A16, vs=A16), -1),  # 1-byte: %32
     (dict(rope_s_broadcast=2), {}, -1),
+    (dict(k_quant_scalar=2, k_cache_dtype=2), dict(ks=A16), -1),   # flag is 0 or 1
+    (dict(k_quant_scalar=1), {}, -1),                           # [1] flag without its scale
+    (dict(variant=2, N=2, Dkv=192, Dv=128, k_cache_dtype=2, k_quant_scalar=1),
+     dict(v=A16, ks=A16), -1),                                  # V2 parameters are [N, D]
     (dict(is_output_kv=1), {}, -1),                             # needs k_rope / c_kv
     (dict(epsilon=-1.0), {}, -1),
     ({}, dict(kv=A16 + 2), -3), ({}, dict(index=A16 + 4), -3), ({}, dict(kc=A16 + 8), -3),

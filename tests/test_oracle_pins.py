@@ -720,9 +720,39 @@ def check_kv_fp8_caches():
     check_kv_mode(case)
 
 
+def check_kv_scalar_quant_params():
+    """V1 quantisation parameters of shape [1] (the page's shape table): the same
+    caches as [D] arrays filled with that value, and every written int8 code is
+    torch's round(x * s + o).clamp(-128, 127) of the unquantised output."""
+    case = synth.make_kv("scal", 39, variant=1, B=2, N=1, S=6, Dkv=24, Dv=16, rope_size=8,
+                         block_size=4, block_num=4, quant_k=True, quant_v=True, skip_frac=0.2,
+                         k_scalar=True, v_scalar=True)
+    assert case.k_scale.shape == (1,) and case.v_offset.shape == (1,)
+    got = run_kv(case)
+    full = dataclasses.replace(case, k_scale=np.full(8, case.k_scale[0], np.float32),
+                               k_offset=np.full(8, case.k_offset[0], np.float32),
+                               v_scale=np.full(16, case.v_scale[0], np.float32),
+                               v_offset=np.full(16, case.v_offset[0], np.float32))
+    ref = run_kv(full)
+    for key in ("k_cache", "ckv_cache"):
+        assert np.array_equal(got[key], ref[key]), key
+    for cache, out, sc, of, written in (("k_cache", "k_rope", case.k_scale, case.k_offset, "k_written"),
+                                        ("ckv_cache", "c_kv", case.v_scale, case.v_offset, "ckv_written")):
+        x = torch.from_numpy(got[out])                                       # [B, N, S, D]
+        codes = torch.round(x * float(sc[0]) + float(of[0])).clamp(-128, 127).to(torch.int64)
+        p = okv.token_slots(case.index, "PA_BNSD", np.repeat(np.arange(2), 6), np.tile(np.arange(6), 2), 6, 4)
+        for t, slot in enumerate(p):
+            if slot < 0:
+                continue
+            b, s_ = divmod(t, 6)
+            row = got[cache][slot // 4, 0, slot % 4]
+            assert np.array_equal(row, codes[b, 0, s_].numpy()), (cache, t)
+        assert got[written].sum() > 0
+
+
 @pytest.mark.parametrize("check", [check_fp8_encoders_vs_torch, check_kv_norm_mode, check_kv_norm_v1_no_outputs,
                                    check_kv_blk_mode, check_kv_rope_broadcast, check_kv_fp16_inputs,
-                                   check_kv_fp8_caches])
+                                   check_kv_fp8_caches, check_kv_scalar_quant_params])
 def test_kv_variants(check):
     check()
 

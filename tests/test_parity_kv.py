@@ -99,6 +99,15 @@ VARIANTS = [
                              quant_k=True, quant_v=True, k_qtype="e5m2", v_qtype="e4m3", offsets=False)),
     ("fp8_fp16_norm_v2", dict(variant=2, B=2, N=2, S=40, Dkv=192, Dv=128, cache_mode="Norm", cache_seq=40,
                               dtype="fp16", quant_k=True, quant_v=True, k_qtype="e4m3", v_qtype="int8")),
+    # V1 quantisation parameters of shape [1]: pipelined (576/64 int8), register (other dims), FP8
+    ("scalar_v1_int8", dict(variant=1, B=2, N=1, S=45, Dkv=576, Dv=512, block_size=32, block_num=4,
+                            quant_k=True, quant_v=True, k_scalar=True, v_scalar=True)),
+    ("scalar_v1_k_only_sym", dict(variant=1, B=2, N=1, S=33, Dkv=576, Dv=512, block_size=32, block_num=4,
+                                  quant_k=True, quant_v=True, k_scalar=True, offsets=False)),
+    ("scalar_v1_small_dims", dict(variant=1, B=2, N=1, S=21, Dkv=136, Dv=128, rope_size=8, block_size=32,
+                                  block_num=2, quant_k=True, quant_v=True, k_scalar=True, v_scalar=True)),
+    ("scalar_fp8_v1", dict(variant=1, B=2, N=1, S=30, Dkv=576, Dv=512, block_size=32, block_num=2,
+                           quant_k=True, quant_v=True, k_qtype="e4m3", v_qtype="e5m2", v_scalar=True)),
 ]
 
 
