@@ -38,6 +38,9 @@
  *    caller reads after synchronising (qkv_cte_mx_status,
  *    kv_rms_norm_rope_cache_status, dev_error_count).
  *  - bf16 values are passed as their 16-bit patterns (uint16_t).
+ *  - The compute calls launch kernels only (no allocation, no synchronisation),
+ *    so after one eager call per device they can be captured into a CUDA graph
+ *    and replayed; the status readers synchronise and cannot be captured.
  */
 #ifndef ROPE_ATTENTION_H_
 #define ROPE_ATTENTION_H_
