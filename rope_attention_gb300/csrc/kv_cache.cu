@@ -13,8 +13,11 @@
 // Quantisation uses the fp32 value (before any bf16 rounding); round() is
 // round-half-to-even.
 //
-// GB300 mapping: an HBM stream of short rows (0.6-1.4 KB); the kernel is built
-// to keep bytes in flight with few instructions per byte:
+// GB300 mapping: an HBM stream of short rows (0.6-1.4 KB).  The two row shapes
+// of the common calls (V1 576 = 512 + 64, V2 192 / 128 with RoPE on 64) in the
+// paged modes with int8 or 16-bit caches run the bulk-copy pipelined kernel
+// further down; every other call runs this register kernel, built to keep bytes
+// in flight with few instructions per byte:
 //  * persistent warps, each owning a contiguous range of (b, n, s) rows and
 //    walking (b, n, s) incrementally (no integer division per row);
 //  * a warp works on 32 / LPR rows at once, LPR = 8, 16 or 32 lanes per row
@@ -24,9 +27,6 @@
 //  * two row groups in registers per lane: one is processed while the next loads;
 //  * the per-channel quantisation scales and offsets (per head in V2) are
 //    staged once per block in shared memory, laid out for conflict-free reads;
-//  * the two common row shapes (V1 576 = 512 + 64, V2 192 / 128 with RoPE on 64)
-//    are compiled in for the paged int8 / 16-bit calls, so that addressing and the
-//    per-chunk tests fold to constants; other shapes read theirs at run time;
 //  * packed fp32x2 arithmetic; int8 codes are rounded with cvt.rni and packed
 //    with saturation by cvt.pack.sat;
 //  * lane j < rope_size/8 of a row owns interleaved pairs 4j..4j+3, whose outputs
@@ -169,12 +169,10 @@ __device__ __forceinline__ void store4(int32_t qt, void* row_base, int ch, float
   }
 }
 
-// Row shapes compiled in for the common calls, so that the per-row addressing and
-// the chunk tests fold to constants (0: every size read at run time).
+// The row shapes of the pipelined kernel, compiled in so that the per-row
+// addressing and the chunk tests fold to constants.
 template <int SHAPE>
-struct RowShape {
-  static constexpr int dkv = 0, dv = 0, r = 0;
-};
+struct RowShape;
 template <>
 struct RowShape<1> {  // V1, the MLA combined kv: 512 normed + 64 RoPE channels
   static constexpr int dkv = 576, dv = 512, r = 64;
@@ -227,7 +225,7 @@ struct Cursor {
 // GEN: the general kernel (Norm and PA_BLK_BNSD modes, S-broadcast cos/sin, FP8
 // caches); without it only PA / PA_BNSD with int8 or 16-bit caches is compiled in.
 // JLO: lane = g * LPR + j (a row's lanes adjacent), else lane = j * (32 / LPR) + g.
-template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE, bool JLO = false>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, bool JLO = false>
 struct KvRows {
   const KvLaunch& p;
   KvAux aux;
@@ -423,7 +421,7 @@ size_t quant_table_bytes(const KvLaunch& L, bool qk, bool qv, bool split) {
 
 constexpr int kMinBlocks = 3;  // 12 warps per SM: up to 168 registers per thread
 
-template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     kv_rms_norm_rope_cache_kernel(const KvLaunch p, const KvAux aux) {
   extern __shared__ float4 tabs[];
@@ -432,10 +430,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   const int lane = threadIdx.x & 31;
   const int g = lane % RPG, j = lane / RPG;
   const int64_t rows = p.B * p.N * p.S;
-  using Sh = RowShape<SHAPE>;
-  const int R = Sh::r ? Sh::r : p.R;
-  const int dkv = Sh::dkv ? Sh::dkv : static_cast<int>(p.Dkv);
-  const int dv = Sh::dv ? Sh::dv : static_cast<int>(p.Dv);
+  const int R = p.R;
+  const int dkv = static_cast<int>(p.Dkv), dv = static_cast<int>(p.Dv);
   const int rms = VARIANT == 1 ? dkv - R : dkv;
   const int kw = VARIANT == 1 ? R : dkv;
   const int cw = VARIANT == 1 ? rms : dv;
@@ -461,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   float4* vs = ko + ku;
   float4* vo = vs + vu;
   const int64_t slots = p.mode == kModeNorm ? p.cache_seq : p.block_num * p.block_size;
-  const KvRows<VARIANT, LPR, CPL, F16, GEN, SHAPE> w{p, aux, j, dkv, dv, R, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
+  const KvRows<VARIANT, LPR, CPL, F16, GEN> w{p, aux, j, dkv, dv, R, rms, rms / 8, VARIANT == 2 ? cw / 8 : 0, R / 8, R / 2, kw, cw,
                                          slots, gam, QuantTab{ks, ko, kl.odd, kl.step, kl.stride},
                                          QuantTab{vs, vo, vl.odd, vl.step, vl.stride}};
 
@@ -648,7 +644,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
 #pragma unroll
   for (int i = 0; i < T::CPL; ++i) gam[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * (j + T::LPR * i)));
   const int64_t slots = p.block_num * p.block_size;
-  const KvRows<VARIANT, T::LPR, T::CPL, F16, false, VARIANT, true> w{
+  const KvRows<VARIANT, T::LPR, T::CPL, F16, false, true> w{
       p, aux, j, T::DKV, T::DV, T::R, T::RMS, T::RMS / 8, VARIANT == 2 ? T::CW / 8 : 0, T::R / 8, T::R / 2,
       T::KW, T::CW, slots, gam, QuantTab{ks, ko, kl.odd, kl.step, kl.stride},
       QuantTab{vs, vo, vl.odd, vl.step, vl.stride}};
@@ -730,9 +726,9 @@ unsigned persistent_grid(K kernel, int64_t rows, size_t smem) {
   return static_cast<unsigned>(want < cap ? want : cap);
 }
 
-template <int VARIANT, int LPR, int CPL, bool F16, bool GEN, int SHAPE>
+template <int VARIANT, int LPR, int CPL, bool F16, bool GEN>
 cudaError_t launch_one(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
-  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL, F16, GEN, SHAPE>;
+  auto kernel = kv_rms_norm_rope_cache_kernel<VARIANT, LPR, CPL, F16, GEN>;
   const size_t smem = quant_table_bytes(L, L.kq != 0, L.vq != 0, true);
   if (smem > 48 * 1024) {
     const cudaError_t e =
@@ -749,31 +745,27 @@ template <int VARIANT, bool F16, bool GEN>
 cudaError_t launch_layout(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st) {
   if (lpr == 8) {
     switch (cpl) {
-      case 1: return launch_one<VARIANT, 8, 1, F16, GEN, 0>(L, aux, st);
-      case 2: return launch_one<VARIANT, 8, 2, F16, GEN, 0>(L, aux, st);
-      case 3: return launch_one<VARIANT, 8, 3, F16, GEN, 0>(L, aux, st);
-      case 4: return launch_one<VARIANT, 8, 4, F16, GEN, 0>(L, aux, st);
+      case 1: return launch_one<VARIANT, 8, 1, F16, GEN>(L, aux, st);
+      case 2: return launch_one<VARIANT, 8, 2, F16, GEN>(L, aux, st);
+      case 3: return launch_one<VARIANT, 8, 3, F16, GEN>(L, aux, st);
+      case 4: return launch_one<VARIANT, 8, 4, F16, GEN>(L, aux, st);
       default: return cudaErrorInvalidValue;
     }
   }
-  if (lpr == 16) return launch_one<VARIANT, 16, 4, F16, GEN, 0>(L, aux, st);
-  if (lpr == 32) return launch_one<VARIANT, 32, 4, F16, GEN, 0>(L, aux, st);
+  if (lpr == 16) return launch_one<VARIANT, 16, 4, F16, GEN>(L, aux, st);
+  if (lpr == 32) return launch_one<VARIANT, 32, 4, F16, GEN>(L, aux, st);
   return cudaErrorInvalidValue;
 }
 
-// the lean kernel with a fixed row shape, when the call has one of them
+// the pipelined kernel, when the call has one of its row shapes (and the status
+// word its waits report to is known)
 template <int VARIANT, bool F16>
 bool launch_fixed(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st, cudaError_t* err) {
   const bool shape = VARIANT == 1 ? L.Dkv == RowShape<1>::dkv && L.R == RowShape<1>::r && lpr == 16 && cpl == 4
                                    : L.Dkv == RowShape<2>::dkv && L.Dv == RowShape<2>::dv && L.R == RowShape<2>::r &&
                                          lpr == 8 && cpl == 3;
-  if (!shape) return false;
-  if (L.status != nullptr && L.B * L.N * L.S < (int64_t(1) << 31) - kTileRows) {
-    *err = launch_staged<VARIANT, F16>(L, aux, st);
-    return true;
-  }
-  *err = VARIANT == 1 ? launch_one<VARIANT, 16, 4, F16, false, 1>(L, aux, st)
-                      : launch_one<VARIANT, 8, 3, F16, false, 2>(L, aux, st);
+  if (!shape || L.status == nullptr || L.B * L.N * L.S >= (int64_t(1) << 31) - kTileRows) return false;
+  *err = launch_staged<VARIANT, F16>(L, aux, st);
   return true;
 }
 
