@@ -230,7 +230,8 @@ def run_ours(args):
         e2e = measure_e2e(q, k, qcase, kcase, args, ws)
     # rows measured outside the step come last, so their buffers cannot disturb it
     nxt = {} if args.no_next else {"row_quantize_e4m3": time_row_quantize(qcase, args, hbm),
-                                   "qkv_cte_mx_per_head": time_per_head(q, args, fp8_peak)}
+                                   "qkv_cte_mx_per_head": time_variant(q, args, fp8_peak, "per_head"),
+                                   "qkv_cte_mx_nbsd": time_variant(q, args, fp8_peak, "nbsd")}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
@@ -297,40 +298,54 @@ def time_row_quantize(qcase, args, hbm_gbs):
             "note": "measured alone, not part of the step"}
 
 
-def time_per_head(q, args, fp8_peak):
-    """The per-head qk-norm variant (each head normed by its own RMS, gamma [head_dim],
-    then the rotate-half RoPE) on the workload's projection: the step's inputs and
-    weights with q_norm = k_norm = RMS_PER_HEAD, projection + RoPE pass timed alone
-    (CUDA events over K calls after W warm-ups)."""
+def time_variant(q, args, fp8_peak, which):
+    """A variant of the step's projection + second pass on the same inputs and
+    weights, timed alone (CUDA events over K calls after W warm-ups):
+      per_head  q_norm = k_norm = RMS_PER_HEAD (each head normed by its own RMS,
+                gamma [head_dim]), then the rotate-half RoPE;
+      nbsd      the output layout [I / head_dim, B, S, head_dim] of the
+                cross-attention calls."""
     import torch
     from rope_attention_gb300 import native, runner, synth
     c = q.case
     pp = native.QkvCteMxParams.from_buffer_copy(q.params)
-    pp.q_norm = pp.k_norm = native.RA_NORM_RMS_PER_HEAD
-    qg = runner.to_dev(synth.stream(97, 0).uniform(0.5, 1.5, c.head_dim).astype("float32"))
-    kg = runner.to_dev(synth.stream(97, 1).uniform(0.5, 1.5, c.head_dim).astype("float32"))
+    qg, kg, out = q.q_gamma, q.k_gamma, q.out
+    if which == "per_head":
+        pp.q_norm = pp.k_norm = native.RA_NORM_RMS_PER_HEAD
+        qg = runner.to_dev(synth.stream(97, 0).uniform(0.5, 1.5, c.head_dim).astype("float32"))
+        kg = runner.to_dev(synth.stream(97, 1).uniform(0.5, 1.5, c.head_dim).astype("float32"))
+        note = f"q_norm = k_norm = RMS_PER_HEAD (gamma [{c.head_dim}])"
+    else:
+        pp.output_layout = native.RA_LAYOUT_NBSD
+        out = q.out.view(c.I // c.head_dim, c.T, c.head_dim)
+        note = f"output layout NBSd [{c.I // c.head_dim}, {c.B}, {c.S}, {c.head_dim}]"
     ws = torch.zeros(native.qkv_cte_mx_workspace_bytes(pp), dtype=torch.uint8, device="cuda")
 
     def call():
-        native.qkv_cte_mx_project(pp, q.a, q.a_scale, q.w_packed, q.weight_scales, q.bias, qg, kg, q.out, ws)
-        native.qkv_cte_mx_norm_rope(pp, q.cos, q.sin, q.out, ws)
+        native.qkv_cte_mx_project(pp, q.a, q.a_scale, q.w_packed, q.weight_scales, q.bias, qg, kg, out, ws)
+        native.qkv_cte_mx_norm_rope(pp, q.cos, q.sin, out, ws)
 
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(args.steps):
-        call()
-    end.record()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e0, e1, e2 in ev:
+        e0.record()
+        native.qkv_cte_mx_project(pp, q.a, q.a_scale, q.w_packed, q.weight_scales, q.bias, qg, kg, out, ws)
+        e1.record()
+        native.qkv_cte_mx_norm_rope(pp, q.cos, q.sin, out, ws)
+        e2.record()
     torch.cuda.synchronize()
-    assert native.qkv_cte_mx_status(ws) == 0, "per-head call reported a wait timeout"
-    ms = start.elapsed_time(end) / args.steps
+    k1_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in ev)
+    k2_ms = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in ev)
+    ms = ev[0][0].elapsed_time(ev[-1][2]) / args.steps
+    assert native.qkv_cte_mx_status(ws) == 0, f"{which} call reported a wait timeout"
     tf = c.flops / (ms * 1e-3) / 1e12
     del ws
     return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4),
-            "note": f"q_norm = k_norm = RMS_PER_HEAD (gamma [{c.head_dim}]) on the step's projection, "
-                    "projection + RoPE pass, measured alone, not part of the step"}
+            "projection_ms": round(k1_ms, 4), "second_pass_ms": round(k2_ms, 4),
+            "note": f"{note} on the step's projection, projection + second pass, measured alone, "
+                    "not part of the step"}
 
 
 def measure_e2e(q, k, qcase, kcase, args, ws):
