@@ -231,7 +231,8 @@ def run_ours(args):
     # rows measured outside the step come last, so their buffers cannot disturb it
     nxt = {} if args.no_next else {"row_quantize_e4m3": time_row_quantize(qcase, args, hbm),
                                    "qkv_cte_mx_per_head": time_variant(q, args, fp8_peak, "per_head"),
-                                   "qkv_cte_mx_nbsd": time_variant(q, args, fp8_peak, "nbsd")}
+                                   "qkv_cte_mx_nbsd": time_variant(q, args, fp8_peak, "nbsd"),
+                                   **time_kv_variants(kcase, args, hbm)}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
@@ -346,6 +347,44 @@ def time_variant(q, args, fp8_peak, which):
             "projection_ms": round(k1_ms, 4), "second_pass_ms": round(k2_ms, 4),
             "note": f"{note} on the step's projection, projection + second pass, measured alone, "
                     "not part of the step"}
+
+
+def time_kv_variants(kcase, args, hbm_gbs):
+    """The KvRmsNormRopeCache variants of the pages' constraint tables on the step's
+    KV shape (V2 when the step's call is V2), each timed alone: CUDA events over K
+    calls after W warm-ups, algorithmic bytes as for the step's call."""
+    import torch
+    from rope_attention_gb300 import runner, synth
+    c = kcase
+    base = dict(variant=c.variant, B=c.B, N=c.N, S=c.S, Dkv=c.Dkv, Dv=c.Dv, rope_size=c.rope_size,
+                block_size=c.block_size, is_output_kv=False)
+    variants = {
+        "kv_fp8_e4m3_caches": dict(quant_k=True, quant_v=True, k_qtype="e4m3", v_qtype="e4m3"),
+        "kv_pa_blk_bnsd": dict(cache_mode="PA_BLK_BNSD", quant_k=True, quant_v=True),
+        "kv_norm_mode": dict(cache_mode="Norm", quant_k=True, quant_v=True),
+        "kv_bf16_caches_with_outputs": dict(is_output_kv=True),
+    }
+    res = {}
+    for name, kw in variants.items():
+        case = synth.make_kv(name, 91, **{**base, **kw})
+        run = runner.KvRun(case)
+        for _ in range(args.warmup):
+            run.run()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.steps):
+            run.run()
+        end.record()
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end) / args.steps
+        nbytes = case.algorithmic_bytes()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4),
+                     "note": f"{kw}, kv {list(case.kv.shape)}, measured alone (back to back), not part of the step"}
+        del run
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_e2e(q, k, qcase, kcase, args, ws):

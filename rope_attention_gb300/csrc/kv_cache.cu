@@ -507,12 +507,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 }
 
 // ---------------------------------------------------------------- staged kernel
-// For the two common row shapes on the paged int8 / 16-bit path.  A tile of
+// For the two common row shapes, in every cache mode and cache type, with
+// per-token cos/sin (S-broadcast tables take the register kernel).  A tile of
 // kTileRows consecutive (b, n, s) rows is one contiguous span in each of kv, v,
 // cos and sin, so one lane of a producer warp moves it into shared memory with
 // four bulk copies (cp.async.bulk, completion counted by the stage's mbarrier),
 // kStages - 1 tiles ahead of four consumer warps.  The producer warp also looks up
-// each row's head and cache slot.  The consumers run the same row arithmetic as
+// each row's head, its index entry (per token, or per block of block_size tokens
+// in PA_BLK_BNSD) and the row's batch (Norm) or place in its block (PA_BLK_BNSD).  The consumers run the same row arithmetic as
 // the kernel above on operands read from shared memory, with a row's lanes
 // adjacent so that those reads are free of bank conflicts.  Every wait has a time
 // limit: when one runs out the block records it in the status word and leaves,
@@ -527,7 +529,7 @@ __device__ int32_t g_kv_status;
 
 // Shared-memory plan of the staged kernel, in bytes from the dynamic base.
 struct StagedPlan {
-  uint32_t tables, stage_bytes, stages, slots, heads, bars, flag, total;
+  uint32_t tables, stage_bytes, stages, slots, heads, auxs, bars, flag, total;
 };
 __host__ __device__ inline StagedPlan staged_plan(uint32_t table_bytes, uint32_t stage_bytes) {
   StagedPlan pl;
@@ -536,7 +538,8 @@ __host__ __device__ inline StagedPlan staged_plan(uint32_t table_bytes, uint32_t
   pl.stages = (table_bytes + 127u) & ~127u;
   pl.slots = pl.stages + kStages * stage_bytes;
   pl.heads = pl.slots + kStages * kTileRows * 8;
-  pl.bars = pl.heads + kStages * kTileRows * 4;
+  pl.auxs = pl.heads + kStages * kTileRows * 4;
+  pl.bars = pl.auxs + kStages * kTileRows * 4;
   pl.flag = pl.bars + 2 * kStages * 8;
   pl.total = pl.flag + 16;
   return pl;
@@ -561,7 +564,8 @@ struct StagedShape {
   static_assert(RMS / 8 <= LPR * CPL && Sh::dv / 8 <= LPR * CPL && R / 8 <= LPR, "lane layout holds the row");
 };
 
-template <int VARIANT, bool F16>
+// GEN: Norm / PA_BLK_BNSD addressing and FP8 caches compiled in
+template <int VARIANT, bool F16, bool GEN>
 __global__ void __launch_bounds__(kStagedThreads, 3)
     kv_staged_kernel(const KvLaunch p, const KvAux aux, const uint32_t tiles) {
   using T = StagedShape<VARIANT>;
@@ -579,6 +583,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   float4* vo = vs + vu;
   int64_t* slot_s = reinterpret_cast<int64_t*>(smem + pl.slots);
   int32_t* head_s = reinterpret_cast<int32_t*>(smem + pl.heads);
+  int32_t* aux_s = reinterpret_cast<int32_t*>(smem + pl.auxs);
   const uint32_t bars = smem_u32(smem + pl.bars);  // full[kStages], then empty[kStages]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pl.flag);
   const uint32_t stage0 = smem_u32(smem + pl.stages);
@@ -619,12 +624,21 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
           bulk_load(dst + T::KV_B + T::V_B + T::CS_B, p.sin + static_cast<size_t>(r0) * T::R, nr * T::R * 2, full);
         }
       }
-      if (lane < static_cast<int>(nr)) {  // row r0 + lane: its head and its token's cache slot
+      if (lane < static_cast<int>(nr)) {  // row r0 + lane: its head and its token's index entry
         const uint32_t r = r0 + lane;
         const uint32_t bn = r / S, sq = r - bn * S;
         const uint32_t b = bn / N;
-        slot_s[s * kTileRows + lane] = __ldg(p.index + static_cast<int64_t>(b) * S + sq);
+        int64_t ipos = static_cast<int64_t>(b) * S + sq;
+        int32_t ax = 0;
+        if (GEN && p.mode == kModeNorm) ax = static_cast<int32_t>(b);
+        if (GEN && p.mode == kModePaBlkBnsd) {
+          const uint32_t blk = aux.bs_shift >= 0 ? sq >> aux.bs_shift : sq / static_cast<uint32_t>(p.block_size);
+          ipos = static_cast<int64_t>(b) * aux.blocks_per_batch + blk;
+          ax = static_cast<int32_t>(sq - blk * static_cast<uint32_t>(p.block_size));
+        }
+        slot_s[s * kTileRows + lane] = __ldg(p.index + ipos);
         head_s[s * kTileRows + lane] = static_cast<int32_t>(bn - b * N);
+        aux_s[s * kTileRows + lane] = ax;
       }
       mbar_arrive(full);  // each lane releases its own writes above
     }
@@ -643,8 +657,8 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   uint4 gam[T::CPL];
 #pragma unroll
   for (int i = 0; i < T::CPL; ++i) gam[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * (j + T::LPR * i)));
-  const int64_t slots = p.block_num * p.block_size;
-  const KvRows<VARIANT, T::LPR, T::CPL, F16, false, true> w{
+  const int64_t slots = GEN && p.mode == kModeNorm ? p.cache_seq : p.block_num * p.block_size;
+  const KvRows<VARIANT, T::LPR, T::CPL, F16, GEN, true> w{
       p, aux, j, T::DKV, T::DV, T::R, T::RMS, T::RMS / 8, VARIANT == 2 ? T::CW / 8 : 0, T::R / 8, T::R / 2,
       T::KW, T::CW, slots, gam, QuantTab{ks, ko, kl.odd, kl.step, kl.stride},
       QuantTab{vs, vo, vl.odd, vl.step, vl.stride}};
@@ -684,7 +698,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
       }
       in.slot = slot_s[s * kTileRows + lr];
       in.n = head_s[s * kTileRows + lr];
-      in.aux = 0;
+      in.aux = GEN ? aux_s[s * kTileRows + lr] : 0;
       const uint32_t row = r0 + lr;
       w.process(in, row, row < rows);
     }
@@ -693,10 +707,10 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   }
 }
 
-template <int VARIANT, bool F16>
+template <int VARIANT, bool F16, bool GEN>
 cudaError_t launch_staged(const KvLaunch& L, const KvAux& aux, cudaStream_t st) {
   using T = StagedShape<VARIANT>;
-  auto kernel = kv_staged_kernel<VARIANT, F16>;
+  auto kernel = kv_staged_kernel<VARIANT, F16, GEN>;
   const StagedPlan pl =
       staged_plan(static_cast<uint32_t>(quant_table_bytes(L, L.kq != 0, L.vq != 0, T::SPLIT)), T::STAGE_B);
   const cudaError_t e =
@@ -757,15 +771,17 @@ cudaError_t launch_layout(const KvLaunch& L, const KvAux& aux, int lpr, int cpl,
   return cudaErrorInvalidValue;
 }
 
-// the pipelined kernel, when the call has one of its row shapes (and the status
-// word its waits report to is known)
+// the pipelined kernel, when the call has one of its row shapes, per-token cos/sin,
+// and the status word its waits report to is known
 template <int VARIANT, bool F16>
-bool launch_fixed(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, cudaStream_t st, cudaError_t* err) {
+bool launch_fixed(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, bool gen, cudaStream_t st,
+                  cudaError_t* err) {
   const bool shape = VARIANT == 1 ? L.Dkv == RowShape<1>::dkv && L.R == RowShape<1>::r && lpr == 16 && cpl == 4
                                    : L.Dkv == RowShape<2>::dkv && L.Dv == RowShape<2>::dv && L.R == RowShape<2>::r &&
                                          lpr == 8 && cpl == 3;
-  if (!shape || L.status == nullptr || L.B * L.N * L.S >= (int64_t(1) << 31) - kTileRows) return false;
-  *err = launch_staged<VARIANT, F16>(L, aux, st);
+  if (!shape || L.rope_bcast || L.status == nullptr || L.B * L.N * L.S >= (int64_t(1) << 31) - kTileRows)
+    return false;
+  *err = gen ? launch_staged<VARIANT, F16, true>(L, aux, st) : launch_staged<VARIANT, F16, false>(L, aux, st);
   return true;
 }
 
@@ -774,8 +790,8 @@ cudaError_t launch_variant(const KvLaunch& L, const KvAux& aux, int lpr, int cpl
   const bool gen = (L.mode != kModePa && L.mode != kModePaBnsd) || L.rope_bcast ||
                    L.kq == kQuantE4m3 || L.kq == kQuantE5m2 || L.vq == kQuantE4m3 || L.vq == kQuantE5m2;
   cudaError_t err = cudaSuccess;
-  if (!gen && (L.f16 ? launch_fixed<VARIANT, true>(L, aux, lpr, cpl, st, &err)
-                     : launch_fixed<VARIANT, false>(L, aux, lpr, cpl, st, &err)))
+  if (L.f16 ? launch_fixed<VARIANT, true>(L, aux, lpr, cpl, gen, st, &err)
+            : launch_fixed<VARIANT, false>(L, aux, lpr, cpl, gen, st, &err))
     return err;
   if (L.f16) return gen ? launch_layout<VARIANT, true, true>(L, aux, lpr, cpl, st)
                         : launch_layout<VARIANT, true, false>(L, aux, lpr, cpl, st);
