@@ -362,6 +362,7 @@ def time_kv_variants(kcase, args, hbm_gbs):
         "kv_fp8_e4m3_caches": dict(quant_k=True, quant_v=True, k_qtype="e4m3", v_qtype="e4m3"),
         "kv_pa_blk_bnsd": dict(cache_mode="PA_BLK_BNSD", quant_k=True, quant_v=True),
         "kv_norm_mode": dict(cache_mode="Norm", quant_k=True, quant_v=True),
+        "kv_rope_s_broadcast": dict(rope_broadcast=True, quant_k=True, quant_v=True),
         "kv_bf16_caches_with_outputs": dict(is_output_kv=True),
     }
     res = {}

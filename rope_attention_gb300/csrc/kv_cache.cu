@@ -507,11 +507,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 }
 
 // ---------------------------------------------------------------- staged kernel
-// For the two common row shapes, in every cache mode and cache type, with
-// per-token cos/sin (S-broadcast tables take the register kernel).  A tile of
+// For the two common row shapes, in every cache mode and cache type.  A tile of
 // kTileRows consecutive (b, n, s) rows is one contiguous span in each of kv, v,
 // cos and sin, so one lane of a producer warp moves it into shared memory with
-// four bulk copies (cp.async.bulk, completion counted by the stage's mbarrier),
+// four bulk copies (cp.async.bulk, completion counted by the stage's mbarrier;
+// with S-broadcast cos/sin only kv and v are copied, and the consumers read the
+// one cos/sin row of each (b, n), which stays cached, straight from global memory),
 // kStages - 1 tiles ahead of four consumer warps.  The producer warp also looks up
 // each row's head, its index entry (per token, or per block of block_size tokens
 // in PA_BLK_BNSD) and the row's batch (Norm) or place in its block (PA_BLK_BNSD).  The consumers run the same row arithmetic as
@@ -529,7 +530,7 @@ __device__ int32_t g_kv_status;
 
 // Shared-memory plan of the staged kernel, in bytes from the dynamic base.
 struct StagedPlan {
-  uint32_t tables, stage_bytes, stages, slots, heads, auxs, bars, flag, total;
+  uint32_t tables, stage_bytes, stages, slots, heads, auxs, bns, bars, flag, total;
 };
 __host__ __device__ inline StagedPlan staged_plan(uint32_t table_bytes, uint32_t stage_bytes) {
   StagedPlan pl;
@@ -539,7 +540,8 @@ __host__ __device__ inline StagedPlan staged_plan(uint32_t table_bytes, uint32_t
   pl.slots = pl.stages + kStages * stage_bytes;
   pl.heads = pl.slots + kStages * kTileRows * 8;
   pl.auxs = pl.heads + kStages * kTileRows * 4;
-  pl.bars = pl.auxs + kStages * kTileRows * 4;
+  pl.bns = pl.auxs + kStages * kTileRows * 4;
+  pl.bars = pl.bns + kStages * kTileRows * 4;
   pl.flag = pl.bars + 2 * kStages * 8;
   pl.total = pl.flag + 16;
   return pl;
@@ -584,6 +586,8 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   int64_t* slot_s = reinterpret_cast<int64_t*>(smem + pl.slots);
   int32_t* head_s = reinterpret_cast<int32_t*>(smem + pl.heads);
   int32_t* aux_s = reinterpret_cast<int32_t*>(smem + pl.auxs);
+  int32_t* bn_s = reinterpret_cast<int32_t*>(smem + pl.bns);  // b * N + n (S-broadcast cos/sin row)
+  const bool bcast = GEN && p.rope_bcast;
   const uint32_t bars = smem_u32(smem + pl.bars);  // full[kStages], then empty[kStages]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pl.flag);
   const uint32_t stage0 = smem_u32(smem + pl.stages);
@@ -615,13 +619,15 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
       const uint32_t nr = rows - r0 < static_cast<uint32_t>(kTileRows) ? rows - r0 : kTileRows;
       const uint32_t full = bars + 8 * s;
       if (lane == 0) {  // the copies first, so that the slot lookups below overlap them
-        mbar_expect_tx(full, nr * T::ROW_B);
+        mbar_expect_tx(full, nr * (bcast ? T::ROW_B - 4 * T::R : T::ROW_B));
         if (!p.stall_loads) {
           const uint32_t dst = stage0 + s * T::STAGE_B;
           bulk_load(dst, p.kv + static_cast<size_t>(r0) * T::DKV, nr * T::DKV * 2, full);
           if (VARIANT == 2) bulk_load(dst + T::KV_B, p.v + static_cast<size_t>(r0) * T::DV, nr * T::DV * 2, full);
-          bulk_load(dst + T::KV_B + T::V_B, p.cos + static_cast<size_t>(r0) * T::R, nr * T::R * 2, full);
-          bulk_load(dst + T::KV_B + T::V_B + T::CS_B, p.sin + static_cast<size_t>(r0) * T::R, nr * T::R * 2, full);
+          if (!bcast) {
+            bulk_load(dst + T::KV_B + T::V_B, p.cos + static_cast<size_t>(r0) * T::R, nr * T::R * 2, full);
+            bulk_load(dst + T::KV_B + T::V_B + T::CS_B, p.sin + static_cast<size_t>(r0) * T::R, nr * T::R * 2, full);
+          }
         }
       }
       if (lane < static_cast<int>(nr)) {  // row r0 + lane: its head and its token's index entry
@@ -639,6 +645,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
         slot_s[s * kTileRows + lane] = __ldg(p.index + ipos);
         head_s[s * kTileRows + lane] = static_cast<int32_t>(bn - b * N);
         aux_s[s * kTileRows + lane] = ax;
+        bn_s[s * kTileRows + lane] = static_cast<int32_t>(bn);
       }
       mbar_arrive(full);  // each lane releases its own writes above
     }
@@ -689,12 +696,22 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
         }
       }
       if (j < T::R / 8) {
-        const uint8_t* cs = st + T::KV_B + T::V_B + lr * T::R * 2;
-        const uint8_t* sn = cs + T::CS_B;
-        in.c1 = *reinterpret_cast<const uint2*>(cs + 8 * j);
-        in.c2 = *reinterpret_cast<const uint2*>(cs + T::R + 8 * j);
-        in.s1 = *reinterpret_cast<const uint2*>(sn + 8 * j);
-        in.s2 = *reinterpret_cast<const uint2*>(sn + T::R + 8 * j);
+        if (bcast) {  // cos/sin [B, N, 1, R]: the row of this (b, n)
+          const size_t off = static_cast<size_t>(bn_s[s * kTileRows + lr]) * T::R;
+          const uint16_t* cg = p.cos + off;
+          const uint16_t* sg = p.sin + off;
+          in.c1 = __ldg(reinterpret_cast<const uint2*>(cg + 4 * j));
+          in.c2 = __ldg(reinterpret_cast<const uint2*>(cg + T::R / 2 + 4 * j));
+          in.s1 = __ldg(reinterpret_cast<const uint2*>(sg + 4 * j));
+          in.s2 = __ldg(reinterpret_cast<const uint2*>(sg + T::R / 2 + 4 * j));
+        } else {
+          const uint8_t* cs = st + T::KV_B + T::V_B + lr * T::R * 2;
+          const uint8_t* sn = cs + T::CS_B;
+          in.c1 = *reinterpret_cast<const uint2*>(cs + 8 * j);
+          in.c2 = *reinterpret_cast<const uint2*>(cs + T::R + 8 * j);
+          in.s1 = *reinterpret_cast<const uint2*>(sn + 8 * j);
+          in.s2 = *reinterpret_cast<const uint2*>(sn + T::R + 8 * j);
+        }
       }
       in.slot = slot_s[s * kTileRows + lr];
       in.n = head_s[s * kTileRows + lr];
@@ -771,15 +788,15 @@ cudaError_t launch_layout(const KvLaunch& L, const KvAux& aux, int lpr, int cpl,
   return cudaErrorInvalidValue;
 }
 
-// the pipelined kernel, when the call has one of its row shapes, per-token cos/sin,
-// and the status word its waits report to is known
+// the pipelined kernel, when the call has one of its row shapes and the status word
+// its waits report to is known
 template <int VARIANT, bool F16>
 bool launch_fixed(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, bool gen, cudaStream_t st,
                   cudaError_t* err) {
   const bool shape = VARIANT == 1 ? L.Dkv == RowShape<1>::dkv && L.R == RowShape<1>::r && lpr == 16 && cpl == 4
                                    : L.Dkv == RowShape<2>::dkv && L.Dv == RowShape<2>::dv && L.R == RowShape<2>::r &&
                                          lpr == 8 && cpl == 3;
-  if (!shape || L.rope_bcast || L.status == nullptr || L.B * L.N * L.S >= (int64_t(1) << 31) - kTileRows)
+  if (!shape || L.status == nullptr || L.B * L.N * L.S >= (int64_t(1) << 31) - kTileRows)
     return false;
   *err = gen ? launch_staged<VARIANT, F16, true>(L, aux, st) : launch_staged<VARIANT, F16, false>(L, aux, st);
   return true;
