@@ -12,15 +12,17 @@ namespace ra {
 constexpr int kProjBN = 256;          // output columns per CTA-pair tile (256 rows x 256 columns)
 constexpr int kProjBK = 128;          // contraction elements (= bytes) per pipeline stage
 constexpr int kPartCols = 128;        // columns covered by one sum-of-squares partial
-constexpr int kSfChunkBytes = 512;    // 128 columns x 4 block scales, tcgen05.cp image
-constexpr int kSfStageBytes = ((kProjBN + 127) / 128) * kSfChunkBytes;
+// W's block scales of one (256-column pair tile, 128-deep K stage): a 4 KB image of
+// 128 rows x 32 bytes (TMEM lane L: the 4 block scales of columns c * 32 + L % 32,
+// c = 0..7), copied into TMEM by one tcgen05.cp 128x256b
+constexpr int kSfStageBytes = 4096;
 constexpr int kWorkspaceHeader = 256; // status word + padding, ahead of the partial sums
 
 struct ProjLaunch {
   const uint8_t* a;            // [T, H] e4m3
   const float* a_scale;        // [T]
   const uint8_t* w_t;          // [I, H] e4m3 (packed, K-major)
-  const uint8_t* sf;           // packed block-scale images (1 KB per column tile and K stage)
+  const uint8_t* sf;           // packed block-scale images (4 KB per column tile and K stage)
   const float* weight_scales;  // [I] or null
   const uint16_t* bias;        // [I] bf16 or null
   uint16_t* out;               // [T, I]: bf16, except columns [s_begin, s_end) (see below)

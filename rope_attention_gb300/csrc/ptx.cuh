@@ -223,6 +223,11 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 __device__ __forceinline__ uint64_t sdesc_scale_rows(uint32_t saddr) {
   return sdesc(saddr, 0, 128, kLayoutNone);
 }
+// 128 rows x 32 bytes in core matrices of 8 rows x 16 bytes: (row group rg, half ch)
+// at (2 rg + ch) * 128 bytes, i.e. 128 bytes between the halves, 256 between row groups
+__device__ __forceinline__ uint64_t sdesc_scale_image(uint32_t saddr) {
+  return sdesc(saddr, 128, 256, kLayoutNone);
+}
 
 // ---------------------------------------------------------------- clusters and CTA pairs
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -298,6 +303,9 @@ __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t 
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+__device__ __forceinline__ void tc_cp_pair_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 __device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)

@@ -59,7 +59,7 @@ constexpr int BK = kProjBK;
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN_HALF * BK;
-constexpr int SF_BYTES = kSfStageBytes;
+constexpr int SF_BYTES = kSfStageBytes;  // one stage's W scale image (see pack_sf_kernel)
 constexpr uint32_t STAGE_TX = 2u * (A_BYTES + B_BYTES + SF_BYTES);  // both CTAs, on the leader's barrier
 constexpr int ACC_COL = 0;
 constexpr int SFA_COL = BN;           // 4 columns of A scales
@@ -83,7 +83,7 @@ constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
 static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 static_assert(SFB_COL + 16 <= TMEM_COLS, "TMEM budget");
-static_assert(BN == 256 && SF_BYTES == 1024, "pair tile shape");
+static_assert(BN == 256 && SF_BYTES == 4096, "pair tile shape");
 static_assert(kPartCols == EPI_COLS, "one partial per epilogue warp and row");
 
 // Instruction descriptor, block-scaled kinds: A/B format E4M3 (0) in bits
@@ -94,7 +94,7 @@ constexpr uint32_t kIdesc = (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t(P
 struct Params {
   CUtensorMap tmap_a;   // [T, H] bytes, box 128 x 128, 128-byte swizzle
   CUtensorMap tmap_b;   // [I, H] bytes, box 128 x 128, 128-byte swizzle
-  CUtensorMap tmap_sf;  // scale images viewed as [rows, 256] bytes, box 256 x 2
+  CUtensorMap tmap_sf;  // scale images viewed as [rows, 256] bytes, box 256 x 16 (one image)
   const float* a_scale;
   const float* wch;
   const uint16_t* bias;
@@ -302,7 +302,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int sf_row = (nt * p.num_k + kb) * (SF_BYTES / 256);
           const uint32_t sf_dst = sSF + stage * SF_BYTES;
           tma_load_2d_pair(sf_dst, &p.tmap_sf, fb, 0, sf_row);
-          tma_load_2d_pair(sf_dst + 512u, &p.tmap_sf, fb, 0, sf_row + 2);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -327,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // since every address here is below 2^18), so the loop steps them by addition
       const uint64_t a_desc0 = sdesc_kmajor_sw128(sA);
       const uint64_t b_desc0 = sdesc_kmajor_sw128(sB);
-      const uint64_t sf_desc0 = sdesc_scale_rows(sSF);
+      const uint64_t sf_desc0 = sdesc_scale_image(sSF);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -346,8 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t sfb = tmem + SFB_COL + (kb & 1) * 8;
           const uint64_t sfd = sf_desc0 + static_cast<uint64_t>(stage * (SF_BYTES >> 4));
-          tc_cp_pair_32x128b_warpx4(sfb, sfd);
-          tc_cp_pair_32x128b_warpx4(sfb + 4, sfd + (kSfChunkBytes >> 4));
+          tc_cp_pair_128x256b(sfb, sfd);
           const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4));
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4));
 #pragma unroll
@@ -601,10 +599,12 @@ __global__ void transpose_w_kernel(const uint8_t* __restrict__ w, uint8_t* __res
   }
 }
 
-// Scale image of one (column tile, K stage): for each 128-column group g, 32
-// rows of 16 bytes; row n0, word c, byte j holds the exponent of column
-// g*128 + c*32 + n0 and 32-block j of the stage -- the layout tcgen05.cp
-// 32x128b.warpx4 turns into "TMEM lane n%32, column n/32, byte = block".
+// Scale image of one (column tile, K stage), 4 KB: 128 rows (TMEM lanes) of 32
+// bytes, stored as core matrices of 8 rows x 16 bytes, (row group, half) at
+// (2 * group + half) * 128.  Row L, word c (0..7), byte j holds the exponent of
+// column c * 32 + L % 32 of the tile and 32-block j of the stage, so that one
+// tcgen05.cp 128x256b gives "TMEM lane n % 32 (in each lane quadrant), column n / 32,
+// byte = block", the layout the block-scaled MMA reads.
 __global__ void pack_sf_kernel(const uint8_t* __restrict__ e, uint8_t* __restrict__ sf, int H, int I,
                                int num_n, int num_k) {
   const size_t total = static_cast<size_t>(num_n) * num_k * SF_BYTES;
@@ -614,9 +614,11 @@ __global__ void pack_sf_kernel(const uint8_t* __restrict__ e, uint8_t* __restric
     const size_t t = idx / SF_BYTES;
     const int kb = static_cast<int>(t % num_k);
     const int nt = static_cast<int>(t / num_k);
-    const int g = off / kSfChunkBytes, w = off % kSfChunkBytes;
-    const int n0 = w / 16, c = (w % 16) / 4, j = w % 4;
-    const int nl = g * 128 + c * 32 + n0;
+    // core matrices of 8 rows x 16 bytes: (row group rg, column half ch) at (2 rg + ch) * 128;
+    // row L (TMEM lane), word cc (column), byte j (K block): column cc * 32 + L % 32
+    const int cm = off / 128, within = off % 128;
+    const int L = (cm / 2) * 8 + within / 16, cc = (cm % 2) * 4 + (within % 16) / 4, j = within % 4;
+    const int nl = cc * 32 + L % 32;
     const int n = nt * BN + nl;
     const int hb = kb * (BK / 32) + j;
     uint8_t v = 127;
@@ -681,7 +683,7 @@ cudaError_t launch_qkv_project(const ProjLaunch& L, cudaStream_t stream, const c
   const uint64_t sf_rows = static_cast<uint64_t>(num_n) * num_k * (SF_BYTES / 256);
   if (!make_tmap_2d(&p.tmap_a, L.a, L.H, L.T, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&p.tmap_b, L.w_t, L.H, L.I, BK, BN_HALF, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&p.tmap_sf, L.sf, 256, sf_rows, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      !make_tmap_2d(&p.tmap_sf, L.sf, 256, sf_rows, 256, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) {
     *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;
   }
