@@ -27,6 +27,40 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def norm_code(norm) -> int:
+    """synth's norm flag (False, True = across heads, "per_head") as an RA_NORM_* value."""
+    if norm == "per_head":
+        return native.RA_NORM_RMS_PER_HEAD
+    return native.RA_NORM_RMS_ACROSS_HEADS if norm else native.RA_NORM_NONE
+
+
+def qkv_params(c: synth.QKVCase, layout: int = native.RA_LAYOUT_BSD) -> native.QkvCteMxParams:
+    """The qkv_cte_mx parameters of a synth.QKVCase (host only)."""
+    return native.QkvCteMxParams(
+        B=c.B, S=c.S, H=c.H, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
+        head_dim=c.head_dim, q_norm=norm_code(c.q_norm), k_norm=norm_code(c.k_norm),
+        fused_rope=1 if c.fused_rope else 0, norm_eps=c.eps, output_layout=layout)
+
+
+_KV_QTYPES = {"int8": native.RA_INT8, "e4m3": native.RA_FP8_E4M3, "e5m2": native.RA_FP8_E5M2}
+
+
+def kv_params(c: synth.KVCase) -> native.KvRmsNormRopeCacheParams:
+    """The kv_rms_norm_rope_cache parameters of a synth.KVCase (host only)."""
+    qk, qv = c.k_scale is not None, c.v_scale is not None
+    half = native.RA_FP16 if c.dtype == "fp16" else native.RA_BF16
+    return native.KvRmsNormRopeCacheParams(
+        B=c.B, N=c.N, S=c.S, Dkv=c.Dkv, Dv=c.Dv, rope_size=c.rope_size, variant=c.variant,
+        cache_mode=synth.CACHE_MODES[c.cache_mode], block_num=c.block_num,
+        block_size=c.block_size, kv_dtype=half,
+        k_cache_dtype=_KV_QTYPES[c.k_qtype] if qk else half,
+        ckv_cache_dtype=_KV_QTYPES[c.v_qtype] if qv else half,
+        epsilon=c.eps, is_output_kv=1 if c.is_output_kv else 0,
+        rope_s_broadcast=1 if c.rope_broadcast else 0, cache_seq_len=c.cache_seq,
+        k_quant_scalar=1 if qk and c.k_scale.shape == (1,) else 0,
+        c_kv_quant_scalar=1 if qv and c.v_scale.shape == (1,) else 0)
+
+
 class QkvRun:
     """Device buffers for one qkv_cte_mx call of a synth.QKVCase."""
 
@@ -34,11 +68,7 @@ class QkvRun:
                  layout: int = native.RA_LAYOUT_BSD):
         self.case = case
         c = case
-        self.params = native.QkvCteMxParams(
-            B=c.B, S=c.S, H=c.H, num_heads=c.num_heads, num_kv_heads=c.num_kv_heads,
-            head_dim=c.head_dim,
-            q_norm=self.norm_code(c.q_norm), k_norm=self.norm_code(c.k_norm),
-            fused_rope=1 if c.fused_rope else 0, norm_eps=c.eps, output_layout=layout)
+        self.params = qkv_params(c, layout)
         self.a = to_dev(c.a, device)
         self.a_scale = to_dev(c.a_scale, device)
         w = to_dev(c.w, device)
@@ -56,12 +86,6 @@ class QkvRun:
         self.out = torch.empty(shape, dtype=torch.bfloat16, device=device)
         nws = native.qkv_cte_mx_workspace_bytes(self.params)
         self.workspace = torch.zeros(nws, dtype=torch.uint8, device=device)
-
-    @staticmethod
-    def norm_code(norm) -> int:
-        if norm == "per_head":
-            return native.RA_NORM_RMS_PER_HEAD
-        return native.RA_NORM_RMS_ACROSS_HEADS if norm else native.RA_NORM_NONE
 
     def run(self, stream=None) -> None:
         native.qkv_cte_mx(self.params, self.a, self.a_scale, self.w_packed, self.weight_scales,
@@ -83,22 +107,10 @@ class QkvRun:
 class KvRun:
     """Device buffers for one kv_rms_norm_rope_cache call of a synth.KVCase."""
 
-    QTYPES = {"int8": native.RA_INT8, "e4m3": native.RA_FP8_E4M3, "e5m2": native.RA_FP8_E5M2}
-
     def __init__(self, case: synth.KVCase, device: str = "cuda"):
         self.case = c = case
         qk, qv = c.k_scale is not None, c.v_scale is not None
-        half = native.RA_FP16 if c.dtype == "fp16" else native.RA_BF16
-        self.params = native.KvRmsNormRopeCacheParams(
-            B=c.B, N=c.N, S=c.S, Dkv=c.Dkv, Dv=c.Dv, rope_size=c.rope_size, variant=c.variant,
-            cache_mode=synth.CACHE_MODES[c.cache_mode], block_num=c.block_num,
-            block_size=c.block_size, kv_dtype=half,
-            k_cache_dtype=self.QTYPES[c.k_qtype] if qk else half,
-            ckv_cache_dtype=self.QTYPES[c.v_qtype] if qv else half,
-            epsilon=c.eps, is_output_kv=1 if c.is_output_kv else 0,
-            rope_s_broadcast=1 if c.cos.shape[2] == 1 and c.S > 1 else 0, cache_seq_len=c.cache_seq,
-            k_quant_scalar=1 if qk and c.k_scale.shape == (1,) else 0,
-            c_kv_quant_scalar=1 if qv and c.v_scale.shape == (1,) else 0)
+        self.params = kv_params(c)
         dev = lambda x: to_dev(x, device, c.dtype)
         self.kv = dev(c.kv)
         self.gamma = dev(c.gamma)

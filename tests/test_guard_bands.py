@@ -115,3 +115,19 @@ def test_kv_output_bands(name, kw):
     kr.check(name + " k_rope")
     ckv.check(name + " c_kv")
     check_kv(case, run, name)
+
+
+def test_short_cache_is_refused_before_launch():
+    """A cache one block short of what the parameters address is refused by the
+    binding (the C ABI cannot see buffer sizes), and nothing is launched: the
+    caches keep their sentinel."""
+    case = synth.make_kv("guard_short", 99, variant=2, B=2, N=8, S=21, Dkv=192, Dv=128, block_size=32,
+                         block_num=2, quant_k=True, quant_v=True)
+    run = runner.KvRun(case)
+    full = run.k_cache
+    run.k_cache = full[:-1]
+    with pytest.raises(ValueError, match=r"^k_cache: the call needs"):
+        run.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(full.cpu().numpy(), case.k_cache)
+    assert np.array_equal(run.ckv_cache.cpu().numpy(), case.ckv_cache)
