@@ -465,10 +465,14 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
 
 
 def oracle_sample_time(qcase, kcase, q_rows: int, kv_batches: int):
-    """Wall time of the fp64 oracle on q_rows projection rows and kv_batches KV batches."""
+    """Wall times of the fp64 oracle, as it stands, on a deterministic sample of
+    about q_rows projection rows (all I columns; a quarter from the first rows, a
+    quarter from the last, the rest at random) and on kv_batches KV batches.
+    Returns (rows sampled, projection seconds, batches, KV seconds)."""
     import oracle
     from rope_attention_gb300 import synth
-    rows = synth.sample_rows(qcase.T, seed=5, n_head=q_rows // 4, n_tail=q_rows // 4, n_rand=q_rows // 2)
+    rows = synth.sample_rows(qcase.T, seed=5, n_head=q_rows // 4, n_tail=q_rows // 4,
+                             n_rand=q_rows - 2 * (q_rows // 4))
     c = qcase
     t0 = time.perf_counter()
     oracle.qkv_cte_mx(c.a[rows], c.a_scale[rows], c.w, c.w_block_exp, num_heads=c.num_heads,
@@ -486,18 +490,46 @@ def oracle_sample_time(qcase, kcase, q_rows: int, kv_batches: int):
         epsilon=kc.eps, k_scale=kc.k_scale, k_offset=kc.k_offset, v_scale=kc.v_scale,
         v_offset=kc.v_offset, v=None if kc.v is None else kc.v[sl], is_output_kv=kc.is_output_kv)
     t2 = time.perf_counter()
-    f_q = len(rows) / c.T
-    f_k = nb / kc.B
-    full_s = (t1 - t0) / f_q + (t2 - t1) / f_k
-    return full_s, len(rows), nb, t2 - t0
+    return len(rows), t1 - t0, nb, t2 - t1
+
+
+def fit_full_time(n1: int, t1: float, n2: int, t2: float, n_full: int):
+    """Time of n_full units from two samples of n1 < n2 units, as fixed + per_unit * n.
+    Each oracle call has a part that does not grow with the sample (the projection
+    decodes all of W to fp64; the KV call copies both caches), and scaling one
+    sample linearly would charge that part once per sample-sized slice of the
+    workload.  When timing noise makes either part negative, or there is only one
+    sample size, the larger sample is scaled linearly instead (an upper bound on
+    the time).  Returns (seconds, "fit" | "linear", fixed seconds, seconds per unit)."""
+    if n2 > n1:
+        per_unit = (t2 - t1) / (n2 - n1)
+        fixed = t1 - per_unit * n1
+        if per_unit > 0 and fixed >= 0:
+            return fixed + per_unit * n_full, "fit", fixed, per_unit
+    return t2 * n_full / n2, "linear", 0.0, t2 / n2
+
+
+def oracle_full_estimate(qcase, kcase, args, warm: bool = True):
+    """The oracle's time for the whole step, from two sample sizes of each part;
+    a small untimed call first when ``warm`` (the first call also pays one-time
+    page faults).  Returns (seconds, description of the sample)."""
+    if warm:
+        oracle_sample_time(qcase, kcase, 64, 1)
+    n1, q1, b1, k1 = oracle_sample_time(qcase, kcase, args.oracle_rows, 1)
+    n2, q2, b2, k2 = oracle_sample_time(qcase, kcase, min(qcase.T, 32 * args.oracle_rows), 2)
+    q_full, q_how, q_fixed, q_row = fit_full_time(n1, q1, n2, q2, qcase.T)
+    k_full, k_how, k_fixed, k_batch = fit_full_time(b1, k1, b2, k2, kcase.B)
+    sample = (f"oracle on {n1} and {n2} of {qcase.T} projection rows (all {qcase.I} columns) and on {b1} and "
+              f"{b2} of {kcase.B} KV batches, fp64 numpy, {q1 + k1 + q2 + k2:.1f} s timed; step time "
+              f"extrapolated as fixed + per-unit cost (projection {q_how}: {q_fixed:.2f} s + "
+              f"{1e3 * q_row:.3f} ms per row; KV {k_how}: {k_fixed:.2f} s + {k_batch:.2f} s per batch)")
+    return q_full + k_full, sample
 
 
 def cpu_baseline(qcase, kcase, args):
-    full_s, nrows, nb, wall = oracle_sample_time(qcase, kcase, args.oracle_rows, 1)
+    full_s, sample = oracle_full_estimate(qcase, kcase, args)
     return {"value": round(qcase.flops / full_s / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{nrows} of {qcase.T} projection rows (all {qcase.I} columns) + {nb} of {kcase.B} "
-                      f"KV batches, fp64 numpy, {wall:.1f} s wall; step time extrapolated linearly"}
+            "kind": "oracle", "sample": sample}
 
 
 def run_reference(args):
@@ -508,11 +540,10 @@ def run_reference(args):
     for _ in range(args.warmup):
         oracle_sample_time(qcase, kcase, 64, 1)
     times = []
-    info = None
+    sample = None
     for _ in range(args.steps):
-        full_s, nrows, nb, wall = oracle_sample_time(qcase, kcase, args.oracle_rows, 1)
+        full_s, sample = oracle_full_estimate(qcase, kcase, args, warm=False)
         times.append(full_s)
-        info = (nrows, nb, wall)
     full_s = statistics.mean(times)
     value = qcase.flops / full_s / 1e12
     line = {
@@ -522,8 +553,7 @@ def run_reference(args):
         "config": {"workload": f"{qcase.name} (S={qcase.S}, H={qcase.H}, I={qcase.I}) + {kcase.name}",
                    "global_batch": qcase.T, "seq_len": qcase.S, "parallelism": "cpu"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{info[0]} projection rows + {info[1]} KV batch per step, fp64 numpy; "
-                                   f"step time extrapolated to the full workload"},
+                         "sample": f"per step: {sample}"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -536,7 +566,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="wan720", choices=["wan720", "wan480", "small"])
-    ap.add_argument("--oracle-rows", type=int, default=128)
+    ap.add_argument("--oracle-rows", type=int, default=128,
+                    help="smaller projection-row sample of the CPU oracle timing (the larger one is 32x)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the rows measured outside the step")
