@@ -261,7 +261,7 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:  # the CPU baseline is an N=1 figure
         line["cpu_baseline"] = cpu_baseline(qcase, kcase, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
