@@ -933,3 +933,33 @@ def test_mutants(i, monkeypatch):
         except (AssertionError, ValueError):
             caught.append(check.__name__)
     assert caught, f"mutant {name}/{fn.__name__} survived every check"
+
+
+@pytest.mark.parametrize("fmt,tdtype,top", [("e4m3", torch.float8_e4m3fn, 0x7E), ("e5m2", torch.float8_e5m2, 0x7B)])
+def test_fp8_neighbours_bracket_the_value(fmt, tdtype, top):
+    """The FP8 parity rule's helper: the codes just below and above |v| (v's sign),
+    adjacent in code order, with their midpoint; torch's cast and the oracle's
+    encoder both land on one of them."""
+    decode = {"e4m3": codes.decode_e4m3, "e5m2": codes.decode_e5m2}[fmt]
+    mags = decode(np.arange(top + 1, dtype=np.uint8))
+    g = np.random.default_rng(11)
+    v = np.concatenate([mags, (mags[:-1] + mags[1:]) / 2, g.uniform(0, mags[-1], 4000),
+                        np.exp(g.uniform(np.log(mags[1]), np.log(mags[-1]), 4000))])
+    v = np.concatenate([v, -v]).astype(np.float32).astype(np.float64)  # values torch can take exactly
+    lo, hi, mid = codes.fp8_neighbours(v, fmt)
+    mlo, mhi = lo & 0x7F, hi & 0x7F
+    assert ((mhi - mlo.astype(np.int64)) <= 1).all() and (mhi >= mlo).all()
+    assert (mhi <= top).all()
+    a = np.abs(v)
+    assert (mags[mlo] <= a).all() and (a <= mags[mhi]).all()
+    assert np.array_equal(mid, (mags[mlo] + mags[mhi]) / 2)
+    sign = np.signbit(v)
+    assert np.array_equal((lo >> 7).astype(bool), sign) and np.array_equal((hi >> 7).astype(bool), sign)
+    enc = codes.encode_fp8(v, fmt)
+    assert ((enc == lo) | (enc == hi)).all()
+    ref = torch.from_numpy(v.astype(np.float32)).to(tdtype).view(torch.uint8).numpy()
+    assert ((ref == lo) | (ref == hi)).all()
+    # a value on a code comes back as that code's magnitude at the top of the bracket
+    on = np.arange(1, top + 1)
+    lo_on, hi_on, _ = codes.fp8_neighbours(mags[on], fmt)
+    assert np.array_equal(hi_on, on.astype(np.uint8)) and np.array_equal(lo_on, (on - 1).astype(np.uint8))
