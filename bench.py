@@ -144,6 +144,19 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu), or the machine type."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def dist_env():
     from rope_attention_gb300 import dist
     e = dist.env()
@@ -256,6 +269,9 @@ def run_ours(args):
                                        "frac_hbm": round(k3_gbs / hbm, 4)},
         },
         "clocks": clk.summary(),
+        "device": {"gpu": torch.cuda.get_device_name(local),
+                   "sms": torch.cuda.get_device_properties(local).multi_processor_count,
+                   "host_cpu": host_cpu_model(), "host_cores": os.cpu_count()},
         "gpu_launches": 3 * K,
         "next": nxt,
     }
