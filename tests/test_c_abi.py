@@ -61,3 +61,22 @@ def test_rejections_reach_a_c_caller_with_their_messages(c_output):
     n = ctypes.c_size_t()
     assert lib.qkv_cte_mx_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == -1
     assert lib.ra_last_error().decode() == c_output["bad_h_message"]
+
+
+def test_call_sequence_example_compiles():
+    """tests/c/example_prologue.c, the setup / step / status sequence from C with the
+    CUDA runtime (it needs a GPU to run, so it is compiled only)."""
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = None
+    for root in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if root and os.path.exists(os.path.join(root, "include", "cuda_runtime_api.h")):
+            cuda_inc = os.path.join(root, "include")
+            break
+    if cuda_inc is None:
+        pytest.skip("CUDA runtime headers not found")
+    cmd = [cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE,
+           "-isystem", cuda_inc, "-c", os.path.join(HERE, "c", "example_prologue.c"), "-o", os.devnull]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, f"{' '.join(cmd)}\n{r.stdout}\n{r.stderr}"
