@@ -15,5 +15,6 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def lib():
     """The C-ABI library through its Python binding (built on demand)."""
-    from rope_attention_gb300 import native
+    from rope_attention_gb300 import build, native
+    build.build()
     return native.load()

@@ -14,6 +14,13 @@ import torch
 
 from rope_attention_gb300 import build, native, runner, synth
 
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    """The wrappers reach the library (load()) before they marshal tensors: build it
+    if this file runs first in a fresh checkout."""
+    build.build()
+
 QKV_CASES = [
     dict(S=16, H=128, num_heads=2, num_kv_heads=2, head_dim=64),
     dict(B=2, S=9, H=256, num_heads=3, num_kv_heads=1, head_dim=128, weight_scales=True, bias=False),
@@ -117,7 +124,6 @@ def test_short_kv_cache_is_refused_before_the_device():
 
 
 def test_short_qkv_buffers_are_refused_before_the_device():
-    build.build()
     c = synth.make_qkv("short", 10, S=16, H=128, num_heads=2, num_kv_heads=2, head_dim=64)
     p = runner.qkv_params(c)
     out = torch.empty((c.T, c.I), dtype=torch.bfloat16)
