@@ -40,3 +40,23 @@ def test_fit_falls_back_to_the_linear_upper_bound():
     # one sample size only
     full, how, _, _ = bench.fit_full_time(8, 2.0, 8, 2.0, 8)
     assert how == "linear" and math.isclose(full, 2.0)
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    """`bench.py --impl reference` launched as two ranks: rank 0 times the oracle
+    and prints the one JSON line; the other rank exits 0 without work."""
+    import json
+    import subprocess
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", "--master-port=29731", os.path.join(root, "bench.py"),
+           "--impl", "reference", "--workload", "small", "--gpus", "2", "--steps", "1", "--warmup", "1",
+           "--oracle-rows", "64"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
