@@ -46,11 +46,15 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     """`bench.py --impl reference` launched as two ranks: rank 0 times the oracle
     and prints the one JSON line; the other rank exits 0 without work."""
     import json
+    import socket
     import subprocess
 
+    with socket.socket() as sk:  # a free port for the rendezvous
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
-           "--master-addr=127.0.0.1", "--master-port=29731", os.path.join(root, "bench.py"),
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.join(root, "bench.py"),
            "--impl", "reference", "--workload", "small", "--gpus", "2", "--steps", "1", "--warmup", "1",
            "--oracle-rows", "64"]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
