@@ -84,8 +84,9 @@ int32_t ra_abi_version(void);
  *   [n * head_dim]; applied by the second pass.
  * RMS_PER_HEAD: the upstream qk-norm (Design 1: each head's slice by its own RMS),
  *   gamma [head_dim] shared by the heads; a head fits in one projection tile, so
- *   this norm and the segment's RoPE are applied in the projection epilogue and
- *   the second pass leaves the segment alone.  Built for head_dim 64 and 128. */
+ *   this norm is applied in the projection epilogue.  Without fused_rope the
+ *   segment is then final; with it, the second pass applies the segment's RoPE
+ *   (and no norm).  Built for head_dim 64 and 128. */
 enum { RA_NORM_NONE = 0, RA_NORM_RMS_ACROSS_HEADS = 1, RA_NORM_RMS_PER_HEAD = 2 };
 /* Output layout, after QKVOutputLayout ("Interface", output_layout). */
 enum { RA_LAYOUT_BSD = 0, RA_LAYOUT_NBSD = 1 };
@@ -185,7 +186,8 @@ ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cach
 /* Synchronises `stream`, reads the workspace status word, clears it, and
  * stores it in *device_status (0 = fine).  Returns RA_ERR_TIMEOUT if a wait of
  * the projection or of the pipelined norm/RoPE pass gave up since the last
- * read, else RA_OK. */
+ * read, else RA_OK.  workspace NULL reads the status word of the static
+ * workspace that qkv_cte_mx_noalloc uses on the current device. */
 ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_status);
 
 /* qkv_cte_mx for callers that cannot allocate device memory.  The pages have
@@ -203,9 +205,11 @@ ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_statu
  *     before any stream capture.
  *   - Every call shares the array: calls that overlap on the GPU (unordered
  *     streams or threads) race and give undefined results.  Calls ordered on
- *     one stream are independent (the status word is cleared by each call).
- *   - A device wait timeout is recorded only in the shared array and is not
- *     reported by this entry point. */
+ *     one stream are independent (each call clears the status word, once its
+ *     arguments have passed every check).
+ *   - A device wait timeout is recorded in the array's status word; read it
+ *     with qkv_cte_mx_status(NULL, stream, &word) after the call and before
+ *     the next one, which clears it. */
 ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
                              const void* w_packed, const float* weight_scales, const uint16_t* bias,
                              const float* cos_cache, const float* sin_cache, const float* q_gamma,
@@ -215,6 +219,15 @@ ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_t* a, const
  * projection kernel, the pipelined norm/RoPE pass and the pipelined KV cache
  * kernel (default 2e9).  Values < 1000 are raised to 1000. */
 void ra_set_wait_timeout_ns(int64_t ns);
+
+/* Test hook for host-side checks without a device.  While `on` is non-zero,
+ * every entry point returns RA_OK as soon as its arguments have passed the
+ * host checks, before any CUDA runtime call: nothing is launched, copied or
+ * looked up, and the status readers report 0.  A rejected call is rejected as
+ * usual.  Tests that hand the library placeholder addresses set it, so that no
+ * such address can reach a kernel whatever the order of the checks.  Global to
+ * the process. */
+void ra_test_validate_only(int32_t on);
 
 /* Test hook for failure detection.  The next projection launch (qkv_cte_mx or
  * qkv_cte_mx_project) issues none of its TMA loads, so the waits of its

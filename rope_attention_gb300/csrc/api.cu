@@ -34,6 +34,11 @@ std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_stall_next{0};  // ra_test_stall_next_projection
 std::atomic<int> g_stall_next_kv{0};  // ra_test_stall_next_kv_cache
 std::atomic<int> g_stall_next_norm{0};  // ra_test_stall_next_norm_rope
+std::atomic<int> g_validate_only{0};    // ra_test_validate_only
+
+// ra_test_validate_only: a call that passed its host checks returns here, before
+// any CUDA runtime call
+bool validate_only() { return g_validate_only.load() != 0; }
 
 ra_status fail(ra_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ra_status fail(ra_status code, const char* fmt, ...) {
@@ -140,35 +145,36 @@ ra_status check_params(const qkv_cte_mx_params* p, QkvShape* s) {
   return RA_OK;
 }
 
-ra_status check_project_args(const qkv_cte_mx_params* p, const QkvShape& s, const uint8_t* a,
-                             const float* a_scale, const void* w_packed, const float* ws,
-                             const uint16_t* bias, const float* qg, const float* kg,
-                             const uint16_t* out, const void* workspace, size_t workspace_bytes) {
-  if (!a || !a_scale || !w_packed || !out || !workspace)
-    return fail(RA_ERR_INVALID_ARG, "a, a_scale, w_packed, out and workspace are required");
-  if (!aligned16(a) || !aligned16(out) || !aligned16(w_packed) || !aligned16(workspace))
-    return fail(RA_ERR_ALIGNMENT, "a, out, w_packed and workspace must be 16-byte aligned");
+ra_status check_project_inputs(const qkv_cte_mx_params* p, const uint8_t* a, const float* a_scale,
+                               const void* w_packed, const float* ws, const uint16_t* bias,
+                               const float* qg, const float* kg, const uint16_t* out) {
+  if (!a || !a_scale || !w_packed || !out)
+    return fail(RA_ERR_INVALID_ARG, "a, a_scale, w_packed and out are required");
+  if (!aligned16(a) || !aligned16(out) || !aligned16(w_packed))
+    return fail(RA_ERR_ALIGNMENT, "a, out and w_packed must be 16-byte aligned");
   if ((ws && !aligned16(ws)) || (bias && !aligned16(bias)))
     return fail(RA_ERR_ALIGNMENT, "weight_scales and bias must be 16-byte aligned");
   if (p->q_norm && !qg) return fail(RA_ERR_INVALID_ARG, "q_norm requires q_gamma");
   if (p->k_norm && !kg) return fail(RA_ERR_INVALID_ARG, "k_norm requires k_gamma");
   if ((qg && !aligned16(qg)) || (kg && !aligned16(kg)))
     return fail(RA_ERR_ALIGNMENT, "gammas must be 16-byte aligned");
-  if (workspace_bytes < s.workspace)
-    return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
   return RA_OK;
 }
 
-ra_status check_norm_args(const qkv_cte_mx_params* p, const float* cos, const float* sin,
-                          const uint16_t* out, const void* workspace, size_t workspace_bytes,
-                          const QkvShape& s) {
-  if (!out || !workspace) return fail(RA_ERR_INVALID_ARG, "out and workspace are required");
-  if (!aligned16(out) || !aligned16(workspace))
-    return fail(RA_ERR_ALIGNMENT, "out and workspace must be 16-byte aligned");
+ra_status check_norm_inputs(const qkv_cte_mx_params* p, const float* cos, const float* sin,
+                            const uint16_t* out) {
+  if (!out) return fail(RA_ERR_INVALID_ARG, "out is required");
+  if (!aligned16(out)) return fail(RA_ERR_ALIGNMENT, "out must be 16-byte aligned");
   if (p->fused_rope && (!cos || !sin))
     return fail(RA_ERR_INVALID_ARG, "fused_rope requires cos_cache and sin_cache");
   if ((cos && !aligned16(cos)) || (sin && !aligned16(sin)))
     return fail(RA_ERR_ALIGNMENT, "cos/sin caches must be 16-byte aligned");
+  return RA_OK;
+}
+
+ra_status check_workspace(const void* workspace, size_t workspace_bytes, const QkvShape& s) {
+  if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace is required");
+  if (!aligned16(workspace)) return fail(RA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
   if (workspace_bytes < s.workspace)
     return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu", workspace_bytes, s.workspace);
   return RA_OK;
@@ -262,13 +268,45 @@ namespace ra {
 void set_last_error(int code, const char* where, const char* what) {
   fail(static_cast<ra_status>(code), "%s: %s", where, what);
 }
+
+ra_status qkv_cte_mx_on_library_workspace(const qkv_cte_mx_params* p, const uint8_t* a,
+                                          const float* a_scale, const void* w_packed,
+                                          const float* weight_scales, const uint16_t* bias,
+                                          const float* cos_cache, const float* sin_cache,
+                                          const float* q_gamma, const float* k_gamma, uint16_t* out,
+                                          size_t capacity, ra_status (*get_workspace)(void**),
+                                          void* stream) {
+  QkvShape s;
+  ra_status st = check_params(p, &s);
+  if (st != RA_OK) return st;
+  if (s.workspace > capacity)
+    return fail(RA_ERR_WORKSPACE,
+                "qkv_cte_mx_noalloc: this call needs %zu bytes of scratch; the static workspace holds %zu",
+                s.workspace, capacity);
+  st = check_project_inputs(p, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out);
+  if (st == RA_OK) st = check_norm_inputs(p, cos_cache, sin_cache, out);
+  if (st != RA_OK) return st;
+  if (validate_only()) return ok();
+  void* ws = nullptr;
+  st = get_workspace(&ws);
+  if (st != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // the only scratch that must start at zero is the status word: the partial sums
+  // and the exponents are written by the projection before the second pass reads them
+  const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), cs);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static workspace status word");
+  st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out, ws, cs);
+  if (st != RA_OK) return st;
+  st = run_norm_rope(p, s, cos_cache, sin_cache, out, ws, cs);
+  return st == RA_OK ? ok() : st;
+}
 }  // namespace ra
 
 extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
 
-int32_t ra_abi_version(void) { return 8; }
+int32_t ra_abi_version(void) { return 9; }
 
 void ra_set_wait_timeout_ns(int64_t ns) { g_wait_ns.store(ns < 1000 ? 1000 : ns); }
 
@@ -277,6 +315,8 @@ void ra_test_stall_next_projection(void) { g_stall_next.store(1); }
 void ra_test_stall_next_kv_cache(void) { g_stall_next_kv.store(1); }
 
 void ra_test_stall_next_norm_rope(void) { g_stall_next_norm.store(1); }
+
+void ra_test_validate_only(int32_t on) { g_validate_only.store(on != 0 ? 1 : 0); }
 
 ra_status qkv_cte_mx_packed_weight_bytes(int64_t H, int64_t I, size_t* bytes) {
   if (!bytes) return fail(RA_ERR_INVALID_ARG, "bytes is NULL");
@@ -295,6 +335,7 @@ ra_status qkv_cte_mx_pack_weight(const uint8_t* w, const uint8_t* w_block_exp, i
   if (!aligned16(packed)) return fail(RA_ERR_ALIGNMENT, "packed must be 16-byte aligned");
   if (packed_bytes < need) return fail(RA_ERR_WORKSPACE, "packed buffer too small: %zu < %zu", packed_bytes, need);
   if (H > 0x7fffffffLL || I > 0x7fffffffLL) return fail(RA_ERR_INVALID_ARG, "H or I too large");
+  if (validate_only()) return ok();
   cudaError_t e = ra::launch_pack_weight(w, w_block_exp, H, I, static_cast<uint8_t*>(packed),
                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "pack_weight launch");
@@ -316,10 +357,10 @@ ra_status qkv_cte_mx_project(const qkv_cte_mx_params* p, const uint8_t* a, const
                              size_t workspace_bytes, void* stream) {
   QkvShape s;
   ra_status st = check_params(p, &s);
+  if (st == RA_OK) st = check_project_inputs(p, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out);
+  if (st == RA_OK) st = check_workspace(workspace, workspace_bytes, s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
-                          workspace, workspace_bytes);
-  if (st != RA_OK) return st;
+  if (validate_only()) return ok();
   st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma,
                    k_gamma, out, workspace, static_cast<cudaStream_t>(stream));
   return st == RA_OK ? ok() : st;
@@ -330,9 +371,10 @@ ra_status qkv_cte_mx_norm_rope(const qkv_cte_mx_params* p, const float* cos_cach
                                size_t workspace_bytes, void* stream) {
   QkvShape s;
   ra_status st = check_params(p, &s);
+  if (st == RA_OK) st = check_norm_inputs(p, cos_cache, sin_cache, out);
+  if (st == RA_OK) st = check_workspace(workspace, workspace_bytes, s);
   if (st != RA_OK) return st;
-  st = check_norm_args(p, cos_cache, sin_cache, out, workspace, workspace_bytes, s);
-  if (st != RA_OK) return st;
+  if (validate_only()) return ok();
   st = run_norm_rope(p, s, cos_cache, sin_cache, out, workspace, static_cast<cudaStream_t>(stream));
   return st == RA_OK ? ok() : st;
 }
@@ -344,12 +386,11 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
                      void* stream) {
   QkvShape s;
   ra_status st = check_params(p, &s);
+  if (st == RA_OK) st = check_project_inputs(p, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out);
+  if (st == RA_OK) st = check_norm_inputs(p, cos_cache, sin_cache, out);
+  if (st == RA_OK) st = check_workspace(workspace, workspace_bytes, s);
   if (st != RA_OK) return st;
-  st = check_project_args(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma, k_gamma, out,
-                          workspace, workspace_bytes);
-  if (st != RA_OK) return st;
-  st = check_norm_args(p, cos_cache, sin_cache, out, workspace, workspace_bytes, s);
-  if (st != RA_OK) return st;
+  if (validate_only()) return ok();
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   st = run_project(p, s, a, a_scale, w_packed, weight_scales, bias, q_gamma,
                    k_gamma, out, workspace, cs);
@@ -359,7 +400,15 @@ ra_status qkv_cte_mx(const qkv_cte_mx_params* p, const uint8_t* a, const float* 
 }
 
 ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_status) {
-  if (!workspace || !device_status) return fail(RA_ERR_INVALID_ARG, "workspace and device_status are required");
+  if (!device_status) return fail(RA_ERR_INVALID_ARG, "device_status is required");
+  if (validate_only()) {
+    *device_status = 0;
+    return ok();
+  }
+  if (!workspace) {  // the static workspace of qkv_cte_mx_noalloc on the current device
+    const ra_status st = ra::noalloc_workspace(&workspace);
+    if (st != RA_OK) return st;
+  }
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   int32_t v = 0;
   cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, cs);
@@ -382,6 +431,7 @@ static ra_status row_quantize_common(const uint16_t* x, int64_t T, int64_t H, ui
       (scale && (reinterpret_cast<uintptr_t>(scale) & 3u) != 0))
     return fail(RA_ERR_ALIGNMENT, packed ? "packed must be 4-byte aligned"
                                          : "codes must be 8-byte and scale 4-byte aligned");
+  if (validate_only()) return ok();
   cudaError_t e = ra::launch_row_quantize(x, T, H, codes, scale, packed, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "row_quantize launch");
   return ok();
@@ -485,6 +535,7 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
   if (p->B * p->N * p->S > (1LL << 40)) return fail(RA_ERR_INVALID_ARG, "too many rows");
   if (mode == RA_CACHE_NORM && p->cache_seq_len > (1LL << 31)) return fail(RA_ERR_INVALID_ARG, "cache_seq_len too large");
   if (p->S > (1LL << 31)) return fail(RA_ERR_INVALID_ARG, "S too large");
+  if (validate_only()) return ok();
 
   ra::KvLaunch L{};
   L.kv = kv;
@@ -531,6 +582,10 @@ ra_status kv_rms_norm_rope_cache(const kv_rms_norm_rope_cache_params* p, const u
 
 ra_status kv_rms_norm_rope_cache_status(void* stream, int32_t* device_status) {
   if (!device_status) return fail(RA_ERR_INVALID_ARG, "device_status is required");
+  if (validate_only()) {
+    *device_status = 0;
+    return ok();
+  }
   int32_t* word = ra::kv_status_word();
   if (!word) return fail(RA_ERR_CUDA, "the KV status word cannot be found on this device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

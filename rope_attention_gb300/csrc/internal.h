@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "rope_attention.h"
+
 namespace ra {
 
 // ------------------------------------------------------------ projection (K1)
@@ -83,5 +85,21 @@ int device_sm_count();
 
 // Sets the thread-local message returned by ra_last_error() ("where: what").
 void set_last_error(int code, const char* where, const char* what);
+
+// ------------------------------------------------------------ qkv_cte_mx_noalloc
+// The whole qkv_cte_mx call on a workspace the library owns: every host check of
+// qkv_cte_mx (and the problem's scratch against `capacity`) first; then
+// `get_workspace` supplies the workspace's device address, its status word is
+// cleared on `stream` and both passes launch.  Nothing is enqueued for a rejected call.
+ra_status qkv_cte_mx_on_library_workspace(const qkv_cte_mx_params* p, const uint8_t* a,
+                                          const float* a_scale, const void* w_packed,
+                                          const float* weight_scales, const uint16_t* bias,
+                                          const float* cos_cache, const float* sin_cache,
+                                          const float* q_gamma, const float* k_gamma, uint16_t* out,
+                                          size_t capacity, ra_status (*get_workspace)(void**),
+                                          void* stream);
+// Device address of qkv_cte_mx_noalloc's static workspace on the current device
+// (looked up once per device).
+ra_status noalloc_workspace(void** ws);
 
 }  // namespace ra

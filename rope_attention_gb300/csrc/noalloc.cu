@@ -13,11 +13,12 @@
 // The array is part of the library image: every GPU that loads the library
 // holds kNoAllocWorkspaceBytes of device memory for it until the process
 // exits.  All calls share it and it keeps the last call's contents; the status
-// word is cleared on every call (the partials and the exponents are fully
-// rewritten before they are read), so calls issued one after another are
-// independent, but calls that overlap on the GPU (different streams or
-// threads without ordering between them) race on the array.
-#include <cstdio>
+// word is cleared on every call, once every argument check has passed (the
+// partials and the exponents are fully rewritten before they are read), so
+// calls issued one after another are independent, but calls that overlap on the
+// GPU (different streams or threads without ordering between them) race on the
+// array.  A pipeline wait that runs out of time leaves its mark in the array's
+// status word, which qkv_cte_mx_status reads when given a NULL workspace.
 #include <mutex>
 
 #include "rope_attention.h"
@@ -33,18 +34,22 @@ static __device__ __align__(256) uint8_t g_noalloc_workspace[kNoAllocWorkspaceBy
 std::mutex g_mu;
 void* g_dev_ptr[kMaxDevices] = {};
 
+}  // namespace
+
+namespace ra {
+
 // Device address of the array on the current device.  Host code may not use
 // the symbol itself as a device pointer, so the address is looked up once per
 // device (with that device current) and cached.
-ra_status workspace_on_current_device(void** out) {
+ra_status noalloc_workspace(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
-    ra::set_last_error(RA_ERR_CUDA, "cudaGetDevice", cudaGetErrorString(e));
+    set_last_error(RA_ERR_CUDA, "cudaGetDevice", cudaGetErrorString(e));
     return RA_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) {
-    ra::set_last_error(RA_ERR_INVALID_ARG, "qkv_cte_mx_noalloc", "device index out of range");
+    set_last_error(RA_ERR_INVALID_ARG, "qkv_cte_mx_noalloc", "device index out of range");
     return RA_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lock(g_mu);
@@ -52,8 +57,8 @@ ra_status workspace_on_current_device(void** out) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
     if (e != cudaSuccess || p == nullptr) {
-      ra::set_last_error(RA_ERR_CUDA, "cudaGetSymbolAddress(static workspace)",
-                         e != cudaSuccess ? cudaGetErrorString(e) : "null address");
+      set_last_error(RA_ERR_CUDA, "cudaGetSymbolAddress(static workspace)",
+                     e != cudaSuccess ? cudaGetErrorString(e) : "null address");
       return RA_ERR_CUDA;
     }
     g_dev_ptr[dev] = p;
@@ -62,7 +67,7 @@ ra_status workspace_on_current_device(void** out) {
   return RA_OK;
 }
 
-}  // namespace
+}  // namespace ra
 
 extern "C" ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_t* a,
                                         const float* a_scale, const void* w_packed,
@@ -70,25 +75,7 @@ extern "C" ra_status qkv_cte_mx_noalloc(const qkv_cte_mx_params* p, const uint8_
                                         const float* cos_cache, const float* sin_cache,
                                         const float* q_gamma, const float* k_gamma, uint16_t* out,
                                         void* stream) {
-  size_t need = 0;
-  ra_status st = qkv_cte_mx_workspace_bytes(p, &need);
-  if (st != RA_OK) return st;
-  if (need > kNoAllocWorkspaceBytes) {
-    char msg[160];
-    snprintf(msg, sizeof(msg), "this call needs %zu bytes of scratch; the static workspace holds %zu",
-             need, kNoAllocWorkspaceBytes);
-    ra::set_last_error(RA_ERR_WORKSPACE, "qkv_cte_mx_noalloc", msg);
-    return RA_ERR_WORKSPACE;
-  }
-  void* ws = nullptr;
-  st = workspace_on_current_device(&ws);
-  if (st != RA_OK) return st;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), cs);  // status word starts at zero
-  if (e != cudaSuccess) {
-    ra::set_last_error(RA_ERR_CUDA, "clearing the static workspace status", cudaGetErrorString(e));
-    return RA_ERR_CUDA;
-  }
-  return qkv_cte_mx(p, a, a_scale, w_packed, weight_scales, bias, cos_cache, sin_cache, q_gamma,
-                    k_gamma, out, ws, kNoAllocWorkspaceBytes, stream);
+  return ra::qkv_cte_mx_on_library_workspace(p, a, a_scale, w_packed, weight_scales, bias, cos_cache,
+                                             sin_cache, q_gamma, k_gamma, out, kNoAllocWorkspaceBytes,
+                                             ra::noalloc_workspace, stream);
 }

@@ -33,7 +33,7 @@ EXPORTS = ["ra_last_error", "ra_abi_version", "ra_set_wait_timeout_ns", "ra_test
            "qkv_cte_mx", "qkv_cte_mx_project", "qkv_cte_mx_norm_rope", "qkv_cte_mx_status",
            "qkv_cte_mx_noalloc", "kv_rms_norm_rope_cache", "kv_rms_norm_rope_cache_status",
            "ra_test_stall_next_kv_cache", "ra_test_stall_next_norm_rope", "row_quantize_e4m3",
-           "row_quantize_e4m3_packed"]
+           "row_quantize_e4m3_packed", "ra_test_validate_only"]
 
 
 class RAError(RuntimeError):
@@ -96,6 +96,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "ra_test_stall_next_norm_rope": (None, []),
         "row_quantize_e4m3": (i32, [P, i64, i64, P, P, P]),
         "row_quantize_e4m3_packed": (i32, [P, i64, i64, P, P]),
+        "ra_test_validate_only": (None, [i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -217,6 +218,11 @@ def ra_set_wait_timeout_ns(ns: int) -> None:
     load().ra_set_wait_timeout_ns(int(ns))
 
 
+def ra_test_validate_only(on: bool) -> None:
+    """Test hook: while on, every call returns right after its host checks (no CUDA call)."""
+    load().ra_test_validate_only(1 if on else 0)
+
+
 def ra_test_stall_next_projection() -> None:
     """Test hook: the next projection launch issues no loads, so its waits time out."""
     load().ra_test_stall_next_projection()
@@ -317,8 +323,9 @@ def qkv_cte_mx_noalloc(params, a, a_scale, w_packed, weight_scales, bias, cos_ca
         _ptr(k_gamma, torch.float32, "k_gamma"), _ptr(_bits16(out), None, "out"), _stream(stream)))
 
 
-def qkv_cte_mx_status(workspace: torch.Tensor, stream=None) -> int:
-    """Synchronises the stream; returns the device status word (0 = fine) and clears it."""
+def qkv_cte_mx_status(workspace: torch.Tensor | None, stream=None) -> int:
+    """Synchronises the stream; returns the device status word (0 = fine) and clears it.
+    workspace None: the static workspace of qkv_cte_mx_noalloc on the current device."""
     v = ctypes.c_int32()
     st = load().qkv_cte_mx_status(_ptr(workspace, torch.uint8, "workspace"), _stream(stream), ctypes.byref(v))
     if st not in (RA_OK, -6):

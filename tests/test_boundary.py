@@ -2,9 +2,12 @@
 
 * the library loads and exports every function include/rope_attention.h declares;
 * every rejection rule of the header returns its status code and a message.
-Each rejected call has exactly one violation and fails host-side validation,
-so the placeholder device addresses used here are never dereferenced or
-launched on.
+Each rejected call has exactly one violation and fails host-side validation.
+Every test here runs with the library's validate-only hook set
+(ra_test_validate_only), under which a call that passes its checks returns
+before any CUDA runtime call: the placeholder device addresses used here can
+never reach a kernel, on this machine or on one with a GPU, whatever the order
+of the library's checks.
 """
 import ctypes
 import os
@@ -29,7 +32,10 @@ def declared_functions():
 def L():
     from rope_attention_gb300 import build
     build.build()
-    return native.load()
+    lib = native.load()
+    lib.ra_test_validate_only(1)
+    yield lib
+    lib.ra_test_validate_only(0)
 
 
 def test_exports_every_declared_function(L):
@@ -38,7 +44,7 @@ def test_exports_every_declared_function(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in the header but not exported"
     assert sorted(names) == sorted(native.EXPORTS)
-    assert native.ra_abi_version() == 8
+    assert native.ra_abi_version() == 9
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -134,8 +140,7 @@ def test_project_and_norm_rejections(L):
     assert st == -1 and b"k_gamma" in L.ra_last_error()     # the per-head K norm needs its gamma
     st = L.qkv_cte_mx_norm_rope(ctypes.byref(p), None, A16, A16, A16, ws_bytes(L, p), None)
     assert st == -1                                          # fused_rope needs cos/sin
-    v = ctypes.c_int32()
-    assert L.qkv_cte_mx_status(None, None, ctypes.byref(v)) == -1
+    assert L.qkv_cte_mx_status(None, None, None) == -1           # device_status is required
     assert L.kv_rms_norm_rope_cache_status(None, None) == -1    # device_status is required
 
 
@@ -231,3 +236,53 @@ def test_row_quantize_rejections(L, what, args, status, msg):
 ])
 def test_row_quantize_packed_rejections(L, what, args, status):
     assert L.row_quantize_e4m3_packed(*args, None) == status, what
+
+
+# ---------------------------------------------------------------- the validate-only hook
+def valid_calls(L):
+    """One call per launching entry point, each passing every host check."""
+    p = qp()
+    n = ws_bytes(L, p)
+    k = kp(variant=2, N=2, Dkv=192, Dv=128, k_cache_dtype=2, ckv_cache_dtype=2)
+    return {
+        "qkv_cte_mx": lambda: qkv_call(L, p),
+        "qkv_cte_mx_project": lambda: L.qkv_cte_mx_project(ctypes.byref(p), A16, A16, A16, None, None, A16, A16,
+                                                           A16, A16, n, None),
+        "qkv_cte_mx_norm_rope": lambda: L.qkv_cte_mx_norm_rope(ctypes.byref(p), A16, A16, A16, A16, n, None),
+        "qkv_cte_mx_noalloc": lambda: L.qkv_cte_mx_noalloc(ctypes.byref(p), A16, A16, A16, None, A16, A16, A16,
+                                                           A16, A16, A16, None),
+        "qkv_cte_mx_pack_weight": lambda: L.qkv_cte_mx_pack_weight(A16, A16, 256, 384, A16, 1 << 30, None),
+        "kv_rms_norm_rope_cache": lambda: kv_call(L, k, v=A16, ks=A16, vs=A16),
+        "row_quantize_e4m3": lambda: L.row_quantize_e4m3(A16, 4, 64, A16, A16, None),
+        "row_quantize_e4m3_packed": lambda: L.row_quantize_e4m3_packed(A16, 4, 64, A16, None),
+    }
+
+
+def test_validate_only_returns_before_any_cuda_call(L):
+    """With the hook set (as for every test in this file), a call that passes its host
+    checks returns RA_OK without touching CUDA, and the status readers report 0."""
+    for name, call in valid_calls(L).items():
+        assert call() == 0, (name, L.ra_last_error())
+    v = ctypes.c_int32(7)
+    assert L.qkv_cte_mx_status(A16, None, ctypes.byref(v)) == 0 and v.value == 0
+    v = ctypes.c_int32(7)
+    assert L.qkv_cte_mx_status(None, None, ctypes.byref(v)) == 0 and v.value == 0
+    v = ctypes.c_int32(7)
+    assert L.kv_rms_norm_rope_cache_status(None, ctypes.byref(v)) == 0 and v.value == 0
+
+
+def test_validate_only_is_what_stops_the_launch(L):
+    """Without the hook the same valid calls go on to the CUDA runtime, which on a
+    machine without a GPU fails (RA_ERR_CUDA): so it is the hook, not a check,
+    that keeps the placeholder addresses away from the device.  Runs only where no
+    GPU is visible, since these calls would otherwise launch on those addresses."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on placeholder addresses with a GPU present")
+    calls = valid_calls(L)
+    L.ra_test_validate_only(0)
+    try:
+        for name, call in calls.items():
+            assert call() == -5, (name, L.ra_last_error())  # RA_ERR_CUDA: no device here
+    finally:
+        L.ra_test_validate_only(1)

@@ -176,3 +176,51 @@ def test_repeat_call_is_idempotent():
     r.run()
     torch.cuda.synchronize()
     assert torch.equal(first[0], r.k_cache) and torch.equal(first[1], r.ckv_cache)
+
+
+# The configuration the bench times for the KV half of the 720p step: V2 separate
+# k/v, PA_BNSD, int8 per-head quantisation, is_output_kv off (the CANN parameter
+# table's default), so the kernel takes its no-outputs branch.
+OUTPUTS_OFF = [
+    ("v2_int8_off", dict(variant=2, B=2, N=8, S=29, Dkv=192, Dv=128, block_size=32, block_num=4,
+                         quant_k=True, quant_v=True)),
+    # rows per warp step crossing head and batch boundaries; fewer rows than a tile
+    ("v2_int8_off_s3", dict(variant=2, B=3, N=8, S=3, Dkv=192, Dv=128, block_size=32, block_num=1,
+                            quant_k=True, quant_v=True)),
+    # a ragged tail of rows after several full 16-row tiles of the pipelined kernel
+    ("v2_int8_off_ragged", dict(variant=2, B=2, N=4, S=203, Dkv=192, Dv=128, block_size=128,
+                                block_num=4, quant_k=True, quant_v=True)),
+    ("v2_int8_off_sym_n1", dict(variant=2, B=3, N=1, S=77, Dkv=192, Dv=128, block_size=64,
+                                block_num=4, quant_k=True, quant_v=True, offsets=False)),
+]
+
+
+@pytest.mark.parametrize("name,kw", OUTPUTS_OFF, ids=[s[0] for s in OUTPUTS_OFF])
+@pytest.mark.parametrize("skip", [0.0, 0.25])
+def test_v2_outputs_off(name, kw, skip):
+    case = synth.make_kv(name, 600 + len(name), skip_frac=skip, is_output_kv=False, **kw)
+    run = runner.KvRun(case)
+    assert not run.outputs
+    # k_rope / c_kv buffers handed over although is_output_kv is off: the call must
+    # leave them alone (the page writes them only when is_output_kv is set)
+    fdt = torch.bfloat16
+    sentinel = torch.tensor(synth.K_SENTINEL_BF16, dtype=torch.int16)
+    run.k_rope = torch.full((case.B, case.N, case.S, case.k_width), 0, dtype=fdt, device="cuda")
+    run.c_kv = torch.full((case.B, case.N, case.S, case.ckv_width), 0, dtype=fdt, device="cuda")
+    run.k_rope.view(torch.int16).fill_(sentinel.item())
+    run.c_kv.view(torch.int16).fill_(sentinel.item())
+    run.run()
+    torch.cuda.synchronize()
+    for t in (run.k_rope, run.c_kv):
+        assert bool((t.view(torch.int16) == sentinel.item()).all()), f"{name}: an output was written"
+    run.k_rope = run.c_kv = None  # check_kv compares the outputs only when they are on
+    check_kv(case, run, name)
+
+
+def test_full_sep_v2_outputs_off():
+    """The benched call itself: kv [8,8,4096,192], v [8,8,4096,128], int8 per-head
+    quantisation, PA_BNSD bs=128, 256 blocks, is_output_kv off; every cache slot
+    compared (written slots against the oracle, the rest bit for bit)."""
+    case = synth.kv_sep_v2(is_output_kv=False)
+    stats = check_kv(case, run_case(case), "sep_v2_outputs_off")
+    print("tie differences:", stats)
