@@ -79,6 +79,14 @@ def workload(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
+def bench_config(qcase, kcase, ws: int) -> dict:
+    """The ``config`` of the JSON line, the same for both arms."""
+    return {"workload": f"{qcase.name} (S={qcase.S}, H={qcase.H}, I={qcase.I}) + {kcase.name} "
+                        f"(kv [{kcase.B},{kcase.N},{kcase.S},{kcase.Dkv}])",
+            "global_batch": ws * qcase.T, "seq_len": qcase.S, "parallelism": f"replica x{ws}",
+            "l2": "inputs larger than L2 (each step streams > 3 GB)"}
+
+
 def qkv_bytes_k2(c) -> int:
     """Algorithmic bytes of the norm/RoPE pass: Q|K read + write, cos/sin, gammas, sums."""
     qk = c.T * (c.num_heads + c.num_kv_heads) * c.head_dim * 2
@@ -155,6 +163,29 @@ def host_cpu_model() -> str:
     except (OSError, subprocess.SubprocessError):
         pass
     return platform.machine()
+
+
+def host_topology(gpu_index: int) -> dict:
+    """Where the host side of the link sits: the GPU's PCI address and NUMA node,
+    the CPUs local to it, and the CPUs this process may run on (the end-to-end
+    copies go through pinned host memory, placed by the allocating thread)."""
+    info = {"process_cpus": len(os.sched_getaffinity(0))}
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={gpu_index}", "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True, timeout=20).stdout.strip()
+        bus = out.lower()
+        if bus.count(":") == 2 and len(bus.split(":")[0]) == 8:  # 00000000:XX:YY.Z -> 0000:XX:YY.Z
+            bus = bus[4:]
+        info["gpu_pci"] = bus
+        base = f"/sys/bus/pci/devices/{bus}"
+        for name, key in (("numa_node", "gpu_numa_node"), ("local_cpulist", "gpu_local_cpus")):
+            path = os.path.join(base, name)
+            if os.path.exists(path):
+                with open(path) as f:
+                    info[key] = f.read().strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return info
 
 
 def dist_env():
@@ -251,10 +282,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3-mx/bf16/int8", "data": "synthetic",
-        "config": {"workload": f"{qcase.name} (S={qcase.S}, H={qcase.H}, I={qcase.I}) + {kcase.name} "
-                               f"(kv [{kcase.B},{kcase.N},{kcase.S},{kcase.Dkv}])",
-                   "global_batch": ws * qcase.T, "seq_len": qcase.S, "parallelism": f"replica x{ws}",
-                   "l2": "inputs larger than L2 (each step streams > 3 GB)"},
+        "config": bench_config(qcase, kcase, ws),
         "roofline": {"bound": "tensor", "achieved": round(k1_tf, 1), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(k1_tf / fp8_peak, 4),
                      "traffic": K1_DRAM_BYTES.get((args.workload, k1_source_digest())),
@@ -271,7 +299,8 @@ def run_ours(args):
         "clocks": clk.summary(),
         "device": {"gpu": torch.cuda.get_device_name(local),
                    "sms": torch.cuda.get_device_properties(local).multi_processor_count,
-                   "host_cpu": host_cpu_model(), "host_cores": os.cpu_count()},
+                   "host_cpu": host_cpu_model(), "host_cores": os.cpu_count(),
+                   "host_topology": host_topology(local)},
         "gpu_launches": 3 * K,
         "next": nxt,
     }
@@ -474,10 +503,48 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / K
     ms = dist.max_over_ranks(ms, device="cuda")
+    link = measure_link(h_in, dev_in(q, k), h_out[0], (q.out, k.k_cache, k.ckv_cache), s_h2d, s_d2h, bi, bo)
     del q2, k2
     return {"value": round(dist.job_rate(qcase.flops, ws, ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "overlap": "uploads, kernels and downloads of consecutive steps on three streams"}
+            "overlap": "uploads, kernels and downloads of consecutive steps on three streams",
+            "link": link, "e2e_frac_of_link": round(link["link_bound_ms"] / ms, 4)}
+
+
+def measure_link(h_in, d_in, h_out, d_out, s_h2d, s_d2h, bi: int, bo: int, reps: int = 3) -> dict:
+    """The host link on this machine, with the e2e leg's own pinned buffers and copies:
+    the step's uploads alone, its downloads alone, and both at once on their two
+    streams (best of ``reps`` each, CUDA events).  A step that moves these bytes
+    cannot take less than the slowest of the three: that is ``link_bound_ms``."""
+    import torch
+
+    def timed(up: bool, down: bool) -> float:
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(s_h2d)
+            s_d2h.wait_event(t0)
+            if up:
+                with torch.cuda.stream(s_h2d):
+                    for h, d in zip(h_in, d_in):
+                        d.copy_(h, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s_d2h):
+                    for h, d in zip(h_out, d_out):
+                        h.copy_(d, non_blocking=True)
+            s_h2d.wait_stream(s_d2h)
+            t1.record(s_h2d)
+            torch.cuda.synchronize()
+            best = min(best, t0.elapsed_time(t1))
+        return best
+
+    up_ms, down_ms, both_ms = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_ms": round(up_ms, 3), "h2d_gbs": round(bi / up_ms / 1e6, 1),
+            "d2h_ms": round(down_ms, 3), "d2h_gbs": round(bo / down_ms / 1e6, 1),
+            "both_ms": round(both_ms, 3), "link_bound_ms": round(max(up_ms, down_ms, both_ms), 3),
+            "note": "the step's uploads alone, its downloads alone and both at once, pinned host memory, "
+                    "best of %d; e2e_frac_of_link = link_bound_ms / e2e ms_per_step" % reps}
 
 
 def oracle_sample_time(qcase, kcase, q_rows: int, kv_batches: int):
@@ -549,27 +616,35 @@ def cpu_baseline(qcase, kcase, args):
 
 
 def run_reference(args):
+    """The oracle, as it stands, on the machine's host cores.  Each timed step is one
+    bounded sample of the workload (two sample sizes of the projection and of the
+    KV call); ``ms_per_step`` is the wall time such a step took, and ``value`` the
+    whole workload's throughput extrapolated from it (fixed + per-unit cost),
+    with the extrapolated time of one full step in ``extrapolated_step_s``."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     qcase, kcase = workload(args.workload)
     for _ in range(args.warmup):
         oracle_sample_time(qcase, kcase, 64, 1)
-    times = []
+    walls, fulls = [], []
     sample = None
     for _ in range(args.steps):
+        t0 = time.perf_counter()
         full_s, sample = oracle_full_estimate(qcase, kcase, args, warm=False)
-        times.append(full_s)
-    full_s = statistics.mean(times)
+        walls.append(time.perf_counter() - t0)
+        fulls.append(full_s)
+    full_s = statistics.mean(fulls)
     value = qcase.flops / full_s / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 1),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(walls), 1),
+        "extrapolated_step_s": round(full_s, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{qcase.name} (S={qcase.S}, H={qcase.H}, I={qcase.I}) + {kcase.name}",
-                   "global_batch": qcase.T, "seq_len": qcase.S, "parallelism": "cpu"},
+        "config": bench_config(qcase, kcase, ws),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"per step: {sample}"},
+                         "sample": f"per timed step: {sample}; value = the whole step's work over that "
+                                   f"extrapolated time ({full_s:.1f} s)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -256,11 +256,13 @@ void ra_test_stall_next_norm_rope(void);
  * input is a row-packed activation -- H FP8 (E4M3) codes followed by a 4-byte
  * fp32 dequantisation scale per row -- made by a row quantiser from the bf16
  * hidden state.  The page gives no formula; this library computes, per row t,
+ * with the code defined by the layout's dequantisation identity x ~ code * scale,
  *   m = max(max_h |x[t,h]|, 2^-100),  scale[t] = m / 448,
- *   code[t,h] = E4M3(x[t,h] * (448 / m)),
- * every step in fp32 rounded to nearest-even, the E4M3 rounding half-to-even and
- * saturated to +-448 (the sign of zero is kept); the floor keeps 448 / m finite
- * for rows of zeros or of bf16 subnormals.  Inputs must be finite.
+ *   code[t,h] = E4M3(x[t,h] / scale[t]),
+ * every step in fp32 rounded to nearest-even (the divisions correctly rounded),
+ * the E4M3 rounding half-to-even and saturated to +-448 (the sign of zero is
+ * kept); the floor keeps the scale a normal fp32 number for rows of zeros or of
+ * bf16 subnormals.  Inputs must be finite.
  *
  * row_quantize_e4m3: the split form qkv_cte_mx reads (`a` and `a_scale`).
  *   x      [T, H] bf16 bit patterns, device, 16-byte aligned

@@ -5,20 +5,22 @@ input is a row-packed activation [B, S, H + 4] -- H FP8 (E4M3) codes followed by
 a 4-byte fp32 dequantisation scale per row -- made from the bf16 hidden state by
 a row quantiser (row_quantize_packed); the projection kernel itself does not
 quantise.  The page names the operation and its output layout but gives no
-formula.  The reading used here is symmetric absmax scaling onto the E4M3 range:
+formula.  The reading used here is symmetric absmax scaling onto the E4M3 range,
+with the code defined by the layout's own dequantisation identity: the row
+stores one fp32 scale, and x is recovered as code * scale, so the code is x
+divided by that stored scale, rounded to E4M3:
 
     m[t]      = max(max_h |x[t, h]|, 2^-100)      (exact: x is bf16; the floor keeps
-                                                  448 / m finite for rows of zeros or of
-                                                  bf16 subnormals)
-    scale[t]  = m[t] / 448                        fp32, rounded to nearest -- the dequant scale
-    inv[t]    = 448 / m[t]                        fp32, rounded to nearest
-    code[t,h] = E4M3(x[t, h] * inv[t])            the fp32 product rounded to nearest, then
-                                                  rounded to E4M3 half-to-even, saturated
-                                                  to +-448, the sign of zero kept
+                                                  the scale a normal fp32 number for rows
+                                                  of zeros or of bf16 subnormals)
+    scale[t]  = m[t] / 448                        fp32, rounded to nearest -- the stored scale
+    code[t,h] = E4M3(x[t, h] / scale[t])          the fp32 quotient (IEEE division, rounded to
+                                                  nearest), then rounded to E4M3 half-to-even,
+                                                  saturated to +-448, the sign of zero kept
 
 The codes are integers that floating point decides, so every step is taken in
-fp32, the precision the definition above fixes (numpy float32 arithmetic is
-IEEE binary32 with round-to-nearest-even).
+fp32, the type of the stored scale (numpy float32 arithmetic is IEEE binary32
+with round-to-nearest-even, division included).
 """
 from __future__ import annotations
 
@@ -54,9 +56,8 @@ def row_quantize(x_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     x = decode_bf16(np.asarray(x_bits, dtype=np.uint16)).astype(np.float32)
     m = np.maximum(np.max(np.abs(x), axis=1), np.float32(AMAX_FLOOR)).astype(np.float32)
     scale = (m / np.float32(E4M3_MAX)).astype(np.float32)
-    inv = (np.float32(E4M3_MAX) / m).astype(np.float32)
-    prod = (x * inv[:, None]).astype(np.float32)
-    return encode_e4m3_rne_sat(prod), scale
+    quot = (x / scale[:, None]).astype(np.float32)
+    return encode_e4m3_rne_sat(quot), scale
 
 
 def row_quantize_packed(x_bits: np.ndarray) -> np.ndarray:

@@ -5,19 +5,21 @@
 // AWS Neuron "Kernel reference: qkv_cte", section "Interface": the projection's
 // input is the row-packed activation, H FP8 codes followed by a 4-byte fp32
 // dequantisation scale per row, made by a row quantiser from the bf16 hidden
-// state.  The page gives no formula; the plain absmax reading is used:
-//   m = max(max_h |x|, 2^-100),  scale = m / 448,  code = E4M3(x * (448 / m)),
-// every step in fp32 with round-to-nearest-even, the E4M3 rounding half-to-even
-// with saturation to +-448 (the floor keeps 448 / m finite for rows of zeros or
-// of bf16 subnormals).
+// state.  The page gives no formula; the plain absmax reading is used, with the
+// code defined by the layout's dequantisation identity x ~ code * scale:
+//   m = max(max_h |x|, 2^-100),  scale = m / 448,  code = E4M3(x / scale),
+// every step in fp32 with round-to-nearest-even (the division correctly
+// rounded), the E4M3 rounding half-to-even with saturation to +-448 (the floor
+// keeps the scale a normal fp32 number for rows of zeros or of bf16 subnormals).
 //
 // GB300 mapping: an HBM stream (2 bytes in, 1 byte out per element).  One warp
 // per row, persistent over rows: the row is loaded once into registers with
 // 16-byte loads, its amax is taken on the bf16 bit patterns (|x| as an unsigned
 // 15-bit integer orders like the value) with per-halfword max and one
-// warp-wide integer max-reduction, then each lane converts its chunks with
-// packed fp32x2 multiplies and the hardware E4M3x2 conversion and writes 8
-// bytes per chunk, coalesced across the warp.  Rows longer than the register
+// warp-wide integer max-reduction, then each lane divides its chunks by the
+// row's scale (IEEE division, round to nearest) and converts them with the
+// hardware E4M3x2 conversion, and writes 8 bytes per chunk, coalesced across
+// the warp.  Rows longer than the register
 // budget (H > 8192) take a two-pass path that re-reads the row (from L2).
 #include <cuda_fp8.h>
 
@@ -51,21 +53,22 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
+// x / scale for a bf16 pair, each quotient correctly rounded
+__device__ __forceinline__ float2 div2(uint32_t bf16x2, float scale) {
+  const float2 f = bf16x2_to_float2(bf16x2);
+  return make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+}
+
 // 8 codes (two 32-bit words, first element in the lowest byte) for one chunk
-__device__ __forceinline__ uint2 quant8(uint4 v, float inv) {
-  const float2 s = make_float2(inv, inv);
-  const float2 f0 = __fmul2_rn(bf16x2_to_float2(v.x), s);
-  const float2 f1 = __fmul2_rn(bf16x2_to_float2(v.y), s);
-  const float2 f2 = __fmul2_rn(bf16x2_to_float2(v.z), s);
-  const float2 f3 = __fmul2_rn(bf16x2_to_float2(v.w), s);
+__device__ __forceinline__ uint2 quant8(uint4 v, float scale) {
+  const float2 f0 = div2(v.x, scale), f1 = div2(v.y, scale);
+  const float2 f2 = div2(v.z, scale), f3 = div2(v.w, scale);
   return make_uint2(e4m3x2(f0.x, f0.y) | (e4m3x2(f1.x, f1.y) << 16),
                     e4m3x2(f2.x, f2.y) | (e4m3x2(f3.x, f3.y) << 16));
 }
 
-__device__ __forceinline__ void row_scales(float amax, float& scale, float& inv) {
-  const float m = fmaxf(amax, kAmaxFloor);
-  scale = m / kE4m3Max;  // IEEE division, round to nearest
-  inv = kE4m3Max / m;
+__device__ __forceinline__ float row_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4m3Max);
 }
 
 __device__ __forceinline__ void store8(uint8_t* dst, uint2 c, bool packed) {
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(const uint16_t* __r
        row += warps) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
     uint8_t* cr = codes + row * out_stride;
-    float sc, inv;
+    float sc;
     if constexpr (CPL > 0) {
       uint4 v[CPL];
       uint32_t m = 0;
@@ -100,17 +103,17 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(const uint16_t* __r
         v[i] = c < chunks ? __ldcs(xr + c) : make_uint4(0, 0, 0, 0);
         m = abs_max_bits(m, v[i]);
       }
-      row_scales(warp_amax(m), sc, inv);
+      sc = row_scale(warp_amax(m));
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = lane + 32 * i;
-        if (c < chunks) store8(cr + 8 * c, quant8(v[i], inv), PACKED);
+        if (c < chunks) store8(cr + 8 * c, quant8(v[i], sc), PACKED);
       }
     } else {
       uint32_t m = 0;
       for (int c = lane; c < chunks; c += 32) m = abs_max_bits(m, __ldg(xr + c));
-      row_scales(warp_amax(m), sc, inv);
-      for (int c = lane; c < chunks; c += 32) store8(cr + 8 * c, quant8(__ldcs(xr + c), inv), PACKED);
+      sc = row_scale(warp_amax(m));
+      for (int c = lane; c < chunks; c += 32) store8(cr + 8 * c, quant8(__ldcs(xr + c), sc), PACKED);
     }
     if (lane == 0) {
       if (PACKED) *reinterpret_cast<float*>(cr + H) = sc;

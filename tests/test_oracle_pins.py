@@ -523,6 +523,62 @@ def check_row_quant_roundtrip():
     assert np.allclose(sc, amax / 448.0, rtol=2 ** -23, atol=0)
 
 
+def _rn_binary32(v):
+    """Exact round-to-nearest-even of a Fraction to IEEE binary32 (normal and subnormal
+    range, no overflow at these sizes), returned as a Fraction."""
+    from fractions import Fraction
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    quantum = Fraction(2) ** max(e - 23, -149)     # 24 significant bits, or the subnormal step
+    q, r = divmod(a, quantum)
+    if r * 2 > quantum or (r * 2 == quantum and q % 2 == 1):
+        q += 1
+    return sign * q * quantum
+
+
+def _e4m3_code_exact(v):
+    """E4M3 code of a Fraction by exhaustive search over the format's definition (bias 7,
+    3 mantissa bits, no infinities, S.1111.111 = NaN): nearest magnitude, ties to the even
+    code, above 448 saturated to 448, the sign bit from v."""
+    from fractions import Fraction
+    mags = []
+    for code in range(127):                        # 0x00 .. 0x7E, increasing magnitude
+        ef, mf = code >> 3, code & 7
+        mags.append(Fraction(mf, 8) * Fraction(2) ** -6 if ef == 0 else (1 + Fraction(mf, 8)) * Fraction(2) ** (ef - 7))
+    a = min(abs(v), mags[-1])
+    best = min(range(127), key=lambda c: (abs(mags[c] - a), c % 2))
+    return best | (0x80 if v < 0 else 0)
+
+
+def check_row_quant_exact_rational():
+    """The row quantiser against exact rational arithmetic: scale = RN32(m / 448) and
+    code = E4M3(RN32(x / scale)) evaluated with Fractions and an independent binary32
+    rounding, on rows of bf16 values whose largest magnitudes span 2^-20 .. 2^20.  On
+    this input the multiply-by-reciprocal form E4M3(RN32(x * RN32(448 / m))) gives other
+    codes (checked with plain float32 arithmetic), so the pin tells the readings apart."""
+    from fractions import Fraction
+    rng = np.random.default_rng(19)  # a seed whose rows hold codes the two forms round apart
+    x = (rng.normal(0, 1, (48, 96)) * np.exp2(rng.integers(-20, 20, 48))[:, None]).astype(np.float32)
+    bits = synth.encode_bf16(x)
+    xb = codes.decode_bf16(bits).astype(np.float32)
+    c, sc = orq.row_quantize(bits)
+    for t in range(xb.shape[0]):
+        m = max(max(Fraction(float(v)) for v in np.abs(xb[t])), Fraction(2) ** -100)
+        scale = _rn_binary32(m / 448)
+        assert Fraction(float(sc[t])) == scale, t
+        for h in range(xb.shape[1]):
+            q = _rn_binary32(Fraction(float(xb[t, h])) / scale)
+            assert c[t, h] == _e4m3_code_exact(q), (t, h, float(xb[t, h]), float(q))
+    m32 = np.maximum(np.max(np.abs(xb), axis=1), np.float32(2.0 ** -100)).astype(np.float32)
+    recip = orq.encode_e4m3_rne_sat((xb * (np.float32(448) / m32)[:, None]).astype(np.float32))
+    assert np.count_nonzero(recip != c) > 0
+
+
 def check_row_quant_packed():
     """The packed row: H codes, then the fp32 scale's four bytes."""
     rng = np.random.default_rng(13)
@@ -535,7 +591,8 @@ def check_row_quant_packed():
 
 @pytest.mark.parametrize("check", [check_e4m3_encoder_vs_torch, check_e4m3_encoder_saturates,
                                    check_row_quant_hand, check_row_quant_zero_row,
-                                   check_row_quant_roundtrip, check_row_quant_packed])
+                                   check_row_quant_roundtrip, check_row_quant_packed,
+                                   check_row_quant_exact_rational])
 def test_row_quant(check):
     check()
 
@@ -802,7 +859,7 @@ ALL_CHECKS = [check_decoders, check_projection_permutation, check_projection_blo
               check_kv_v1_bf16, check_kv_v1_int8, check_kv_v2_int8, check_kv_v2_pa_bf16,
               check_kv_bad_index, check_e4m3_encoder_vs_torch, check_e4m3_encoder_saturates,
               check_row_quant_hand, check_row_quant_zero_row, check_row_quant_roundtrip,
-              check_row_quant_packed, check_nbsd_layout, check_fp8_encoders_vs_torch,
+              check_row_quant_packed, check_row_quant_exact_rational, check_nbsd_layout, check_fp8_encoders_vs_torch,
               check_kv_norm_mode, check_kv_norm_v1_no_outputs, check_kv_blk_mode,
               check_kv_rope_broadcast, check_kv_fp16_inputs, check_kv_fp8_caches,
               check_per_head_norm, check_qkv_per_head_segments]
@@ -884,6 +941,12 @@ def mutants():
         safe = np.maximum(np.max(np.abs(x), axis=1), np.float32(2.0 ** -100)).astype(np.float32)
         return orig_enc(x * (np.float32(240) / safe)[:, None]), (safe / np.float32(240)).astype(np.float32)
 
+    def rq_reciprocal(bits):                # x times RN(448 / m) in place of x / scale
+        c, sc = orig_rq(bits)
+        x = codes.decode_bf16(np.asarray(bits, np.uint16)).astype(np.float32)
+        safe = np.maximum(np.max(np.abs(x), axis=1), np.float32(2.0 ** -100)).astype(np.float32)
+        return orig_enc((x * (np.float32(448) / safe)[:, None]).astype(np.float32)), sc
+
     orig_slots = okv.token_slots
     orig_rows = okv.cache_rows
     orig_fp8 = codes.encode_fp8
@@ -910,7 +973,7 @@ def mutants():
     return [(oq, "rms_norm_per_head", ph_over_all_heads), (okv, "token_slots", slots_blk_per_token), (okv, "cache_rows", rows_norm_ignores_batch),
             (codes, "encode_fp8", fp8_no_saturation),
             (orq, "encode_e4m3_rne_sat", enc_half_away), (orq, "encode_e4m3_rne_sat", enc_no_saturation),
-            (orq, "row_quantize", rq_fnuz_range),
+            (orq, "row_quantize", rq_fnuz_range), (orq, "row_quantize", rq_reciprocal),
             (oq, "rope_rotate_half", rh_sign), (oq, "rms_norm_across_heads", norm_no_eps),
             (oq, "rms_norm_across_heads", norm_pre_gamma_width), (oq, "dequant_weight", dw_transposed_blocks),
             (okv, "interleave_rope", il_no_deinterleave), (okv, "quantize", q_half_away),
