@@ -1,9 +1,11 @@
 """Benchmark of the attention-prologue hot path on GB300.
 
-One step = the whole hot path over one batch of synthetic input:
+One step = the whole hot path over one batch of synthetic input, in this order:
   K1 qkv_cte_mx_project   (block-scaled FP8 GEMM + dequant + bias + sums of squares)
-  K2 qkv_cte_mx_norm_rope (across-heads RMSNorm + rotate-half RoPE, in place)
   K3 kv_rms_norm_rope_cache (RMSNorm + interleaved RoPE + int8 quant + paged scatter)
+  K2 qkv_cte_mx_norm_rope (across-heads RMSNorm + rotate-half RoPE, in place)
+The KV-cache call does not depend on the projection, so it goes between the two
+passes of qkv_cte_mx (whose second pass needs the first's sums of squares).
 on the Wan2.2-A14B 720p self-attention projection (S=75600 = 21x45x80, H=5120,
 40+40+40 heads of 128, I=15360, MXFP8 weights, 3-D RoPE) together with the
 separate-k/v KvRmsNormRopeCache call (kv [8,8,4096,192], v [8,8,4096,128],
@@ -214,8 +216,8 @@ def run_ours(args):
 
     def step():
         q.project()
-        q.norm_rope()
         k.run()
+        q.norm_rope()
 
     for _ in range(args.warmup):
         step()
@@ -239,9 +241,9 @@ def run_ours(args):
             ev[i][0].record(stream)
             q.project()
             ev[i][1].record(stream)
-            q.norm_rope()
-            ev[i][2].record(stream)
             k.run()
+            ev[i][2].record(stream)
+            q.norm_rope()
             ev[i][3].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
@@ -249,8 +251,8 @@ def run_ours(args):
         torch.distributed.barrier()
     total_ms = start.elapsed_time(end)
     k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    k3 = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    k3 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    k2 = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
     total_ms = dist.max_over_ranks(total_ms, device="cuda")  # the slowest rank's time
     ms = total_ms / K
     flops = qcase.flops
@@ -480,8 +482,8 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
             if used[b]:
                 s_cmp.wait_event(outputs_read[b])      # step i-2's results are on the host
             qq.project(s_cmp)
-            qq.norm_rope(s_cmp)
             kk.run(s_cmp)
+            qq.norm_rope(s_cmp)
             compute_done[b].record(s_cmp)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(compute_done[b])
@@ -493,21 +495,35 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
     for i in range(max(2, min(args.warmup, 3))):
         step(i)
     torch.cuda.synchronize()
+    link_before = measure_link(h_in, dev_in(q, k), h_out[0], (q.out, k.k_cache, k.ckv_cache), s_h2d, s_d2h, bi, bo)
+    # one untimed window of K steps, then three timed ones.  The first window after
+    # the buffers are allocated ran at about half speed on every box measured (the
+    # first copies into freshly pinned host memory); later windows agree to 0.1 %.
+    # The host link is also shared with other jobs on the machine, so the median of
+    # the three windows is reported, with each window's time
     K = max(2, min(args.steps, 10))
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(s_h2d)
-    for i in range(K):
-        step(i)
-    s_h2d.wait_stream(s_d2h)
-    end.record(s_h2d)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(end) / K
+    windows = []
+    for w in range(4):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(s_h2d)
+        for i in range(K):
+            step(i)
+        s_h2d.wait_stream(s_d2h)
+        end.record(s_h2d)
+        torch.cuda.synchronize()
+        if w > 0:
+            windows.append(start.elapsed_time(end) / K)
+    ms = statistics.median(windows)
     ms = dist.max_over_ranks(ms, device="cuda")
-    link = measure_link(h_in, dev_in(q, k), h_out[0], (q.out, k.k_cache, k.ckv_cache), s_h2d, s_d2h, bi, bo)
+    link_after = measure_link(h_in, dev_in(q, k), h_out[0], (q.out, k.k_cache, k.ckv_cache), s_h2d, s_d2h, bi, bo)
+    link = min((link_before, link_after), key=lambda d: d["link_bound_ms"])
+    link["link_bound_ms_before_after"] = [link_before["link_bound_ms"], link_after["link_bound_ms"]]
     del q2, k2
     return {"value": round(dist.job_rate(qcase.flops, ws, ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "overlap": "uploads, kernels and downloads of consecutive steps on three streams",
+            "ms_per_step": round(ms, 3), "window_ms": [round(w, 3) for w in windows],
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "overlap": "uploads, kernels and downloads of consecutive steps on three streams; "
+                       "median of three %d-step windows after an untimed one" % K,
             "link": link, "e2e_frac_of_link": round(link["link_bound_ms"] / ms, 4)}
 
 

@@ -121,9 +121,10 @@ struct QuantTab {
 // Fills one table (every head) from the per-channel scale / offset arrays, or
 // from their one value when they are [1] (`scalar`).
 __device__ __forceinline__ void fill_table(float4* ts, float4* to, const float* scale, const float* offset,
-                                           int heads, int width, TabLayout l, bool scalar) {
+                                           int heads, int width, TabLayout l, bool scalar,
+                                           int tid, int nthreads) {
   const int groups = width / 4, n = heads * groups;
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+  for (int e = tid; e < n; e += nthreads) {
     const int hd = e / groups, u = e - hd * groups;
     const int pos = hd * l.stride + ((u & 1) ? l.odd : 0) + (u >> 1) * l.step;
     if (scalar) {
@@ -486,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
       next += RPG;
     }
   }
-  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, kw, kl, p.k_scalar != 0);
-  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, cw, vl, p.v_scalar != 0);
+  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, kw, kl, p.k_scalar != 0, threadIdx.x, blockDim.x);
+  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, cw, vl, p.v_scalar != 0, threadIdx.x, blockDim.x);
   __syncthreads();
 
   for (int64_t base = r_begin; base < r_end; base += DEPTH * RPG) {
@@ -601,8 +602,6 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, T::KW, kl, p.k_scalar != 0);
-  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, T::CW, vl, p.v_scalar != 0);
   __syncthreads();
 
   if (warp == kConsumerWarps) {
@@ -659,7 +658,14 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
     return;
   }
 
-  // consumers
+  // consumers: the quantisation tables first (the producer's first copies are already
+  // in flight), then a barrier among the consumer warps only; every consumer thread
+  // reaches it, since nothing before it can leave early
+  if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, T::KW, kl, p.k_scalar != 0, threadIdx.x,
+                       kConsumerWarps * 32);
+  if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, T::CW, vl, p.v_scalar != 0, threadIdx.x,
+                       kConsumerWarps * 32);
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
   const int g = lane / T::LPR, j = lane % T::LPR;
   uint4 gam[T::CPL];
 #pragma unroll
@@ -696,7 +702,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
         }
       }
       if (j < T::R / 8) {
-        if (bcast) {  // cos/sin [B, N, 1, R]: the row of this (b, n)
+        if (bcast) {  // cos/sin [B, N, 1, R]: the row of this (b, n), from the cache hierarchy
           const size_t off = static_cast<size_t>(bn_s[s * kTileRows + lr]) * T::R;
           const uint16_t* cg = p.cos + off;
           const uint16_t* sg = p.sin + off;
