@@ -276,6 +276,7 @@ def run_ours(args):
         e2e = measure_e2e(q, k, qcase, kcase, args, ws)
     # rows measured outside the step come last, so their buffers cannot disturb it
     nxt = {} if args.no_next else {"row_quantize_e4m3": time_row_quantize(qcase, args, hbm),
+                                   "qkv_cte_mx_bsd": time_variant(q, args, fp8_peak, "bsd"),
                                    "qkv_cte_mx_per_head": time_variant(q, args, fp8_peak, "per_head"),
                                    "qkv_cte_mx_nbsd": time_variant(q, args, fp8_peak, "nbsd"),
                                    **time_kv_variants(kcase, args, hbm)}
@@ -346,19 +347,29 @@ def time_row_quantize(qcase, args, hbm_gbs):
             "note": "measured alone, not part of the step"}
 
 
+VARIANT_IDLE_S = 1.0  # idle time before each variant's window (see time_variant)
+
+
 def time_variant(q, args, fp8_peak, which):
     """A variant of the step's projection + second pass on the same inputs and
     weights, timed alone (CUDA events over K calls after W warm-ups):
+      bsd       the step's own call (BSD output, across-heads norms), the
+                reference the other rows compare with;
       per_head  q_norm = k_norm = RMS_PER_HEAD (each head normed by its own RMS,
                 gamma [head_dim]), then the rotate-half RoPE;
       nbsd      the output layout [I / head_dim, B, S, head_dim] of the
-                cross-attention calls."""
+                cross-attention calls.
+    The projection is power-limited (its clock falls the longer the GPU has been
+    busy), so every variant starts its window after the same idle time, and the
+    rows compare with the bsd row, not with the step."""
     import torch
     from rope_attention_gb300 import native, runner, synth
     c = q.case
     pp = native.QkvCteMxParams.from_buffer_copy(q.params)
     qg, kg, out = q.q_gamma, q.k_gamma, q.out
-    if which == "per_head":
+    if which == "bsd":
+        note = "the step's call (BSD output, across-heads norms), timed like the other variants"
+    elif which == "per_head":
         pp.q_norm = pp.k_norm = native.RA_NORM_RMS_PER_HEAD
         qg = runner.to_dev(synth.stream(97, 0).uniform(0.5, 1.5, c.head_dim).astype("float32"))
         kg = runner.to_dev(synth.stream(97, 1).uniform(0.5, 1.5, c.head_dim).astype("float32"))
@@ -373,6 +384,8 @@ def time_variant(q, args, fp8_peak, which):
         native.qkv_cte_mx_project(pp, q.a, q.a_scale, q.w_packed, q.weight_scales, q.bias, qg, kg, out, ws)
         native.qkv_cte_mx_norm_rope(pp, q.cos, q.sin, out, ws)
 
+    torch.cuda.synchronize()
+    time.sleep(VARIANT_IDLE_S)
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
@@ -392,8 +405,8 @@ def time_variant(q, args, fp8_peak, which):
     del ws
     return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4),
             "projection_ms": round(k1_ms, 4), "second_pass_ms": round(k2_ms, 4),
-            "note": f"{note} on the step's projection, projection + second pass, measured alone, "
-                    "not part of the step"}
+            "note": f"{note} on the step's projection, projection + second pass, measured alone after "
+                    f"{VARIANT_IDLE_S:.0f} s idle, not part of the step"}
 
 
 def time_kv_variants(kcase, args, hbm_gbs):
@@ -496,14 +509,15 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
         step(i)
     torch.cuda.synchronize()
     link_before = measure_link(h_in, dev_in(q, k), h_out[0], (q.out, k.k_cache, k.ckv_cache), s_h2d, s_d2h, bi, bo)
-    # one untimed window of K steps, then three timed ones.  The first window after
+    # one untimed window of K steps, then five timed ones.  The first window after
     # the buffers are allocated ran at about half speed on every box measured (the
     # first copies into freshly pinned host memory); later windows agree to 0.1 %.
-    # The host link is also shared with other jobs on the machine, so the median of
-    # the three windows is reported, with each window's time
+    # The host link is also shared with other jobs on the machine (single windows
+    # measured up to twice as long at random), so the median of the five windows is
+    # reported, with each window's time
     K = max(2, min(args.steps, 10))
     windows = []
-    for w in range(4):
+    for w in range(6):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(s_h2d)
         for i in range(K):
@@ -523,7 +537,7 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
             "ms_per_step": round(ms, 3), "window_ms": [round(w, 3) for w in windows],
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "overlap": "uploads, kernels and downloads of consecutive steps on three streams; "
-                       "median of three %d-step windows after an untimed one" % K,
+                       "median of five %d-step windows after an untimed one" % K,
             "link": link, "e2e_frac_of_link": round(link["link_bound_ms"] / ms, 4)}
 
 

@@ -239,9 +239,10 @@ void ra_test_validate_only(int32_t on);
 void ra_test_stall_next_projection(void);
 
 /* Test hook for failure detection.  The next norm/RoPE pass (qkv_cte_mx or
- * qkv_cte_mx_norm_rope) that runs the pipelined kernel -- BSD output, head_dim
- * 64 or 128, at most 24 KB of rewritten Q/K columns per token -- issues none of
- * its copies, so its waits run out after the time limit above; every block
+ * qkv_cte_mx_norm_rope) that runs a pipelined kernel -- head_dim 64 or 128, and
+ * BSD output with at most 24 KB of rewritten Q/K columns per token, or NBSd
+ * output -- issues none of its copies, so its waits run out after the time
+ * limit above; every block
  * records the timeout in the workspace status word and exits, and
  * qkv_cte_mx_status reports RA_ERR_TIMEOUT.  Nothing is in flight when the
  * waits give up.  The output of that call is undefined.  Applies to one call,

@@ -1,9 +1,12 @@
 // Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "rope_attention.h"
 
@@ -82,6 +85,21 @@ struct NormRopeLaunch {
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream);
 
 int device_sm_count();
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (null if unavailable)
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
 
 // Sets the thread-local message returned by ra_last_error() ("where: what").
 void set_last_error(int code, const char* where, const char* what);

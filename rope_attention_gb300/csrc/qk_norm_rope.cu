@@ -23,6 +23,8 @@
 // time so that several 16-byte loads are in flight; cos/sin loads are warp
 // broadcasts (all heads of a token share them); the arithmetic uses packed
 // fp32x2 FMAs; the bf16 results are 16-byte vectors, coalesced across threads.
+#include <cudaTypedefs.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -365,6 +367,272 @@ cudaError_t launch_staged(const NormRopeLaunch& L, const StagePlan& pl, cudaStre
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- pipelined kernel, NBSd
+// For the NBSd layout out [I / d, T, d] with head_dim 64 or 128.  The rewritten
+// heads are consecutive planes of that stack, so TB consecutive tokens of 16
+// consecutive heads are one 3-D box [d, TB, 16] of it: one tensor copy (TMA)
+// moves a box into a stage and one tensor store writes it back, the hardware
+// doing the plane strides.  The tokens' partial sums, exponents and cos/sin rows
+// are contiguous rows and come in with bulk copies, as in the BSD kernel.  A
+// stage holds TB tokens of every rewritten head; each consumer thread keeps one
+// token and one 8-column offset within a head for the whole stage, so it reads
+// its cos/sin and its token's inv_rms once per stage.  Boxes that run past the
+// last token or the last rewritten head are zero-filled on load and clipped on
+// store, so no other plane is touched.  Every wait is bounded, as in the BSD kernel.
+constexpr int kNbHeads = 16;               // heads per tensor box
+constexpr int kNbSt = 3;                   // stages
+constexpr int kNbWarps = 8;                // consumer warps (one block per SM; 16 measured slower)
+constexpr int kNbThreads = (kNbWarps + 1) * 32;
+constexpr uint32_t kNbSmem = 200u * 1024;  // stage bytes of a block, at most
+
+struct NbPlan {                            // byte offsets within a stage
+  uint32_t tb, nbox, nh;                   // tokens per stage, boxes, rewritten heads
+  uint32_t box_bytes, part, exps, cos, sin, bytes;
+  uint32_t part_row, exp_row, cs_row;      // per-token bytes of each side row
+};
+
+NbPlan nb_plan(const NormRopeLaunch& L, uint32_t tb) {
+  const int h_begin = L.do_q ? 0 : L.num_q_heads;
+  const int h_end = (L.num_k_heads > 0 && L.do_k) ? L.num_q_heads + L.num_k_heads : L.num_q_heads;
+  NbPlan pl{};
+  pl.tb = tb;
+  pl.nh = static_cast<uint32_t>(h_end - h_begin);
+  pl.nbox = (pl.nh + kNbHeads - 1) / kNbHeads;
+  pl.box_bytes = static_cast<uint32_t>(kNbHeads) * tb * static_cast<uint32_t>(L.head_dim) * 2u;
+  pl.part_row = L.n_part_tiles > 0 ? static_cast<uint32_t>(L.part_stride) * 8u : 0u;
+  pl.exp_row = static_cast<uint32_t>(L.exp_stride);
+  pl.cs_row = L.rope ? static_cast<uint32_t>(L.head_dim) * 4u : 0u;
+  auto up = [](uint32_t x) { return (x + 127u) & ~127u; };
+  pl.part = pl.nbox * pl.box_bytes;
+  pl.exps = up(pl.part + tb * pl.part_row);
+  pl.cos = up(pl.exps + tb * pl.exp_row);
+  pl.sin = up(pl.cos + tb * pl.cs_row);
+  pl.bytes = up(pl.sin + tb * pl.cs_row);
+  return pl;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+template <int D, bool ROT>
+__global__ void __launch_bounds__(kNbThreads, 1)
+    qk_norm_rope_nbsd_kernel(const NormRopeLaunch p, const NbPlan pl, const __grid_constant__ CUtensorMap tmap) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int HALF = D / 2;
+  constexpr int PER_HEAD = ROT ? D / 16 : D / 8;  // 8-column items per head
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = p.num_q_heads, nk = p.num_k_heads;
+  const int h_begin = p.do_q ? 0 : nq;
+  const int TB = static_cast<int>(pl.tb);
+  const uint32_t units = static_cast<uint32_t>((p.T + TB - 1) / TB);
+  const uint32_t bars = smem_u32(smem + kNbSt * pl.bytes);  // full[kNbSt], empty[kNbSt], done[kNbSt]
+  auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
+  auto empty_bar = [&](uint32_t s) { return bars + 8u * (kNbSt + s); };
+  auto done_bar = [&](uint32_t s) { return bars + 8u * (2 * kNbSt + s); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kNbSt * pl.bytes + 3 * kNbSt * 8);
+  const uint32_t stage0 = smem_u32(smem);
+  const uint64_t limit = static_cast<uint64_t>(p.wait_ns);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNbSt; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(done_bar(s), kNbWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmap);
+  }
+  __syncthreads();
+
+  if (warp == kNbWarps) {
+    // producer: unit (TB tokens) k of this block goes to stage k % kNbSt
+    if (lane == 0) {
+      uint32_t k = 0;
+      bool live = true;
+      for (uint32_t unit = blockIdx.x; unit < units; unit += gridDim.x, ++k) {
+        const uint32_t s = k % kNbSt, use = k / kNbSt;
+        if (k >= kNbSt && !bounded_wait_one(empty_bar(s), (use & 1u) ^ 1u, limit, abort_flag)) {
+          live = false;
+          break;
+        }
+        const int64_t t0 = static_cast<int64_t>(unit) * TB;
+        const uint32_t nt = static_cast<uint32_t>(p.T - t0 < TB ? p.T - t0 : TB);
+        const uint32_t full = full_bar(s), dst = stage0 + s * pl.bytes;
+        // a box counts its full size, zero-filled past the last token or head
+        mbar_arrive_expect_tx(full, pl.nbox * pl.box_bytes + nt * (pl.part_row + pl.exp_row + 2 * pl.cs_row));
+        if (!p.stall_loads) {
+          for (uint32_t b = 0; b < pl.nbox; ++b)
+            tma_load_3d(dst + b * pl.box_bytes, &tmap, full, 0, static_cast<int32_t>(t0),
+                        static_cast<int32_t>(b * kNbHeads));
+          if (pl.part_row) bulk_load(dst + pl.part, p.partials + t0 * p.part_stride, nt * pl.part_row, full);
+          bulk_load(dst + pl.exps, p.exps + t0 * p.exp_stride, nt * pl.exp_row, full);
+          if (ROT) {
+            bulk_load(dst + pl.cos, p.cos + t0 * D, nt * pl.cs_row, full);
+            bulk_load(dst + pl.sin, p.sin + t0 * D, nt * pl.cs_row, full);
+          }
+        }
+      }
+      if (!live) atomicExch(p.status, 1);
+      // leave only when no copy into this block's shared memory can still be in flight
+      for (uint32_t u = k > static_cast<uint32_t>(kNbSt) ? k - kNbSt : 0; u < k; ++u)
+        if (!bounded_drain(full_bar(u % kNbSt), (u / kNbSt) & 1u, limit)) atomicExch(p.status, 1);
+    }
+    return;
+  }
+
+  // consumers
+  const int ct = threadIdx.x;                                // 0 .. 32 * kNbWarps - 1
+  const int u = ct % PER_HEAD;                               // this thread's 8-column offset within a head
+  const int tok = (ct / PER_HEAD) % TB;                      // and its token within the stage
+  const int hstep = (kNbWarps * 32) / (PER_HEAD * TB);       // heads between this thread's items
+  const int head0 = ct / (PER_HEAD * TB);
+  const int q_end = nq * D;
+  const bool storer = threadIdx.x == 0;
+  const float wq = static_cast<float>(nq * D), wk = static_cast<float>(nk * D);
+  uint32_t k = 0;
+  bool ok = true;
+  for (uint32_t unit = blockIdx.x; unit < units; unit += gridDim.x, ++k) {
+    const uint32_t s = k % kNbSt, use = k / kNbSt;
+    if (!bounded_wait_warp(full_bar(s), use & 1u, limit, abort_flag)) {
+      ok = false;
+      break;
+    }
+    uint8_t* st = smem + s * pl.bytes;
+    const int64_t t0 = static_cast<int64_t>(unit) * TB;
+    const int nt = static_cast<int>(p.T - t0 < TB ? p.T - t0 : TB);
+    // 1b: inv_rms of this thread's token; every warp sums the stage's partials in the
+    // same fixed order (lane-strided, then an xor tree)
+    float inv_q = 1.f, inv_k = 1.f;
+    const float2* part = reinterpret_cast<const float2*>(st + pl.part);
+    for (int tt = 0; tt < nt; ++tt) {
+      float sq = 0.f, sk = 0.f;
+      for (int j = lane; j < p.n_part_tiles; j += 32) {
+        const float2 v = part[tt * p.part_stride + j];
+        sq += v.x;
+        sk += v.y;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      if (tt == tok) {
+        inv_q = p.q_norm ? rsqrtf(sq / wq + p.eps) : 1.f;
+        inv_k = p.k_norm ? rsqrtf(sk / wk + p.eps) : 1.f;
+      }
+    }
+    if (tok < nt) {
+      const int8_t* ex = reinterpret_cast<const int8_t*>(st + pl.exps) + tok * pl.exp_row;
+      float2 c_lo[4], c_hi[4], s_lo[4], s_hi[4];
+      if (ROT) {
+        const float* cs = reinterpret_cast<const float*>(st + pl.cos + tok * pl.cs_row) + 8 * u;
+        const float* sn = reinterpret_cast<const float*>(st + pl.sin + tok * pl.cs_row) + 8 * u;
+        lds8f(cs, c_lo);
+        lds8f(cs + HALF, c_hi);
+        lds8f(sn, s_lo);
+        lds8f(sn + HALF, s_hi);
+      }
+      for (int head = head0; head < static_cast<int>(pl.nh); head += hstep) {
+        const int col = (h_begin + head) * D + 8 * u;
+        const float inv = col < q_end ? inv_q : inv_k;
+        uint4* lo = reinterpret_cast<uint4*>(st + 2 * ((head * TB + tok) * D + 8 * u));
+        float2 y_lo[4];
+        decode8(*lo, inv * exp2_int(ex[col / kPartCols]), y_lo);
+        if (ROT) {
+          uint4* hi = lo + HALF / 8;
+          float2 y_hi[4];
+          decode8(*hi, inv * exp2_int(ex[(col + HALF) / kPartCols]), y_hi);
+          float2 o_lo[4], o_hi[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            o_lo[m] = __ffma2_rn(y_lo[m], c_lo[m], __fmul2_rn(y_hi[m], make_float2(-s_lo[m].x, -s_lo[m].y)));
+            o_hi[m] = __ffma2_rn(y_hi[m], c_hi[m], __fmul2_rn(y_lo[m], s_hi[m]));
+          }
+          *lo = pack8(o_lo);
+          *hi = pack8(o_hi);
+        } else {
+          *lo = pack8(y_lo);
+        }
+      }
+    }
+    // the rewritten boxes are read next by the tensor stores (async proxy)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done_bar(s));
+    if (warp == 0) {
+      int go = 1;
+      if (storer) {
+        go = bounded_wait_one(done_bar(s), use & 1u, limit, abort_flag) ? 1 : 0;
+        if (go) {
+          for (uint32_t b = 0; b < pl.nbox; ++b)
+            tma_store_3d(&tmap, stage0 + s * pl.bytes + b * pl.box_bytes, 0, static_cast<int32_t>(t0),
+                         static_cast<int32_t>(b * kNbHeads));
+          bulk_commit();
+          bulk_wait_read<1>();  // the previous unit's stores have read their stage
+          if (k > 0) mbar_arrive(empty_bar((k - 1) % kNbSt));
+        }
+      }
+      go = __shfl_sync(0xffffffffu, go, 0);
+      if (!go) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  if (!ok && lane == 0) atomicExch(p.status, 1);
+  if (storer) bulk_wait_all();  // this thread's stores are complete before the block ends
+}
+
+size_t nb_smem(const NbPlan& pl) { return static_cast<size_t>(kNbSt) * pl.bytes + 3 * kNbSt * 8 + 16; }
+
+// the largest stage of 8, 4, 2 or 1 tokens whose ring fits the budget (0: none fits)
+uint32_t nb_tokens(const NormRopeLaunch& L) {
+  for (uint32_t tb = 8; tb >= 1; tb /= 2)
+    if (tb <= L.T && nb_smem(nb_plan(L, tb)) <= kNbSmem) return tb;
+  return 0;
+}
+
+template <int D, bool ROT>
+cudaError_t launch_nbsd(const NormRopeLaunch& L, const NbPlan& pl, cudaStream_t st) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorInvalidValue;
+  const int h_begin = L.do_q ? 0 : L.num_q_heads;
+  // the rewritten heads' planes as a [nh, T, D] stack of 16-bit values
+  CUtensorMap tmap;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L.T), pl.nh};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L.T) * D * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), pl.tb, static_cast<cuuint32_t>(kNbHeads)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  void* base = L.out + static_cast<size_t>(h_begin) * L.T * D;
+  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  auto kernel = qk_norm_rope_nbsd_kernel<D, ROT>;
+  const size_t smem = nb_smem(pl);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kNbThreads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int64_t units = (L.T + pl.tb - 1) / pl.tb;
+  const int64_t cap = static_cast<int64_t>(per_sm) * device_sm_count();
+  kernel<<<static_cast<unsigned>(units < cap ? units : cap), kNbThreads, smem, st>>>(L, pl, tmap);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream) {
@@ -376,6 +644,15 @@ cudaError_t launch_qk_norm_rope(const NormRopeLaunch& L, cudaStream_t stream) {
   if (staged) {
     if (L.head_dim == 128) return L.rope ? launch_staged<128, true>(L, pl, stream) : launch_staged<128, false>(L, pl, stream);
     return L.rope ? launch_staged<64, true>(L, pl, stream) : launch_staged<64, false>(L, pl, stream);
+  }
+  if (L.nbsd && L.status != nullptr && (L.head_dim == 64 || L.head_dim == 128) && pl.span_bytes > 0 &&
+      L.exp_stride > 0 && L.exp_stride % 16 == 0 && L.part_stride % 2 == 0 && L.T < (int64_t(1) << 31)) {
+    const uint32_t tb = nb_tokens(L);
+    if (tb > 0) {
+      const NbPlan np = nb_plan(L, tb);
+      if (L.head_dim == 128) return L.rope ? launch_nbsd<128, true>(L, np, stream) : launch_nbsd<128, false>(L, np, stream);
+      return L.rope ? launch_nbsd<64, true>(L, np, stream) : launch_nbsd<64, false>(L, np, stream);
+    }
   }
   const int64_t blocks = (L.T + kTok - 1) / kTok;
   qk_norm_rope_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(L);

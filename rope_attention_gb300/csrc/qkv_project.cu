@@ -627,20 +627,6 @@ __global__ void pack_sf_kernel(const uint8_t* __restrict__ e, uint8_t* __restric
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
 bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                   uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();

@@ -47,9 +47,10 @@ def test_stalled_pipeline_reports_timeout_and_context_survives():
     check_qkv(case, as_f64(run.out), qkv_reference(case), "call after a timed-out launch")
 
 
-def test_stalled_norm_rope_pipeline_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("layout", [native.RA_LAYOUT_BSD, native.RA_LAYOUT_NBSD], ids=["bsd", "nbsd"])
+def test_stalled_norm_rope_pipeline_reports_timeout_and_context_survives(layout):
     case = synth.qkv_tiny()
-    run = runner.QkvRun(case)
+    run = runner.QkvRun(case, layout=layout)
     native.ra_set_wait_timeout_ns(2_000_000)  # 2 ms per wait
     try:
         run.project()
@@ -67,7 +68,10 @@ def test_stalled_norm_rope_pipeline_reports_timeout_and_context_survives():
         assert run.status() == 0
     finally:
         native.ra_set_wait_timeout_ns(DEFAULT_WAIT_NS)
-    check_qkv(case, as_f64(run.out), qkv_reference(case), "call after a timed-out norm/RoPE pass")
+    out = run.out
+    if layout == native.RA_LAYOUT_NBSD:  # [I / d, T, d] -> [T, I]
+        out = out.permute(1, 0, 2).reshape(case.T, case.I)
+    check_qkv(case, as_f64(out), qkv_reference(case), "call after a timed-out norm/RoPE pass")
 
 
 def test_stalled_kv_pipeline_reports_timeout_and_context_survives():

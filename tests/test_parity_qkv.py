@@ -67,6 +67,14 @@ NBSD = [
     ("cross_q", dict(S=300, H=512, num_heads=6, num_kv_heads=0, head_dim=128, rope=None)),
     ("cross_v", dict(S=77, H=256, num_heads=2, num_kv_heads=0, head_dim=128, rope=None, q_norm=False)),
     ("d16_one_row", dict(S=1, H=128, num_heads=1, num_kv_heads=1, head_dim=16)),
+    # the pipelined NBSd pass: 19 rewritten heads (a full box of 16 and a clipped one)
+    # with 7 V planes after them that must stay as projected, and token counts that are
+    # not a multiple of the tokens per stage
+    ("heads19_d128", dict(S=1001, H=256, num_heads=12, num_kv_heads=7, head_dim=128)),
+    ("heads19_d64", dict(B=3, S=333, H=256, num_heads=12, num_kv_heads=7, head_dim=64)),
+    ("heads33_norm_only_d64", dict(S=517, H=256, num_heads=20, num_kv_heads=13, head_dim=64, rope=None)),
+    ("q_norm_only_d128", dict(S=259, H=256, num_heads=5, num_kv_heads=3, head_dim=128, k_norm=False)),
+    ("two_rows", dict(S=2, H=128, num_heads=3, num_kv_heads=2, head_dim=64)),
 ]
 
 
@@ -184,3 +192,17 @@ def test_wan_cross_attention_sampled():
 def test_wan720_self_attention_sampled():
     """S=75600 (21x45x80), the bench workload."""
     _sampled(synth.qkv_wan720(), "wan720")
+
+
+def test_wan480_nbsd_sampled():
+    """The 480p self-attention call with output layout NBSd [120, 1, 32760, 128]: sampled
+    rows read back from the 120 head planes, against the oracle."""
+    case = synth.qkv_wan480()
+    r = run_full(case, layout=native.RA_LAYOUT_NBSD)
+    rows = torch.from_numpy(synth.sample_rows(case.T, seed=124)).cuda()
+    n = case.I // case.head_dim
+    got = r.out.view(n, case.T, case.head_dim)[:, rows, :].permute(1, 0, 2).reshape(len(rows), case.I)
+    got = as_f64(got)
+    del r
+    torch.cuda.empty_cache()
+    check_qkv(case, got, qkv_reference(case, rows.cpu().numpy()), "wan480_nbsd")
