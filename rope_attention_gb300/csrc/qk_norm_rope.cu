@@ -369,8 +369,8 @@ cudaError_t launch_staged(const NormRopeLaunch& L, const StagePlan& pl, cudaStre
 
 // ---------------------------------------------------------------- pipelined kernel, NBSd
 // For the NBSd layout out [I / d, T, d] with head_dim 64 or 128.  The rewritten
-// heads are consecutive planes of that stack, so TB consecutive tokens of 16
-// consecutive heads are one 3-D box [d, TB, 16] of it: one tensor copy (TMA)
+// heads are consecutive planes of that stack, so TB consecutive tokens of up to
+// 16 consecutive heads are one 3-D box [d, TB, 16] of it: one tensor copy (TMA)
 // moves a box into a stage and one tensor store writes it back, the hardware
 // doing the plane strides.  The tokens' partial sums, exponents and cos/sin rows
 // are contiguous rows and come in with bulk copies, as in the BSD kernel.  A
@@ -379,14 +379,18 @@ cudaError_t launch_staged(const NormRopeLaunch& L, const StagePlan& pl, cudaStre
 // its cos/sin and its token's inv_rms once per stage.  Boxes that run past the
 // last token or the last rewritten head are zero-filled on load and clipped on
 // store, so no other plane is touched.  Every wait is bounded, as in the BSD kernel.
-constexpr int kNbHeads = 16;               // heads per tensor box
+constexpr int kNbHeads = 16;               // heads per tensor box, at most
 constexpr int kNbSt = 3;                   // stages
-constexpr int kNbWarps = 8;                // consumer warps (one block per SM; 16 measured slower)
+constexpr int kNbWarps = 8;                // consumer warps
 constexpr int kNbThreads = (kNbWarps + 1) * 32;
-constexpr uint32_t kNbSmem = 200u * 1024;  // stage bytes of a block, at most
+constexpr int kNbBlocks = 3;               // blocks per SM
+// stage bytes of a block, at most: three blocks of three 1-token stages per SM
+// measured 0.514 ms at 720p against 0.58-0.61 ms for one block of three 2-token
+// stages, 0.61 ms for two blocks of two 2-token stages, 0.82 ms for 4-token stages
+constexpr uint32_t kNbSmem = 72u * 1024;
 
 struct NbPlan {                            // byte offsets within a stage
-  uint32_t tb, nbox, nh;                   // tokens per stage, boxes, rewritten heads
+  uint32_t tb, hb, nbox, nh;               // tokens per stage, heads per box, boxes, rewritten heads
   uint32_t box_bytes, part, exps, cos, sin, bytes;
   uint32_t part_row, exp_row, cs_row;      // per-token bytes of each side row
 };
@@ -397,8 +401,9 @@ NbPlan nb_plan(const NormRopeLaunch& L, uint32_t tb) {
   NbPlan pl{};
   pl.tb = tb;
   pl.nh = static_cast<uint32_t>(h_end - h_begin);
-  pl.nbox = (pl.nh + kNbHeads - 1) / kNbHeads;
-  pl.box_bytes = static_cast<uint32_t>(kNbHeads) * tb * static_cast<uint32_t>(L.head_dim) * 2u;
+  pl.hb = pl.nh < static_cast<uint32_t>(kNbHeads) ? pl.nh : static_cast<uint32_t>(kNbHeads);
+  pl.nbox = (pl.nh + pl.hb - 1) / pl.hb;
+  pl.box_bytes = pl.hb * tb * static_cast<uint32_t>(L.head_dim) * 2u;
   pl.part_row = L.n_part_tiles > 0 ? static_cast<uint32_t>(L.part_stride) * 8u : 0u;
   pl.exp_row = static_cast<uint32_t>(L.exp_stride);
   pl.cs_row = L.rope ? static_cast<uint32_t>(L.head_dim) * 4u : 0u;
@@ -426,7 +431,7 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int3
 }
 
 template <int D, bool ROT>
-__global__ void __launch_bounds__(kNbThreads, 1)
+__global__ void __launch_bounds__(kNbThreads, kNbBlocks)
     qk_norm_rope_nbsd_kernel(const NormRopeLaunch p, const NbPlan pl, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int HALF = D / 2;
@@ -475,7 +480,7 @@ __global__ void __launch_bounds__(kNbThreads, 1)
         if (!p.stall_loads) {
           for (uint32_t b = 0; b < pl.nbox; ++b)
             tma_load_3d(dst + b * pl.box_bytes, &tmap, full, 0, static_cast<int32_t>(t0),
-                        static_cast<int32_t>(b * kNbHeads));
+                        static_cast<int32_t>(b * pl.hb));
           if (pl.part_row) bulk_load(dst + pl.part, p.partials + t0 * p.part_stride, nt * pl.part_row, full);
           bulk_load(dst + pl.exps, p.exps + t0 * p.exp_stride, nt * pl.exp_row, full);
           if (ROT) {
@@ -578,7 +583,7 @@ __global__ void __launch_bounds__(kNbThreads, 1)
         if (go) {
           for (uint32_t b = 0; b < pl.nbox; ++b)
             tma_store_3d(&tmap, stage0 + s * pl.bytes + b * pl.box_bytes, 0, static_cast<int32_t>(t0),
-                         static_cast<int32_t>(b * kNbHeads));
+                         static_cast<int32_t>(b * pl.hb));
           bulk_commit();
           bulk_wait_read<1>();  // the previous unit's stores have read their stage
           if (k > 0) mbar_arrive(empty_bar((k - 1) % kNbSt));
@@ -613,7 +618,7 @@ cudaError_t launch_nbsd(const NormRopeLaunch& L, const NbPlan& pl, cudaStream_t 
   CUtensorMap tmap;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L.T), pl.nh};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L.T) * D * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), pl.tb, static_cast<cuuint32_t>(kNbHeads)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), pl.tb, pl.hb};
   cuuint32_t estr[3] = {1, 1, 1};
   void* base = L.out + static_cast<size_t>(h_begin) * L.T * D;
   if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -27,6 +27,7 @@ BUDGETS = {
     },
     "qk_norm_rope.cu": {
         "qk_norm_rope_staged_kernel": (128, 0),
+        "qk_norm_rope_nbsd_kernel": (75, 0),      # 288 threads, 3 blocks per SM: at most 75 registers
         "qk_norm_rope_kernel": (128, 0),
     },
     "kv_cache.cu": {
