@@ -509,23 +509,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 
 // ---------------------------------------------------------------- staged kernel
 // For the two common row shapes, in every cache mode and cache type.  A tile of
-// kTileRows consecutive (b, n, s) rows is one contiguous span in each of kv, v,
+// consecutive (b, n, s) rows is one contiguous span in each of kv, v,
 // cos and sin, so one lane of a producer warp moves it into shared memory with
 // four bulk copies (cp.async.bulk, completion counted by the stage's mbarrier;
 // with S-broadcast cos/sin only kv and v are copied, and the consumers read the
 // one cos/sin row of each (b, n), which stays cached, straight from global memory),
-// kStages - 1 tiles ahead of four consumer warps.  The producer warp also looks up
+// kStages - 1 tiles ahead of the consumer warps.  The producer warp also looks up
 // each row's head, its index entry (per token, or per block of block_size tokens
 // in PA_BLK_BNSD) and the row's batch (Norm) or place in its block (PA_BLK_BNSD).  The consumers run the same row arithmetic as
 // the kernel above on operands read from shared memory, with a row's lanes
 // adjacent so that those reads are free of bank conflicts.  Every wait has a time
 // limit: when one runs out the block records it in the status word and leaves,
 // the producer first waiting (with a limit) for the copies it issued.
-constexpr int kTileRows = 16;
 constexpr int kStages = 3;
-constexpr int kConsumerWarps = 4;
-constexpr int kStagedThreads = (kConsumerWarps + 1) * 32;
-static_assert(kTileRows <= 32, "one producer lane per tile row");
 
 __device__ int32_t g_kv_status;
 
@@ -533,16 +529,16 @@ __device__ int32_t g_kv_status;
 struct StagedPlan {
   uint32_t tables, stage_bytes, stages, slots, heads, auxs, bns, bars, flag, total;
 };
-__host__ __device__ inline StagedPlan staged_plan(uint32_t table_bytes, uint32_t stage_bytes) {
+__host__ __device__ inline StagedPlan staged_plan(uint32_t table_bytes, uint32_t stage_bytes, uint32_t tile_rows) {
   StagedPlan pl;
   pl.tables = 0;
   pl.stage_bytes = stage_bytes;
   pl.stages = (table_bytes + 127u) & ~127u;
   pl.slots = pl.stages + kStages * stage_bytes;
-  pl.heads = pl.slots + kStages * kTileRows * 8;
-  pl.auxs = pl.heads + kStages * kTileRows * 4;
-  pl.bns = pl.auxs + kStages * kTileRows * 4;
-  pl.bars = pl.bns + kStages * kTileRows * 4;
+  pl.heads = pl.slots + kStages * tile_rows * 8;
+  pl.auxs = pl.heads + kStages * tile_rows * 4;
+  pl.bns = pl.auxs + kStages * tile_rows * 4;
+  pl.bars = pl.bns + kStages * tile_rows * 4;
   pl.flag = pl.bars + 2 * kStages * 8;
   pl.total = pl.flag + 16;
   return pl;
@@ -555,21 +551,29 @@ struct StagedShape {
   static constexpr int RMS = VARIANT == 1 ? DKV - R : DKV;
   static constexpr int KW = VARIANT == 1 ? R : DKV, CW = VARIANT == 1 ? RMS : Sh::dv;
   static constexpr int LPR = VARIANT == 1 ? 16 : 8, CPL = VARIANT == 1 ? 4 : 3, RPG = 32 / LPR;
-  static constexpr uint32_t KV_B = kTileRows * DKV * 2, V_B = kTileRows * DV * 2, CS_B = kTileRows * R * 2;
+  // tile rows, consumer warps and blocks per SM.  V2 rows (640 B) take tiles of 32 rows
+  // for 8 consumer warps, two blocks per SM: 0.0525 ms at 720p against 0.0543 ms for
+  // 16-row tiles, 4 warps and three blocks (S-broadcast: 0.0537 against 0.0584).  V1
+  // rows (1408 B) keep 16-row tiles: with 32 they fit one block per SM and took
+  // 0.080 ms against 0.073 ms (int8 MLA call)
+  static constexpr int TILE = VARIANT == 1 ? 16 : 32, CWARPS = VARIANT == 1 ? 4 : 8;
+  static constexpr int THREADS = (CWARPS + 1) * 32, MIN_BLOCKS = VARIANT == 1 ? 3 : 2;
+  static constexpr uint32_t KV_B = TILE * DKV * 2, V_B = TILE * DV * 2, CS_B = TILE * R * 2;
   static constexpr uint32_t STAGE_B = KV_B + V_B + 2 * CS_B;
-  static constexpr uint32_t ROW_B = STAGE_B / kTileRows;
-  static constexpr int STEPS = kTileRows / (kConsumerWarps * RPG);  // row groups per consumer warp and tile
+  static constexpr uint32_t ROW_B = STAGE_B / TILE;
+  static constexpr int STEPS = TILE / (CWARPS * RPG);  // row groups per consumer warp and tile
   // V1 keeps the plain table layout: its step (a DRAM-bound mix of reads and
   // row-contiguous output writes) measured faster with it (74 vs 77 us), though
   // the split layout has fewer bank conflicts.
   static constexpr bool SPLIT = VARIANT == 2;
-  static_assert(STEPS * kConsumerWarps * RPG == kTileRows, "tile rows split evenly over the consumer warps");
+  static_assert(STEPS * CWARPS * RPG == TILE, "tile rows split evenly over the consumer warps");
+  static_assert(TILE <= 32, "one producer lane per tile row");
   static_assert(RMS / 8 <= LPR * CPL && Sh::dv / 8 <= LPR * CPL && R / 8 <= LPR, "lane layout holds the row");
 };
 
 // GEN: Norm / PA_BLK_BNSD addressing and FP8 caches compiled in
 template <int VARIANT, bool F16, bool GEN>
-__global__ void __launch_bounds__(kStagedThreads, 3)
+__global__ void __launch_bounds__(StagedShape<VARIANT>::THREADS, StagedShape<VARIANT>::MIN_BLOCKS)
     kv_staged_kernel(const KvLaunch p, const KvAux aux, const uint32_t tiles) {
   using T = StagedShape<VARIANT>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -579,7 +583,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   const int heads = VARIANT == 2 ? static_cast<int>(p.N) : 1;
   const TabLayout kl = tab_layout(T::KW, T::SPLIT), vl = tab_layout(T::CW, T::SPLIT);
   const int ku = p.kq ? heads * kl.stride : 0, vu = p.vq ? heads * vl.stride : 0;
-  const StagedPlan pl = staged_plan(static_cast<uint32_t>(2 * (ku + vu) * 16), T::STAGE_B);
+  const StagedPlan pl = staged_plan(static_cast<uint32_t>(2 * (ku + vu) * 16), T::STAGE_B, T::TILE);
   float4* ks = reinterpret_cast<float4*>(smem);
   float4* ko = ks + ku;
   float4* vs = ko + ku;
@@ -597,14 +601,14 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bars + 8 * s, 32);                           // every producer lane arrives
-      mbar_init(bars + 8 * (kStages + s), kConsumerWarps);   // one arrive per consumer warp
+      mbar_init(bars + 8 * (kStages + s), T::CWARPS);   // one arrive per consumer warp
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == T::CWARPS) {
     // producer: tile k of this block goes to stage k % kStages
     uint32_t k = 0;
     bool live = true;
@@ -614,8 +618,8 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
         live = false;
         break;
       }
-      const uint32_t r0 = tile * kTileRows;
-      const uint32_t nr = rows - r0 < static_cast<uint32_t>(kTileRows) ? rows - r0 : kTileRows;
+      const uint32_t r0 = tile * T::TILE;
+      const uint32_t nr = rows - r0 < static_cast<uint32_t>(T::TILE) ? rows - r0 : T::TILE;
       const uint32_t full = bars + 8 * s;
       if (lane == 0) {  // the copies first, so that the slot lookups below overlap them
         mbar_expect_tx(full, nr * (bcast ? T::ROW_B - 4 * T::R : T::ROW_B));
@@ -641,10 +645,10 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
           ipos = static_cast<int64_t>(b) * aux.blocks_per_batch + blk;
           ax = static_cast<int32_t>(sq - blk * static_cast<uint32_t>(p.block_size));
         }
-        slot_s[s * kTileRows + lane] = __ldg(p.index + ipos);
-        head_s[s * kTileRows + lane] = static_cast<int32_t>(bn - b * N);
-        aux_s[s * kTileRows + lane] = ax;
-        bn_s[s * kTileRows + lane] = static_cast<int32_t>(bn);
+        slot_s[s * T::TILE + lane] = __ldg(p.index + ipos);
+        head_s[s * T::TILE + lane] = static_cast<int32_t>(bn - b * N);
+        aux_s[s * T::TILE + lane] = ax;
+        bn_s[s * T::TILE + lane] = static_cast<int32_t>(bn);
       }
       mbar_arrive(full);  // each lane releases its own writes above
     }
@@ -662,10 +666,10 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
   // in flight), then a barrier among the consumer warps only; every consumer thread
   // reaches it, since nothing before it can leave early
   if (p.kq) fill_table(ks, ko, p.k_scale, p.k_offset, heads, T::KW, kl, p.k_scalar != 0, threadIdx.x,
-                       kConsumerWarps * 32);
+                       T::CWARPS * 32);
   if (p.vq) fill_table(vs, vo, p.v_scale, p.v_offset, heads, T::CW, vl, p.v_scalar != 0, threadIdx.x,
-                       kConsumerWarps * 32);
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+                       T::CWARPS * 32);
+  asm volatile("bar.sync 1, %0;" ::"r"(T::CWARPS * 32) : "memory");
   const int g = lane / T::LPR, j = lane % T::LPR;
   uint4 gam[T::CPL];
 #pragma unroll
@@ -684,7 +688,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
       return;
     }
     const uint8_t* st = smem + pl.stages + s * T::STAGE_B;
-    const uint32_t r0 = tile * kTileRows;
+    const uint32_t r0 = tile * T::TILE;
 #pragma unroll
     for (int step = 0; step < T::STEPS; ++step) {
       const int lr = (warp * T::STEPS + step) * T::RPG + g;  // row within the tile
@@ -703,7 +707,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
       }
       if (j < T::R / 8) {
         if (bcast) {  // cos/sin [B, N, 1, R]: the row of this (b, n), from the cache hierarchy
-          const size_t off = static_cast<size_t>(bn_s[s * kTileRows + lr]) * T::R;
+          const size_t off = static_cast<size_t>(bn_s[s * T::TILE + lr]) * T::R;
           const uint16_t* cg = p.cos + off;
           const uint16_t* sg = p.sin + off;
           in.c1 = __ldg(reinterpret_cast<const uint2*>(cg + 4 * j));
@@ -719,9 +723,9 @@ __global__ void __launch_bounds__(kStagedThreads, 3)
           in.s2 = *reinterpret_cast<const uint2*>(sn + T::R + 8 * j);
         }
       }
-      in.slot = slot_s[s * kTileRows + lr];
-      in.n = head_s[s * kTileRows + lr];
-      in.aux = GEN ? aux_s[s * kTileRows + lr] : 0;
+      in.slot = slot_s[s * T::TILE + lr];
+      in.n = head_s[s * T::TILE + lr];
+      in.aux = GEN ? aux_s[s * T::TILE + lr] : 0;
       const uint32_t row = r0 + lr;
       w.process(in, row, row < rows);
     }
@@ -735,19 +739,19 @@ cudaError_t launch_staged(const KvLaunch& L, const KvAux& aux, cudaStream_t st) 
   using T = StagedShape<VARIANT>;
   auto kernel = kv_staged_kernel<VARIANT, F16, GEN>;
   const StagedPlan pl =
-      staged_plan(static_cast<uint32_t>(quant_table_bytes(L, L.kq != 0, L.vq != 0, T::SPLIT)), T::STAGE_B);
+      staged_plan(static_cast<uint32_t>(quant_table_bytes(L, L.kq != 0, L.vq != 0, T::SPLIT)), T::STAGE_B, T::TILE);
   const cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.total));
   if (e != cudaSuccess) return e;
   const int64_t rows = L.B * L.N * L.S;
-  const uint32_t tiles = static_cast<uint32_t>((rows + kTileRows - 1) / kTileRows);
+  const uint32_t tiles = static_cast<uint32_t>((rows + T::TILE - 1) / T::TILE);
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStagedThreads, pl.total) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, T::THREADS, pl.total) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   const int64_t cap = static_cast<int64_t>(per_sm) * device_sm_count();
   const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
-  kernel<<<grid, kStagedThreads, pl.total, st>>>(L, aux, tiles);
+  kernel<<<grid, T::THREADS, pl.total, st>>>(L, aux, tiles);
   return cudaGetLastError();
 }
 
@@ -802,7 +806,7 @@ bool launch_fixed(const KvLaunch& L, const KvAux& aux, int lpr, int cpl, bool ge
   const bool shape = VARIANT == 1 ? L.Dkv == RowShape<1>::dkv && L.R == RowShape<1>::r && lpr == 16 && cpl == 4
                                    : L.Dkv == RowShape<2>::dkv && L.Dv == RowShape<2>::dv && L.R == RowShape<2>::r &&
                                          lpr == 8 && cpl == 3;
-  if (!shape || L.status == nullptr || L.B * L.N * L.S >= (int64_t(1) << 31) - kTileRows)
+  if (!shape || L.status == nullptr || L.B * L.N * L.S >= (int64_t(1) << 31) - StagedShape<VARIANT>::TILE)
     return false;
   *err = gen ? launch_staged<VARIANT, F16, true>(L, aux, st) : launch_staged<VARIANT, F16, false>(L, aux, st);
   return true;
