@@ -224,3 +224,38 @@ def test_full_sep_v2_outputs_off():
     case = synth.kv_sep_v2(is_output_kv=False)
     stats = check_kv(case, run_case(case), "sep_v2_outputs_off")
     print("tie differences:", stats)
+
+
+def _bf16_values(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def test_every_slot_skipped():
+    """index all -1: no cache slot is written (every one keeps its sentinel), while the
+    k_rope / c_kv outputs are still written for every row."""
+    case = synth.make_kv("all_skip", 12, variant=2, B=2, N=4, S=50, Dkv=192, Dv=128, block_size=32,
+                         block_num=4, quant_k=True, quant_v=True, skip_frac=1.0)
+    assert (case.index == -1).all()
+    run = run_case(case)
+    assert run.outputs
+    check_kv(case, run, "all-skipped")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_zero_huge_and_tiny_rows(variant):
+    """Rows of zeros (RMS 0, so eps alone), rows scaled by 1e15 (int8 codes saturate at
+    -128 / 127) and by 1e-15 (eps dominates the RMS), through the pipelined kernel."""
+    kw = (dict(variant=1, B=2, N=1, S=40, Dkv=576, Dv=512) if variant == 1
+          else dict(variant=2, B=2, N=8, S=40, Dkv=192, Dv=128))
+    case = synth.make_kv(f"extreme_v{variant}", 13, block_size=32, block_num=(3 if variant == 1 else 20),
+                         quant_k=True, quant_v=True, **kw)
+    kv = _bf16_values(case.kv)
+    kv[:, :, 0:5] = 0
+    kv[:, :, 5:10] *= np.float32(1e15)
+    kv[:, :, 10:15] *= np.float32(1e-15)
+    case.kv[:] = synth.encode_bf16(kv)
+    if case.v is not None:
+        v = _bf16_values(case.v)
+        v[:, :, 5:10] *= np.float32(1e15)
+        case.v[:] = synth.encode_bf16(v)
+    check_kv(case, run_case(case), f"extreme-v{variant}")

@@ -206,3 +206,32 @@ def test_wan480_nbsd_sampled():
     del r
     torch.cuda.empty_cache()
     check_qkv(case, got, qkv_reference(case, rows.cpu().numpy()), "wan480_nbsd")
+
+
+def _degenerate(case, bias_on: bool):
+    """Rows and weight blocks at the edges of what the operator meets: all-zero rows
+    (v = bias), rows whose dequant scale is 1e-20 and 1e-30 of the others (v is bias,
+    or tiny when there is no bias, so eps dominates their RMS), rows scaled up 1e3, and
+    W blocks whose MX exponents are moved 20 binades up or down (columns of one row
+    that differ by 2^40, inside the same 128-column blocks of the intermediate)."""
+    c = case
+    c.a[0:8] = 0
+    c.a_scale[8:16] *= np.float32(1e-20)
+    c.a_scale[16:24] *= np.float32(1e-30)
+    c.a_scale[24:32] *= np.float32(1e3)
+    e = c.w_block_exp.astype(np.int32)
+    e[1, 0:96] += 20
+    e[3, 200:330] -= 20
+    c.w_block_exp[:] = np.clip(e, 1, 254).astype(np.uint8)
+    return c
+
+
+@pytest.mark.parametrize("bias", [True, False], ids=["bias", "no_bias"])
+def test_degenerate_rows_and_blocks(bias):
+    case = _degenerate(synth.make_qkv("degenerate", 71, S=260, H=256, num_heads=3, num_kv_heads=2,
+                                      head_dim=64, bias=bias), bias)
+    r = run_full(case)
+    check_qkv(case, as_f64(r.out), qkv_reference(case), f"degenerate ({'bias' if bias else 'no bias'})")
+    s = run_full(case, split=True, layout=native.RA_LAYOUT_NBSD)
+    back = s.out.view(torch.int16).cpu().numpy().transpose(1, 0, 2).reshape(case.T, case.I)
+    assert np.array_equal(back, r.out.view(torch.int16).cpu().numpy()), "NBSd != BSD"
