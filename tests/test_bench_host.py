@@ -64,3 +64,9 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # what was timed is what is reported: a step is one bounded sample, shorter than the
+    # full step the value is extrapolated to, and the config is the repo arm's own
+    assert 0 < d["ms_per_step"] < 1e3 * d["extrapolated_step_s"]
+    from bench import bench_config, workload
+    q, k = workload("small")
+    assert d["config"] == bench_config(q, k, 2)
