@@ -63,9 +63,11 @@ def test_rejections_reach_a_c_caller_with_their_messages(c_output):
     assert lib.ra_last_error().decode() == c_output["bad_h_message"]
 
 
-def test_call_sequence_example_compiles():
-    """tests/c/example_prologue.c, the setup / step / status sequence from C with the
-    CUDA runtime (it needs a GPU to run, so it is compiled only)."""
+@pytest.mark.parametrize("src", ["example_prologue.c", "prologue_gpu.c"])
+def test_call_sequence_example_compiles(src):
+    """tests/c/example_prologue.c (the setup / step / status sequence from C with the
+    CUDA runtime) and tests/c/prologue_gpu.c (the program the GPU test runs) compile
+    as strict C99 here; they need a GPU to run."""
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
@@ -77,6 +79,6 @@ def test_call_sequence_example_compiles():
     if cuda_inc is None:
         pytest.skip("CUDA runtime headers not found")
     cmd = [cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE,
-           "-isystem", cuda_inc, "-c", os.path.join(HERE, "c", "example_prologue.c"), "-o", os.devnull]
+           "-isystem", cuda_inc, "-c", os.path.join(HERE, "c", src), "-o", os.devnull]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, f"{' '.join(cmd)}\n{r.stdout}\n{r.stderr}"
