@@ -19,12 +19,16 @@ from rope_attention_gb300 import native, runner, synth
 pytestmark = pytest.mark.gpu
 
 
-def test_step_replays_from_a_cuda_graph():
-    # across-heads norm + RoPE in BSD (pipelined second pass), V2 int8 PA_BNSD (pipelined KV kernel)
+@pytest.mark.parametrize("layout", [native.RA_LAYOUT_BSD, native.RA_LAYOUT_NBSD], ids=["bsd", "nbsd"])
+def test_step_replays_from_a_cuda_graph(layout):
+    # across-heads norm + RoPE in BSD or NBSd (the pipelined second passes; NBSd's takes a
+    # tensor map as a kernel parameter), V2 int8 PA_BNSD (pipelined KV kernel)
     qcase = synth.make_qkv("graph_q", 41, S=300, H=256, num_heads=4, num_kv_heads=4, head_dim=64)
     kcase = synth.make_kv("graph_kv", 42, variant=2, B=2, N=8, S=40, Dkv=192, Dv=128, block_size=32,
                           block_num=4, quant_k=True, quant_v=True, skip_frac=0.1)
-    q, k = runner.QkvRun(qcase), runner.KvRun(kcase)
+    q, k = runner.QkvRun(qcase, layout=layout), runner.KvRun(kcase)
+    as_bsd = (lambda t: t) if layout == native.RA_LAYOUT_BSD else \
+        (lambda t: t.permute(1, 0, 2).reshape(qcase.T, qcase.I))
     q.project()
     q.norm_rope()
     k.run()
@@ -43,7 +47,7 @@ def test_step_replays_from_a_cuda_graph():
     graph.replay()
     torch.cuda.synchronize()
     assert q.status() == 0 and native.kv_rms_norm_rope_cache_status() == 0
-    check_qkv(qcase, as_f64(q.out), qkv_reference(qcase), "graph replay")
+    check_qkv(qcase, as_f64(as_bsd(q.out)), qkv_reference(qcase), "graph replay")
     check_kv(kcase, k, "graph replay")
 
     first = (q.out.clone(), k.k_cache.clone(), k.ckv_cache.clone())
