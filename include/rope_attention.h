@@ -38,9 +38,11 @@
  *    caller reads after synchronising (qkv_cte_mx_status,
  *    kv_rms_norm_rope_cache_status, dev_error_count).
  *  - bf16 values are passed as their 16-bit patterns (uint16_t).
- *  - The compute calls launch kernels only (no allocation, no synchronisation),
- *    so after one eager call per device they can be captured into a CUDA graph
- *    and replayed; the status readers synchronise and cannot be captured.
+ *  - qkv_cte_mx, qkv_cte_mx_project, qkv_cte_mx_norm_rope, row_quantize_e4m3,
+ *    row_quantize_e4m3_packed, qkv_cte_mx_pack_weight and kv_rms_norm_rope_cache
+ *    launch kernels only (no allocation, no synchronisation), so after one
+ *    eager call per device they can be captured into a CUDA graph and
+ *    replayed; the status readers synchronise and cannot be captured.
  */
 #ifndef ROPE_ATTENTION_H_
 #define ROPE_ATTENTION_H_
@@ -201,8 +203,8 @@ ra_status qkv_cte_mx_status(void* workspace, void* stream, int32_t* device_statu
  *   - Problems whose qkv_cte_mx_workspace_bytes exceeds 32 MiB are rejected
  *     with RA_ERR_WORKSPACE before anything is launched.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and later calls on that
+ *     device reuse it.
  *   - Every call shares the array: calls that overlap on the GPU (unordered
  *     streams or threads) race and give undefined results.  Calls ordered on
  *     one stream are independent (each call clears the status word, once its
