@@ -250,6 +250,76 @@ __device__ __forceinline__ void tc_mma_pair_mxf8(uint32_t d_tmem, uint64_t adesc
       : "memory");
 }
 
+// Two consecutive pipeline stages of the 2-SM block-scaled MMA, issued from one asm
+// block, with a look-ahead probe of the next two stages' full barriers.
+//
+// For each of the two stages: copy the stage's W scale image into its TMEM slot
+// (sfb0, then sfb0 + 8), issue four K=32 MMAs into the accumulator d (the first one
+// of the pair accumulates only when acc_first != 0), and commit to the stage's empty
+// barrier in both CTAs (ebar0, then ebar0 + 8).  The second stage's operands sit one
+// stage further in shared memory: +1024 in the descriptors' 16-byte address units
+// for 16 KB operand stages, +256 for the 4 KB scale images.
+//
+// Before any of that, mbarrier.test_wait (acquire) probes the full barriers nbar0 and
+// nbar0 + 8 for phase parity nphase; the result (both complete) is returned.  Its
+// predicate is read only after the last commit.  A shared-memory round trip of the
+// issuing thread takes hundreds of cycles while the tensor core streams operands,
+// and the thread cannot issue past an instruction that waits for such a result; with
+// the read at the end, the probe's latency overlaps the issue of eight MMAs instead
+// of leaving the tensor pipe without queued work (measured: 27.8k cycles per
+// 160-MMA tile with a wait per stage, 20.5k with this form, 20.48k ideal).
+// The caller keeps the ring and the scale slots from wrapping inside a pair (even
+// first stage, even ring length).
+__device__ __forceinline__ bool tc_mma_stage_pair_mxf8(uint32_t nbar0, uint32_t nphase, uint32_t sfb0,
+                                                       uint64_t sfd0, uint32_t d, uint64_t ad0, uint64_t bd0,
+                                                       uint32_t idesc, uint32_t sfa, uint32_t acc_first,
+                                                       uint32_t ebar0) {
+  uint32_t both_full;
+  asm volatile(
+      "{\n\t"
+      ".reg .pred full0, full1, acc0, on;\n\t"
+      ".reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7, sfd1;\n\t"
+      ".reg .b32 id1, id2, id3, sfb1, nbar1, ebar1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 full0, [%1], %2;\n\t"
+      "add.u32 nbar1, %1, 8;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 full1, [nbar1], %2;\n\t"
+      // the scale-factor ids of K steps 1..3 (bits [29,31) for A, [4,6) for B)
+      "or.b32 id1, %8, 0x20000010;\n\t"
+      "or.b32 id2, %8, 0x40000020;\n\t"
+      "or.b32 id3, %8, 0x60000030;\n\t"
+      "setp.ne.b32 acc0, %10, 0;\n\t"
+      "setp.eq.b32 on, 0, 0;\n\t"
+      "add.s64 a1, %6, 2;\n\tadd.s64 b1, %7, 2;\n\t"
+      "add.s64 a2, %6, 4;\n\tadd.s64 b2, %7, 4;\n\t"
+      "add.s64 a3, %6, 6;\n\tadd.s64 b3, %7, 6;\n\t"
+      "tcgen05.cp.cta_group::2.128x256b [%3], %4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], %6, %7, %8, [%9], [%3], acc0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a1, b1, id1, [%9], [%3], on;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a2, b2, id2, [%9], [%3], on;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a3, b3, id3, [%9], [%3], on;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%11], %12;\n\t"
+      "add.u32 sfb1, %3, 8;\n\tadd.s64 sfd1, %4, 256;\n\t"
+      "add.s64 a4, %6, 1024;\n\tadd.s64 b4, %7, 1024;\n\t"
+      "add.s64 a5, %6, 1026;\n\tadd.s64 b5, %7, 1026;\n\t"
+      "add.s64 a6, %6, 1028;\n\tadd.s64 b6, %7, 1028;\n\t"
+      "add.s64 a7, %6, 1030;\n\tadd.s64 b7, %7, 1030;\n\t"
+      "add.u32 ebar1, %11, 8;\n\t"
+      "tcgen05.cp.cta_group::2.128x256b [sfb1], sfd1;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a4, b4, %8, [%9], [sfb1], on;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a5, b5, id1, [%9], [sfb1], on;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a6, b6, id2, [%9], [sfb1], on;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a7, b7, id3, [%9], [sfb1], on;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [ebar1], %12;\n\t"
+      "and.pred full0, full0, full1;\n\t"
+      "selp.u32 %0, 1, 0, full0;\n\t"
+      "}"
+      : "=r"(both_full)
+      : "r"(nbar0), "r"(nphase), "r"(sfb0), "l"(sfd0), "r"(d), "l"(ad0), "l"(bd0), "r"(idesc), "r"(sfa),
+        "r"(acc_first), "r"(ebar0), "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+  return both_full != 0;
+}
+
 // ---------------------------------------------------------------- small utils
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);

@@ -32,7 +32,10 @@
 //    thread issues the MMAs and copies W's ue8m0 block scales into TMEM each
 //    stage (tcgen05.cp); A's MX scale is the constant 2^0 (its fp32 row scale is
 //    applied in the epilogue, since it is constant along K); commits multicast
-//    to both CTAs;
+//    to both CTAs.  With an even number of K steps it issues two stages per asm
+//    block and learns whether the next two have landed from a probe issued at the
+//    block's start and read at its end, so the thread never stalls on a barrier
+//    read while the tensor pipe has work queued;
 //  * warps 2-9 (both CTAs): epilogue, two warps per TMEM lane quadrant, each
 //    owning 128 of the 256 columns; they pull the whole accumulator into
 //    registers first and release TMEM before the math and stores, so the next
@@ -331,13 +334,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
+      // An even number of K steps per tile keeps every tile (and so every pair of
+      // stages) starting on an even stage of the even-length ring: those calls issue
+      // two stages per asm block with a look-ahead probe of the next pair's barriers
+      // (tc_mma_stage_pair_mxf8).  `ready` is that probe's answer for the pair about
+      // to be issued; without it the issuer takes the bounded waits.
+      const bool paired = (p.num_k & 1) == 0;
+      static_assert(STAGES % 2 == 0, "stage pairs must not wrap the ring");
+      static_assert(A_BYTES == 16384 && B_BYTES == 16384 && SF_BYTES == 4096 && BK == 128,
+                    "tc_mma_stage_pair_mxf8 steps stages by 16 KB operands, 4 KB scale images, 4 K steps");
+      bool ready = false;
       for (int tile = pair; ok && tile < num_tiles; tile += num_pairs, ++local) {
         if (!wait_one(acce_bar, (static_cast<uint32_t>(local) & 1u) ^ 1u, p.wait_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < p.num_k; ++kb) {
+        for (int kb = 0; paired && kb < p.num_k; kb += 2) {
+          if (!ready && !(wait_one(full_bar(stage), phase, p.wait_ns, abort_flag) &&
+                          wait_one(full_bar(stage + 1), phase, p.wait_ns, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nstage = stage + 2 == STAGES ? 0 : stage + 2;
+          const uint32_t nphase = nstage == 0 ? phase ^ 1u : phase;
+          ready = tc_mma_stage_pair_mxf8(full_bar(nstage), nphase, tmem + SFB_COL,
+                                         sf_desc0 + static_cast<uint64_t>(stage * (SF_BYTES >> 4)), tmem + ACC_COL,
+                                         a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4)),
+                                         b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4)), kIdesc,
+                                         tmem + SFA_COL, kb != 0 ? 1u : 0u, empty_bar(stage));
+          stage = nstage;
+          phase = nphase;
+        }
+        for (int kb = 0; !paired && kb < p.num_k; ++kb) {
           if (!wait_one(full_bar(stage), phase, p.wait_ns, abort_flag)) {
             ok = false;
             break;
