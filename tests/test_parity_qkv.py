@@ -1,7 +1,7 @@
 """GPU parity: qkv_cte_mx (C-ABI) against the fp64 oracle.
 
-Small cases are compared in full: they span several 128-row and 240-column
-tiles, ragged row and column tails, single-segment calls, per-channel weight
+Small cases are compared in full: they span several 256 x 256 pair tiles,
+ragged row and column tails, single-segment calls, per-channel weight
 scales, no bias, norm without RoPE and RoPE without norm.  The full-size Wan
 workloads are compared on a deterministic row sample (first 128 rows, last
 256 rows covering the M tail, 640 random rows) with every column, so the
@@ -59,6 +59,22 @@ def test_small(name, kw):
     case = synth.make_qkv(name, 200 + len(name), **kw)
     r = run_full(case)
     check_qkv(case, as_f64(r.out), qkv_reference(case), name)
+
+
+# The projection's MMA issuer takes one of two loops by the number of 128-deep K steps
+# (H / 128): an even count issues two pipeline stages per asm block with a look-ahead
+# probe of the next pair's full barriers, an odd count one stage per bounded wait.
+# 2600 rows x 2048 columns are 88 pair tiles, more than there are CTA pairs, so some
+# pairs run two tiles and carry the ring position and the look-ahead across a tile.
+K_STEPS = [1, 2, 3, 6, 7, 12]
+
+
+@pytest.mark.parametrize("k_steps", K_STEPS, ids=[f"k_steps_{k}" for k in K_STEPS])
+def test_mma_issue_paths(k_steps):
+    case = synth.make_qkv(f"k_steps_{k_steps}", 300 + k_steps, S=2600, H=128 * k_steps, num_heads=8,
+                          num_kv_heads=4, head_dim=128)
+    r = run_full(case)
+    check_qkv(case, as_f64(r.out), qkv_reference(case), case.name)
 
 
 NBSD = [
