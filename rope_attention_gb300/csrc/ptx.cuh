@@ -250,6 +250,27 @@ __device__ __forceinline__ void tc_mma_pair_mxf8(uint32_t d_tmem, uint64_t adesc
       : "memory");
 }
 
+// True once both mbarriers at bar0 and bar0 + 8 have completed the phase with the
+// given parity.  The two non-blocking probes go out back to back, so one
+// shared-memory round trip answers both.
+__device__ __forceinline__ bool mbar_test_wait_pair(uint32_t bar0, uint32_t parity) {
+  uint32_t both;
+  asm volatile(
+      "{\n\t"
+      ".reg .pred f0, f1;\n\t"
+      ".reg .b32 bar1;\n\t"
+      "add.u32 bar1, %1, 8;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 f0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 f1, [bar1], %2;\n\t"
+      "and.pred f0, f0, f1;\n\t"
+      "selp.u32 %0, 1, 0, f0;\n\t"
+      "}"
+      : "=r"(both)
+      : "r"(bar0), "r"(parity)
+      : "memory");
+  return both != 0;
+}
+
 // Two consecutive pipeline stages of the 2-SM block-scaled MMA, issued from one asm
 // block, with a look-ahead probe of the next two stages' full barriers.
 //

@@ -146,6 +146,23 @@ __device__ bool wait_one(uint32_t bar, uint32_t parity, uint64_t limit, volatile
   }
 }
 
+// single-thread bounded wait on a stage pair's two full barriers (same parity); each
+// poll probes both in one shared-memory round trip, not one after the other
+__device__ bool wait_pair(uint32_t bar0, uint32_t parity, uint64_t limit, volatile int* abort_flag) {
+  if (mbar_test_wait_pair(bar0, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait_pair(bar0, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // warp-collective bounded wait: every lane returns the same answer
 __device__ bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit, volatile int* abort_flag) {
   uint64_t t0 = 0;
@@ -351,8 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         for (int kb = 0; paired && kb < p.num_k; kb += 2) {
-          if (!ready && !(wait_one(full_bar(stage), phase, p.wait_ns, abort_flag) &&
-                          wait_one(full_bar(stage + 1), phase, p.wait_ns, abort_flag))) {
+          if (!ready && !wait_pair(full_bar(stage), phase, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
