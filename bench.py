@@ -536,6 +536,9 @@ def measure_e2e(q, k, qcase, kcase, args, ws):
     return {"value": round(dist.job_rate(qcase.flops, ws, ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "window_ms": [round(w, 3) for w in windows],
             "best_window_ms": round(min(windows), 3),
+            # every timed step, stalled windows included: the whole timed run's rate
+            "mean_window_ms": round(statistics.mean(windows), 3),
+            "mean_value": round(dist.job_rate(qcase.flops, ws, statistics.mean(windows) * 1e-3) / 1e12, 2),
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "overlap": "uploads, kernels and downloads of consecutive steps on three streams; "
                        "median of nine %d-step windows after an untimed one" % K,
