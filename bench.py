@@ -56,7 +56,7 @@ def load_peaks():
 # changes the figure no longer describes it and the bench reports null.
 K1_SOURCES = ("rope_attention_gb300/csrc/qkv_project.cu", "rope_attention_gb300/csrc/ptx.cuh",
               "rope_attention_gb300/csrc/internal.h")
-K1_DRAM_BYTES = {("wan720", "5af21baa8b785b6f"): 3443695360 + 2367149312}
+K1_DRAM_BYTES = {("wan720", "26acdd46ea11ee54"): 2206546176 + 2351111424}
 
 
 def k1_source_digest() -> str:

@@ -1,6 +1,8 @@
 // Inline-PTX helpers for sm_103a: mbarriers, TMA (cp.async.bulk), and the
 // 5th-generation tensor core (tcgen05: TMEM allocation, MMA, copies, loads).
-// Each wrapper is one PTX instruction written from the PTX ISA.
+// Each wrapper is written from the PTX ISA.  Most are one instruction; the MMA
+// stage helpers issue a whole pipeline stage (or two) from one asm block, for the
+// reason given at tc_mma_stage_pair_mxf8.
 #pragma once
 
 #include <cstdint>
@@ -230,24 +232,9 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void tc_cp_pair_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 __device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
-}
-// 2-SM block-scaled MMA: A rows split across the CTA pair, B columns split across the pair
-__device__ __forceinline__ void tc_mma_pair_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
-      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
 }
 
 // True once both mbarriers at bar0 and bar0 + 8 have completed the phase with the
@@ -269,6 +256,46 @@ __device__ __forceinline__ bool mbar_test_wait_pair(uint32_t bar0, uint32_t pari
       : "r"(bar0), "r"(parity)
       : "memory");
   return both != 0;
+}
+
+// One pipeline stage of the 2-SM block-scaled MMA from one asm block, with a
+// look-ahead probe of the next stage's full barrier: probe nbar for phase parity
+// nphase (mbarrier.test_wait, acquire), copy the stage's W scale image into the TMEM
+// slot sfb, issue four K=32 MMAs into d (the first accumulates only when
+// acc_first != 0), commit to the stage's empty barrier ebar in both CTAs, and only
+// then read the probe's predicate (see tc_mma_stage_pair_mxf8 below for why the read
+// comes last).  For calls whose number of K steps is odd.
+__device__ __forceinline__ bool tc_mma_stage_mxf8(uint32_t nbar, uint32_t nphase, uint32_t sfb, uint64_t sfd,
+                                                  uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                                  uint32_t sfa, uint32_t acc_first, uint32_t ebar) {
+  uint32_t full;
+  asm volatile(
+      "{\n\t"
+      ".reg .pred full0, acc0, on;\n\t"
+      ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      ".reg .b32 id1, id2, id3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 full0, [%1], %2;\n\t"
+      "or.b32 id1, %8, 0x20000010;\n\t"
+      "or.b32 id2, %8, 0x40000020;\n\t"
+      "or.b32 id3, %8, 0x60000030;\n\t"
+      "setp.ne.b32 acc0, %10, 0;\n\t"
+      "setp.eq.b32 on, 0, 0;\n\t"
+      "add.s64 a1, %6, 2;\n\tadd.s64 b1, %7, 2;\n\t"
+      "add.s64 a2, %6, 4;\n\tadd.s64 b2, %7, 4;\n\t"
+      "add.s64 a3, %6, 6;\n\tadd.s64 b3, %7, 6;\n\t"
+      "tcgen05.cp.cta_group::2.128x256b [%3], %4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], %6, %7, %8, [%9], [%3], acc0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a1, b1, id1, [%9], [%3], on;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a2, b2, id2, [%9], [%3], on;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], a3, b3, id3, [%9], [%3], on;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%11], %12;\n\t"
+      "selp.u32 %0, 1, 0, full0;\n\t"
+      "}"
+      : "=r"(full)
+      : "r"(nbar), "r"(nphase), "r"(sfb), "l"(sfd), "r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(sfa),
+        "r"(acc_first), "r"(ebar), "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+  return full != 0;
 }
 
 // Two consecutive pipeline stages of the 2-SM block-scaled MMA, issued from one asm

@@ -354,8 +354,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // An even number of K steps per tile keeps every tile (and so every pair of
       // stages) starting on an even stage of the even-length ring: those calls issue
       // two stages per asm block with a look-ahead probe of the next pair's barriers
-      // (tc_mma_stage_pair_mxf8).  `ready` is that probe's answer for the pair about
-      // to be issued; without it the issuer takes the bounded waits.
+      // (tc_mma_stage_pair_mxf8); other calls one stage per block with a probe of the
+      // next stage (tc_mma_stage_mxf8).  `ready` is the probe's answer for what is
+      // about to be issued; when it is false the issuer takes a bounded wait first.
       const bool paired = (p.num_k & 1) == 0;
       static_assert(STAGES % 2 == 0, "stage pairs must not wrap the ring");
       static_assert(A_BYTES == 16384 && B_BYTES == 16384 && SF_BYTES == 4096 && BK == 128,
@@ -383,28 +384,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           stage = nstage;
           phase = nphase;
         }
+        // odd number of K steps: one stage per asm block, with the same look-ahead probe
+        // of the next stage; the scale slot follows the ring position, so consecutive
+        // stages use different slots across tile boundaries too
         for (int kb = 0; !paired && kb < p.num_k; ++kb) {
-          if (!wait_one(full_bar(stage), phase, p.wait_ns, abort_flag)) {
+          if (!ready && !wait_one(full_bar(stage), phase, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sfb = tmem + SFB_COL + (kb & 1) * 8;
-          const uint64_t sfd = sf_desc0 + static_cast<uint64_t>(stage * (SF_BYTES >> 4));
-          tc_cp_pair_128x256b(sfb, sfd);
-          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4));
-          const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4));
-#pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
-            const uint32_t idesc = kIdesc | (uint32_t(kk) << 29) | (uint32_t(kk) << 4);
-            tc_mma_pair_mxf8(tmem + ACC_COL, ad + 2 * kk, bd + 2 * kk, idesc, tmem + SFA_COL, sfb,
-                             (kb | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit_pair_multicast(empty_bar(stage), 0x3);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          const int nstage = stage + 1 == STAGES ? 0 : stage + 1;
+          const uint32_t nphase = nstage == 0 ? phase ^ 1u : phase;
+          ready = tc_mma_stage_mxf8(full_bar(nstage), nphase, tmem + SFB_COL + (stage & 1) * 8,
+                                    sf_desc0 + static_cast<uint64_t>(stage * (SF_BYTES >> 4)), tmem + ACC_COL,
+                                    a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4)),
+                                    b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4)), kIdesc, tmem + SFA_COL,
+                                    kb != 0 ? 1u : 0u, empty_bar(stage));
+          stage = nstage;
+          phase = nphase;
         }
         if (ok) tc_commit_pair_multicast(accf_bar, 0x3);
       }
